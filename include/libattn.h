@@ -1,0 +1,181 @@
+/*
+ * libattn -- multi-head scaled-dot-product attention for NVIDIA GB300 (sm_103a).
+ *
+ * The operation, in every entry point, for each query row i and its admitted
+ * key set K(i):
+ *     S = Q K^T * scale,  P = row softmax(S) over K(i),  O = P V
+ * ("cuBLAS matmuls for ... attention scores" plus a softmax kernel, iris.c
+ * issue #15 "CUDA codepath !"; the windowed score / softmax / accumulate of
+ * candle PR #11's neighborhood attention; the single-token decode attention
+ * over a device-resident KV cache of fak "GPU - the in-kernel forward pass",
+ * sections 0 and 4).
+ *
+ * Conventions shared by all entry points
+ *   - Tensors are DEVICE pointers to contiguous row-major arrays with the head
+ *     dimension innermost.  Attention tensors are heads-major [B, H, N, D].
+ *   - dtype ATTN_F32: float32 storage, exact fp32 FMA arithmetic (no TF32).
+ *     dtype ATTN_BF16: bfloat16 storage; the contractions run on the tensor
+ *     cores (tcgen05) with fp32 accumulation, the softmax in fp32; the output
+ *     is rounded to bf16 (round to nearest even).
+ *   - D (head dimension) is 32, 64 or 128.
+ *   - scale <= 0 selects 1/sqrt(D).
+ *   - Inputs are never written.  The output must not alias any input.
+ *   - The caller owns every buffer.  No entry point allocates device memory
+ *     and none synchronises: work is enqueued on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream) and the call returns.
+ *   - Errors: arguments are validated on the host before any launch; a failed
+ *     check returns ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED /
+ *     ATTN_ERR_RESOURCE and launches nothing.  A launch failure returns
+ *     ATTN_ERR_CUDA.  Device-side waits are bounded: a wait that runs out sets
+ *     a device error word that attn_device_status() reports.  Nothing is
+ *     thrown across this interface.
+ *   - Thread safety: calls may come from several host threads; each call only
+ *     reads its arguments and enqueues work.
+ */
+#ifndef LIBATTN_H
+#define LIBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_F32 = 0,
+    ATTN_BF16 = 1
+} attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, bad kernel, ...       */
+    ATTN_ERR_UNSUPPORTED = 2,   /* valid request this build has no kernel for     */
+    ATTN_ERR_RESOURCE = 3,      /* shared memory / workspace too small            */
+    ATTN_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed           */
+    ATTN_ERR_TIMEOUT = 5,       /* a bounded device wait ran out (device word)    */
+    ATTN_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed         */
+} attn_status_t;
+
+/*
+ * Full (unmasked, non-causal) attention.
+ *   q [B, H, Nq, D], k and v [B, H, Nkv, D], o [B, H, Nq, D]; dtype for all.
+ *   Every query attends to all Nkv keys of its (batch, head).
+ *   Requires B, H, Nq, Nkv >= 1 and D in {32, 64, 128}.
+ * Passage: iris.c issue #15, the reply listing "attention scores" among the
+ * cuBLAS matmuls and softmax among the custom kernels.
+ */
+ATTN_API attn_status_t attn_full_fwd(const void *q, const void *k, const void *v, void *o,
+                            int B, int H, int Nq, int Nkv, int D,
+                            attn_dtype_t dtype, float scale, void *stream);
+
+/*
+ * Joint text+image attention with a multi-axis rotary embedding on Q and K.
+ *   q, k, v, o [B, H, N, D]; N = text + image tokens in the caller's order.
+ *   pos: DEVICE int32 [N, 4], the 4 position ids of each token.
+ *   axes_dim: HOST int[4], channel widths of the 4 axis blocks; each even and
+ *   sum == D.  In the block of axis a starting at channel c_a, the adjacent
+ *   pair (c_a + 2i, c_a + 2i + 1) rotates by phi = pos[t][a] * theta^(-2i/axes_dim[a]):
+ *       x0' = x0 cos(phi) - x1 sin(phi),   x1' = x0 sin(phi) + x1 cos(phi).
+ *   V is not rotated.  Then full attention over all N tokens.
+ *   workspace: DEVICE scratch of at least attn_rope_joint_workspace_bytes(...)
+ *   bytes, 256-byte aligned, that no other call uses concurrently; the rotated
+ *   copies of Q and K (in the storage dtype) live there during the call.
+ * Passage: iris.c issue #15, GGML lessons item 3 (FLUX's custom RoPE: 4 axes
+ * [32,32,32,32], separate text/image positions, repeat_interleave) and the
+ * closing "AdaLN + custom RoPE + joint attention" remark.
+ */
+ATTN_API attn_status_t attn_rope_joint_fwd(const void *q, const void *k, const void *v, void *o,
+                                  int B, int H, int N, int D,
+                                  const int32_t *pos, const int axes_dim[4], float theta,
+                                  attn_dtype_t dtype, float scale,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+ATTN_API size_t attn_rope_joint_workspace_bytes(int B, int H, int N, int D, attn_dtype_t dtype);
+
+/*
+ * Single-token grouped-query decode attention over a KV cache.
+ *   q [B, Hq, D], o [B, Hq, D]; k_cache, v_cache [B, Hkv, Lmax, D].
+ *   seq_len: DEVICE int32 [B], 1 <= seq_len[b] <= Lmax (checked on the device;
+ *   a violation sets ATTN_ERR_DEVICE_CHECK and that batch's output is left
+ *   unwritten).  Query head hq reads KV head hq / (Hq / Hkv) and attends to
+ *   cache rows j < seq_len[b]; rows at or beyond seq_len[b] are never used.
+ *   Requires Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}, D in {64, 128}.
+ *   workspace: DEVICE scratch of attn_decode_gqa_workspace_bytes(...) bytes,
+ *   256-byte aligned, ZERO-FILLED before its first use.  It holds per-split
+ *   partial results and per-(batch, kv-head) arrival counters; every call that
+ *   completes leaves the counters at zero again, so the same workspace serves
+ *   the next call without clearing.  Calls that share a workspace must not
+ *   overlap on the GPU.  After a call that reported a device error, zero it
+ *   again.
+ * Passage: fak "GPU - the in-kernel forward pass", section 0 (device-resident
+ * KV cache) and section 4 (naive decode attention: per-call scratch, one block
+ * per head, no flash/paged attention).
+ */
+ATTN_API attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *seq_len, void *o,
+                              int B, int Hq, int Hkv, int Lmax, int D,
+                              attn_dtype_t dtype, float scale,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+ATTN_API size_t attn_decode_gqa_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
+
+/*
+ * 3D neighborhood attention with NATTEN boundary windows.
+ *   q, k, v, o [B, heads, N, D] with N = T * Hg * W tokens in row-major
+ *   (t, h, w) order.  kernel: HOST int[3], the requested window per axis; each
+ *   must be positive and odd, and may exceed the axis extent.  Per axis of
+ *   extent n and request k: k_eff = min(k, n); query coordinate i attends to
+ *   [s, s + k_eff) with s = clamp(i - k/2, 0, n - k_eff); the 3D window is the
+ *   Cartesian product of the three intervals.  A window at least as wide as
+ *   its axis is full attention along that axis.
+ * Passage: candle PR #11, the "Line-for-line port of neighborhood_attention.metal"
+ * commit and the "kernel exceeds grid extent" commit (effective_kernel() clamp,
+ * validate() only requires a positive odd triple).
+ */
+ATTN_API attn_status_t attn_na3d_fwd(const void *q, const void *k, const void *v, void *o,
+                            int B, int heads, int T, int Hg, int W, int D,
+                            const int kernel[3], attn_dtype_t dtype, float scale,
+                            void *stream);
+
+/*
+ * Window starts as the neighborhood kernels compute them (same device
+ * function), for testing: starts = DEVICE int32 [T*Hg*W, 3], the (t, h, w)
+ * start of each query's window.  Same validation as attn_na3d_fwd.
+ */
+ATTN_API attn_status_t attn_na3d_window_starts(int T, int Hg, int W, const int kernel[3],
+                                      int32_t *starts, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+ATTN_API const char *attn_status_string(attn_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * bounded waits and device-side checks set on the current device.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_CHECK or ATTN_ERR_CUDA.
+ */
+ATTN_API attn_status_t attn_device_status(void *stream);
+
+/*
+ * Number of kernel launches this process has made through the given kernel
+ * family, for tests that must prove the path under test really ran.
+ * ids: 0 = fp32/SIMT flash, 1 = tcgen05 flash, 2 = decode split-KV,
+ *      3 = RoPE prologue, 4 = window-start export, 5 = tcgen05 neighborhood.
+ * Returns 0 for an unknown id.
+ */
+ATTN_API uint64_t attn_launch_count(int kernel_family);
+
+/* Library version string, e.g. "libattn 0.1 sm_103a". */
+ATTN_API const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_H */

@@ -1,0 +1,141 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+and host-side validation rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from transformer_attention_tcgen05_gb300.build import build
+    build()
+    import transformer_attention_tcgen05_gb300 as ta
+    return ta.lib()
+
+
+def _declared():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "attn_full_fwd" in names and "attn_decode_gqa" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_no_undeclared_exports(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", L._name], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    ours = {n for n in exported if n.startswith("attn_")}
+    assert ours == set(_declared()), ours ^ set(_declared())
+
+
+def test_status_strings_and_version(L):
+    L.attn_status_string.restype = ctypes.c_char_p
+    assert L.attn_status_string(0) == b"ok"
+    assert b"invalid" in L.attn_status_string(1)
+    L.attn_version.restype = ctypes.c_char_p
+    assert b"sm_103a" in L.attn_version()
+
+
+def test_workspace_queries_are_host_arithmetic(L):
+    import transformer_attention_tcgen05_gb300 as ta
+    b = ta.decode_workspace_bytes(8, 32, 8, 4096, 128)
+    assert b > 0 and b % 256 == 0
+    assert ta.decode_workspace_bytes(8, 30, 8, 4096, 128) == 0       # Hq % Hkv != 0
+    assert ta.decode_workspace_bytes(1, 32, 2, 4096, 128) == 0       # group of 16 unsupported
+    import torch
+    r = ta.rope_joint_workspace_bytes(1, 24, 4608, 128, torch.bfloat16)
+    assert r >= 2 * 24 * 4608 * 128 * 2 and r % 256 == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: validation fails first
+
+
+def _full(L, *, q=FAKE, o=ctypes.c_void_p(0x20000), B=1, H=1, Nq=8, Nkv=8, D=32, dt=0):
+    L.attn_full_fwd.restype = ctypes.c_int
+    return L.attn_full_fwd(q, FAKE, FAKE, o, B, H, Nq, Nkv, D, dt, ctypes.c_float(0.0), None)
+
+
+def test_full_validation(L):
+    assert _full(L, q=None) == 1
+    assert _full(L, q=ctypes.c_void_p(0x10004)) == 1      # misaligned
+    assert _full(L, D=48) == 1
+    assert _full(L, Nq=0) == 1
+    assert _full(L, dt=7) == 1
+    assert _full(L, o=FAKE) == 1                         # output aliases an input
+
+
+def test_na3d_validation(L):
+    L.attn_na3d_fwd.restype = ctypes.c_int
+    o = ctypes.c_void_p(0x20000)
+    for kern in ([3, 4, 3], [0, 3, 3], [-1, 3, 3]):       # even / zero / negative
+        k = (ctypes.c_int * 3)(*kern)
+        assert L.attn_na3d_fwd(FAKE, FAKE, FAKE, o, 1, 1, 2, 4, 4, 32, k, 0,
+                               ctypes.c_float(0.0), None) == 1
+    k = (ctypes.c_int * 3)(3, 3, 3)
+    assert L.attn_na3d_fwd(FAKE, FAKE, FAKE, o, 1, 1, 0, 4, 4, 32, k, 0,
+                           ctypes.c_float(0.0), None) == 1
+
+
+def test_decode_validation(L):
+    L.attn_decode_gqa.restype = ctypes.c_int
+    o = ctypes.c_void_p(0x20000)
+    ws = ctypes.c_void_p(0x40000)
+    f = ctypes.c_float(0.0)
+    # Hq % Hkv != 0
+    assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 6, 4, 64, 128, 1, f, ws, 1 << 20, None) == 1
+    # fp32 decode is not built (bf16 only)
+    assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 0, f, ws, 1 << 20, None) == 2
+    # workspace too small
+    assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 1, f, ws, 16, None) == 3
+    # misaligned workspace
+    assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 1, f,
+                             ctypes.c_void_p(0x40010), 1 << 20, None) == 1
+
+
+def test_rope_validation(L):
+    L.attn_rope_joint_fwd.restype = ctypes.c_int
+    o = ctypes.c_void_p(0x20000)
+    ws = ctypes.c_void_p(0x40000)
+    f = ctypes.c_float(0.0)
+    bad = [(32, 32, 32, 30), (33, 31, 32, 32), (32, 32, 32, 33)]
+    for ax in bad:
+        a = (ctypes.c_int * 4)(*ax)
+        assert L.attn_rope_joint_fwd(FAKE, FAKE, FAKE, o, 1, 2, 16, 128, FAKE, a,
+                                     ctypes.c_float(1e4), 1, f, ws, 1 << 20, None) == 1
+    a = (ctypes.c_int * 4)(32, 32, 32, 32)
+    assert L.attn_rope_joint_fwd(FAKE, FAKE, FAKE, o, 1, 2, 16, 128, FAKE, a,
+                                 ctypes.c_float(-1.0), 1, f, ws, 1 << 20, None) == 1   # theta
+    assert L.attn_rope_joint_fwd(FAKE, FAKE, FAKE, o, 1, 2, 16, 128, FAKE, a,
+                                 ctypes.c_float(1e4), 1, f, ws, 64, None) == 3         # workspace
+
+
+def test_launch_counter_unknown_family(L):
+    L.attn_launch_count.restype = ctypes.c_uint64
+    assert L.attn_launch_count(99) == 0
+    assert L.attn_launch_count(-1) == 0
+
+
+def test_product_path_does_not_import_oracle():
+    import subprocess
+    import sys
+    code = ("import sys, transformer_attention_tcgen05_gb300 as ta; "
+            "assert not any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules), 'oracle imported'")
+    subprocess.run([sys.executable, "-c", code], cwd=ROOT, check=True)
+    for fn in os.listdir(os.path.join(ROOT, "transformer_attention_tcgen05_gb300")):
+        if fn.endswith(".py"):
+            src = open(os.path.join(ROOT, "transformer_attention_tcgen05_gb300", fn)).read()
+            assert "import oracle" not in src and "from oracle" not in src, fn

@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on
+the same seeded host arrays, element by element.
+
+Every test also checks, through the library's launch counters, that the
+kernel family under test really ran (no silent detour).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.util import assert_close, errors, to_dev, to_host64
+from workloads import WORKLOADS, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ta():
+    import torch
+    from transformer_attention_tcgen05_gb300.build import build
+    build()
+    import transformer_attention_tcgen05_gb300 as ta
+    torch.cuda.set_device(0)
+    return ta
+
+
+class launched:
+    """Context manager asserting that a kernel family launched inside it."""
+
+    def __init__(self, ta, family):
+        self.ta, self.family = ta, family
+
+    def __enter__(self):
+        self.n0 = self.ta.launch_count(self.family)
+        return self
+
+    def __exit__(self, *exc):
+        if exc[0] is None:
+            assert self.ta.launch_count(self.family) > self.n0, f"{self.family} did not launch"
+
+
+def _dev(x, w, names="qkv"):
+    return [to_dev(x[n], w.dtype) for n in names]
+
+
+def _f64(x, w, names="qkv"):
+    return [to_f64(x[n], w.dtype) for n in names]
+
+
+# ------------------------------------------------------------ full attention
+
+def test_mha_tiny_fp32(ta):
+    w = WORKLOADS["mha_tiny"]
+    x = make_inputs(w)
+    with launched(ta, "simt"):
+        o = ta.full_fwd(*_dev(x, w))
+    ref = oracle.full_fwd(*_f64(x, w))
+    assert_close(to_host64(o), ref, "f32", "mha_tiny")
+    assert ta.device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H,Nq,Nkv,D", [
+    (1, 1, 1, 1, 32), (2, 3, 17, 33, 32), (1, 2, 130, 257, 64), (1, 2, 200, 129, 128),
+    (2, 1, 64, 1000, 128), (1, 1, 257, 255, 64),
+])
+def test_full_shapes(ta, dtype, B, H, Nq, Nkv, D):
+    rng = np.random.Generator(np.random.PCG64(7000 + Nq + Nkv + D))
+    from workloads import draw
+    q = draw(rng, (B, H, Nq, D), dtype)
+    k = draw(rng, (B, H, Nkv, D), dtype)
+    v = draw(rng, (B, H, Nkv, D), dtype)
+    o = ta.full_fwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype))
+    ref = oracle.full_fwd(to_f64(q, dtype), to_f64(k, dtype), to_f64(v, dtype))
+    assert_close(to_host64(o), ref, dtype, f"full {dtype} {B,H,Nq,Nkv,D}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_full_sharp_rows(ta, dtype):
+    # Q x 8: peaked rows exercise the running-max rescale
+    rng = np.random.Generator(np.random.PCG64(7100))
+    from workloads import bf16_round
+    q = rng.standard_normal((1, 2, 300, 64), dtype=np.float32) * 8
+    k = rng.standard_normal((1, 2, 700, 64), dtype=np.float32)
+    v = rng.standard_normal((1, 2, 700, 64), dtype=np.float32)
+    if dtype == "bf16":
+        q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
+    o = ta.full_fwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype))
+    ref = oracle.full_fwd(to_f64(q, dtype), to_f64(k, dtype), to_f64(v, dtype))
+    assert_close(to_host64(o), ref, dtype, f"sharp {dtype}")
+
+
+def test_explicit_scale_and_determinism(ta):
+    import torch
+    w = WORKLOADS["mha_tiny"]
+    x = make_inputs(w)
+    q, k, v = _dev(x, w)
+    o1 = ta.full_fwd(q, k, v, scale=0.05)
+    o2 = ta.full_fwd(q, k, v, scale=0.05)
+    assert torch.equal(o1, o2)
+    ref = oracle.full_fwd(*_f64(x, w), scale=0.05)
+    assert_close(to_host64(o1), ref, "f32", "scale 0.05")
+
+
+def test_output_guard_bands_untouched(ta):
+    import torch
+    w = WORKLOADS["mha_tiny"]
+    x = make_inputs(w)
+    q, k, v = _dev(x, w)
+    n = q.numel()
+    buf = torch.full((n + 2048,), 12345.0, device=q.device)
+    o = buf[1024:1024 + n].view(q.shape)
+    ta.full_fwd(q, k, v, o=o)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:1024] == 12345.0) and torch.all(buf[1024 + n:] == 12345.0)
+
+
+# ----------------------------------------------------- neighborhood attention
+
+NA_SMALL = ["na3d_1x4x4_k3x7x7_f32", "na3d_1x4x4_k3x7x7_bf16",
+            "na3d_9x64x64_k11_f32", "na3d_9x64x64_k11_bf16"]
+
+
+@pytest.mark.parametrize("name", NA_SMALL)
+def test_na3d_clamp_cases_full_compare(ta, name):
+    w = WORKLOADS[name]
+    x = make_inputs(w)
+    o = ta.na3d_fwd(*_dev(x, w), w.grid, w.kernel)
+    ref = oracle.na3d_fwd(*_f64(x, w), w.grid, w.kernel)
+    assert_close(to_host64(o), ref, w.dtype, name)
+    assert ta.device_status() == 0
+
+
+def test_na3d_kernel_covering_grid_is_full_attention(ta):
+    # the [1,4,4] / k[3,7,7] case: every query attends to all 16 tokens
+    w = WORKLOADS["na3d_1x4x4_k3x7x7_f32"]
+    x = make_inputs(w)
+    q, k, v = _dev(x, w)
+    o_na = to_host64(ta.na3d_fwd(q, k, v, w.grid, w.kernel))
+    o_full = to_host64(ta.full_fwd(q, k, v))
+    np.testing.assert_allclose(o_na, o_full, rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("grid,kernel", [
+    ((1, 4, 4), (3, 7, 7)), ((9, 64, 64), (11, 11, 11)), ((21, 60, 104), (11, 11, 11)),
+    ((5, 7, 3), (3, 9, 1)), ((2, 13, 17), (5, 5, 7)),
+])
+def test_window_starts_bit_exact(ta, grid, kernel):
+    with launched(ta, "na_starts"):
+        st = ta.na3d_window_starts(grid, kernel).cpu().numpy()
+    np.testing.assert_array_equal(st, oracle.na3d_window_starts(grid, kernel))
+
+
+def test_window_sets_through_the_kernel(ta):
+    # black-box probe: Q = 0 makes every output the mean of V over the window;
+    # V channels carry (t, h, w, t^2, h^2, w^2, 1): mean and second moment per
+    # axis identify each query's interval exactly (small integers, exact fp32)
+    import itertools
+    grid, kernel = (6, 20, 24), (3, 7, 11)
+    T, Hg, W = grid
+    N = T * Hg * W
+    c = np.array(list(itertools.product(range(T), range(Hg), range(W))), dtype=np.float32)
+    v = np.zeros((1, 1, N, 32), dtype=np.float32)
+    v[0, 0, :, 0:3] = c
+    v[0, 0, :, 3:6] = c ** 2
+    v[0, 0, :, 6] = 1
+    q = np.zeros_like(v)
+    k = np.random.Generator(np.random.PCG64(7200)).standard_normal(v.shape, dtype=np.float32)
+    o = to_host64(ta.na3d_fwd(to_dev(q, "f32"), to_dev(k, "f32"), to_dev(v, "f32"), grid, kernel))[0, 0]
+    st = oracle.na3d_window_starts(grid, kernel)
+    for ax, n in enumerate(grid):
+        keff = min(kernel[ax], n)
+        lo = st[:, ax].astype(np.float64)
+        mean = lo + (keff - 1) / 2
+        m2 = np.array([np.mean(np.arange(a, a + keff) ** 2) for a in st[:, ax]])
+        np.testing.assert_allclose(o[:, ax], mean, rtol=0, atol=1e-4)
+        np.testing.assert_allclose(o[:, 3 + ax], m2, rtol=2e-6, atol=1e-3)
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode_case(ta, w, check=True):
+    import torch
+    x = make_inputs(w)
+    q, k, v = to_dev(x["q"], "bf16"), to_dev(x["k"], "bf16"), to_dev(x["v"], "bf16")
+    sl = torch.from_numpy(x["seq_len"]).cuda()
+    with launched(ta, "decode"):
+        o = ta.decode_gqa(q, k, v, sl)
+    ref = oracle.decode_gqa(to_f64(x["q"], "bf16"), to_f64(x["k"], "bf16"), to_f64(x["v"], "bf16"),
+                            x["seq_len"])
+    return assert_close(to_host64(o), ref, "bf16", f"decode {w}")
+
+
+def test_decode_workload_full_size(ta):
+    _decode_case(ta, WORKLOADS["gqa_decode"])
+    assert ta.device_status() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 128), (16, 8, 128), (12, 4, 64), (32, 4, 128),
+                                      (9, 3, 64), (6, 1, 64)])
+def test_decode_groups_and_ragged_lengths(ta, Hq, Hkv, D):
+    w = WORKLOADS["gqa_decode"].with_(B=3, H=Hq, Hkv=Hkv, D=D, Lmax=777, seq_len=(1, 777, 300),
+                                      seed=7300 + Hq + D)
+    _decode_case(ta, w)
+
+
+def test_decode_workspace_is_reusable_and_deterministic(ta):
+    import torch
+    w = WORKLOADS["gqa_decode"].with_(B=2, Lmax=1000, seq_len=(1000, 513))
+    x = make_inputs(w)
+    q, k, v = to_dev(x["q"], "bf16"), to_dev(x["k"], "bf16"), to_dev(x["v"], "bf16")
+    sl = torch.from_numpy(x["seq_len"]).cuda()
+    ws = torch.zeros(ta.decode_workspace_bytes(2, 32, 8, 1000, 128), dtype=torch.uint8, device="cuda")
+    o1 = ta.decode_gqa(q, k, v, sl, workspace=ws)
+    o2 = ta.decode_gqa(q, k, v, sl, workspace=ws)
+    assert torch.equal(o1, o2)
+    ref = oracle.decode_gqa(to_f64(x["q"], "bf16"), to_f64(x["k"], "bf16"), to_f64(x["v"], "bf16"),
+                            x["seq_len"])
+    assert_close(to_host64(o2), ref, "bf16", "decode reuse")
+
+
+def test_decode_rejects_bad_seq_len_on_device(ta):
+    import torch
+    w = WORKLOADS["gqa_decode"].with_(B=2, Lmax=128)
+    x = make_inputs(w)
+    q, k, v = to_dev(x["q"], "bf16"), to_dev(x["k"], "bf16"), to_dev(x["v"], "bf16")
+    sl = torch.tensor([128, 129], dtype=torch.int32, device="cuda")   # 129 > Lmax
+    assert ta.device_status() == 0
+    ta.decode_gqa(q, k, v, sl)
+    assert ta.device_status() == 6          # ATTN_ERR_DEVICE_CHECK, context still usable
+    assert ta.device_status() == 0          # cleared by the read
+    _decode_case(ta, w.with_(seq_len=(128, 5)))
+
+
+# ------------------------------------------------------------ joint + RoPE
+
+def test_joint_small_full_compare(ta):
+    import torch
+    w = WORKLOADS["flux_joint"].with_(H=3, N=96 + 12 * 20, n_txt=96, img=(12, 20))
+    x = make_inputs(w)
+    pos = torch.from_numpy(x["pos"]).cuda()
+    with launched(ta, "rope"):
+        o = ta.rope_joint_fwd(*_dev(x, w), pos)
+    ref = oracle.joint_fwd(*_f64(x, w), x["pos"])
+    assert_close(to_host64(o), ref, "bf16", "joint small")
+
+
+def test_joint_fp32_full_compare(ta):
+    import torch
+    w = WORKLOADS["flux_joint"].with_(dtype="f32", H=2, N=40 + 8 * 9, n_txt=40, img=(8, 9))
+    x = make_inputs(w)
+    pos = torch.from_numpy(x["pos"]).cuda()
+    o = ta.rope_joint_fwd(*_dev(x, w), pos)
+    ref = oracle.joint_fwd(*_f64(x, w), x["pos"])
+    assert_close(to_host64(o), ref, "f32", "joint fp32")

@@ -1,0 +1,236 @@
+"""Python binding of libattn (include/libattn.h) -- argument marshalling only.
+
+Every step of the attention path runs in the CUDA library; this module checks
+tensor arguments, allocates outputs with PyTorch (PyTorch provides device
+memory and streams, nothing else) and calls the C ABI through ctypes on the
+current CUDA stream.  There is no fallback: if the library is not built, or
+the tensors are not on a CUDA device, calls raise.
+
+Entry points (names as in the C ABI, without the ``attn_`` prefix):
+    full_fwd(q, k, v)                          q, k, v [B, H, N, D]
+    rope_joint_fwd(q, k, v, pos, axes_dim, theta)
+    decode_gqa(q, k_cache, v_cache, seq_len)   q [B, Hq, D], caches [B, Hkv, Lmax, D]
+    na3d_fwd(q, k, v, grid, kernel)            q, k, v [B, heads, T*Hg*W, D]
+    na3d_window_starts(grid, kernel)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "AttnError", "lib", "full_fwd", "rope_joint_fwd", "decode_gqa", "na3d_fwd",
+    "na3d_window_starts", "decode_workspace_bytes", "rope_joint_workspace_bytes",
+    "device_status", "launch_count", "version", "FAMILIES", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libattn.so")
+
+ATTN_F32, ATTN_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+          3: "insufficient resources", 4: "CUDA error", 5: "device wait timed out",
+          6: "device-side check failed"}
+#: kernel families of attn_launch_count
+FAMILIES = {"simt": 0, "tc_flash": 1, "decode": 2, "rope": 3, "na_starts": 4, "tc_na": 5}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, 'unknown status')} (status {status})")
+
+
+_lib = None
+_vp, _i, _f, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libattn is not built ({LIB_PATH} missing): run "
+                               "`python -m transformer_attention_tcgen05_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.attn_full_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+        L.attn_rope_joint_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp,
+                                          ctypes.POINTER(_i), _f, _i, _f, _vp, _sz, _vp]
+        L.attn_rope_joint_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        L.attn_rope_joint_workspace_bytes.restype = _sz
+        L.attn_decode_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp,
+                                      _sz, _vp]
+        L.attn_decode_gqa_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        L.attn_decode_gqa_workspace_bytes.restype = _sz
+        L.attn_na3d_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                    ctypes.POINTER(_i), _i, _f, _vp]
+        L.attn_na3d_window_starts.argtypes = [_i, _i, _i, ctypes.POINTER(_i), _vp, _vp]
+        L.attn_status_string.argtypes = [_i]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_device_status.argtypes = [_vp]
+        L.attn_launch_count.argtypes = [_i]
+        L.attn_launch_count.restype = _u64
+        L.attn_version.restype = ctypes.c_char_p
+        for name in ("attn_full_fwd", "attn_rope_joint_fwd", "attn_decode_gqa", "attn_na3d_fwd",
+                     "attn_na3d_window_starts", "attn_device_status"):
+            getattr(L, name).restype = _i
+        _lib = L
+    return _lib
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise AttnError(st, where)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _cuda(*ts: torch.Tensor):
+    dev = ts[0].device
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("libattn tensors must be on a CUDA device")
+        if t.device != dev:
+            raise ValueError("all tensors must be on the same device")
+        if not t.is_contiguous():
+            raise ValueError("libattn tensors must be contiguous")
+    return dev
+
+
+def _stream(dev) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ints(vals: Sequence[int], n: int):
+    vals = [int(x) for x in vals]
+    if len(vals) != n:
+        raise ValueError(f"expected {n} integers, got {len(vals)}")
+    return (_i * n)(*vals)
+
+
+def _scale(scale: Optional[float]) -> float:
+    return 0.0 if scale is None else float(scale)
+
+
+def full_fwd(q, k, v, o=None, scale=None):
+    """Full attention; q [B,H,Nq,D], k/v [B,H,Nkv,D] -> o [B,H,Nq,D]."""
+    dev = _cuda(q, k, v)
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    if k.shape != (B, H, Nkv, D) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k/v must be [B, H, Nkv, D] with q's dtype")
+    o = torch.empty_like(q) if o is None else o
+    _cuda(q, o)
+    with torch.cuda.device(dev):
+        _check(lib().attn_full_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   B, H, Nq, Nkv, D, _dtype(q), _scale(scale), _stream(dev)),
+               "attn_full_fwd")
+    return o
+
+
+def rope_joint_workspace_bytes(B, H, N, D, dtype) -> int:
+    return int(lib().attn_rope_joint_workspace_bytes(B, H, N, D, _dtype(torch.empty(0, dtype=dtype))))
+
+
+def rope_joint_fwd(q, k, v, pos, axes_dim=(32, 32, 32, 32), theta=10000.0, o=None, scale=None,
+                   workspace=None):
+    """Multi-axis RoPE on q/k (positions pos [N,4] int32), then full attention."""
+    dev = _cuda(q, k, v, pos)
+    B, H, N, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or pos.shape != (N, 4) or pos.dtype != torch.int32:
+        raise ValueError("q/k/v [B,H,N,D] and pos int32 [N,4] required")
+    o = torch.empty_like(q) if o is None else o
+    need = rope_joint_workspace_bytes(B, H, N, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _cuda(q, o, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().attn_rope_joint_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         B, H, N, D, pos.data_ptr(), _ints(axes_dim, 4),
+                                         float(theta), _dtype(q), _scale(scale),
+                                         workspace.data_ptr(), workspace.numel(), _stream(dev)),
+               "attn_rope_joint_fwd")
+    return o
+
+
+def decode_workspace_bytes(B, Hq, Hkv, Lmax, D) -> int:
+    return int(lib().attn_decode_gqa_workspace_bytes(B, Hq, Hkv, Lmax, D))
+
+
+def decode_gqa(q, k_cache, v_cache, seq_len, o=None, scale=None, workspace=None):
+    """GQA decode: q [B,Hq,D], caches [B,Hkv,Lmax,D], seq_len int32 [B] -> o [B,Hq,D].
+
+    ``workspace`` (uint8, decode_workspace_bytes(...) bytes) must be zero-filled
+    before its first use; calls leave it reusable.  If omitted a zeroed one is
+    allocated for this call.
+    """
+    dev = _cuda(q, k_cache, v_cache, seq_len)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    if k_cache.shape != (B, Hkv, Lmax, D) or v_cache.shape != k_cache.shape or \
+            seq_len.shape != (B,) or seq_len.dtype != torch.int32:
+        raise ValueError("caches [B,Hkv,Lmax,D] and seq_len int32 [B] required")
+    o = torch.empty_like(q) if o is None else o
+    need = decode_workspace_bytes(B, Hq, Hkv, Lmax, D)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    _cuda(q, o, workspace)
+    with torch.cuda.device(dev):
+        _check(lib().attn_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     seq_len.data_ptr(), o.data_ptr(), B, Hq, Hkv, Lmax, D,
+                                     _dtype(q), _scale(scale), workspace.data_ptr(),
+                                     workspace.numel(), _stream(dev)),
+               "attn_decode_gqa")
+    return o
+
+
+def na3d_fwd(q, k, v, grid, kernel, o=None, scale=None):
+    """3D neighborhood attention; q/k/v [B, heads, T*Hg*W, D]."""
+    dev = _cuda(q, k, v)
+    B, Hh, N, D = q.shape
+    T, Hg, W = (int(x) for x in grid)
+    if N != T * Hg * W or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q/k/v must be [B, heads, T*Hg*W, D]")
+    o = torch.empty_like(q) if o is None else o
+    _cuda(q, o)
+    with torch.cuda.device(dev):
+        _check(lib().attn_na3d_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   B, Hh, T, Hg, W, D, _ints(kernel, 3), _dtype(q),
+                                   _scale(scale), _stream(dev)),
+               "attn_na3d_fwd")
+    return o
+
+
+def na3d_window_starts(grid, kernel, device=None):
+    """int32 [T*Hg*W, 3] window starts from the kernels' own device function."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    T, Hg, W = (int(x) for x in grid)
+    out = torch.empty((T * Hg * W, 3), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().attn_na3d_window_starts(T, Hg, W, _ints(kernel, 3), out.data_ptr(),
+                                             _stream(dev)),
+               "attn_na3d_window_starts")
+    return out
+
+
+def device_status(device=None) -> int:
+    """Syncs the current stream and returns (and clears) the device error status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().attn_device_status(_stream(dev)))
+
+
+def launch_count(family: str) -> int:
+    return int(lib().attn_launch_count(FAMILIES[family]))
+
+
+def version() -> str:
+    return lib().attn_version().decode()

@@ -1,0 +1,67 @@
+// Host-side launchers of libattn's kernels (internal; the public ABI is include/libattn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "libattn.h"
+
+namespace attn {
+
+struct Ctx {
+    cudaStream_t stream;
+    unsigned *err;      // device error word of the current device
+    int device;
+    int sm_count;
+};
+
+enum KernelFamily : int {
+    kFamSimt = 0,
+    kFamTcFlash = 1,
+    kFamDecode = 2,
+    kFamRope = 3,
+    kFamNaStarts = 4,
+    kFamTcNa = 5,
+    kFamCount = 6,
+};
+
+void count_launch(int family);
+
+// Converts the result of a launch into a status (and counts it on success).
+attn_status_t launch_status(int family);
+
+// Sets the dynamic shared-memory limit of `func` once per device.
+bool ensure_smem_attr(const void *func, size_t bytes, int device, int *done_mask);
+
+// fp32 / generic SIMT flash attention (exact FFMA for fp32 storage).
+attn_status_t simt_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                        const void *v, void *o, int B, int H, int Nq, int Nkv, int D,
+                        float scale);
+attn_status_t simt_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                        const void *v, void *o, int B, int H, int T, int Hg, int W, int D,
+                        const int kernel[3], float scale);
+attn_status_t na_starts(const Ctx &c, int T, int Hg, int W, const int kernel[3],
+                        int32_t *starts);
+
+// RoPE prologue: rotated copies of q and k into qr / kr (same dtype).
+attn_status_t rope_rotate_qk(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                             void *qr, void *kr, int BH, int N, int D, const int32_t *pos,
+                             const int axes_dim[4], float theta);
+
+// Split-KV GQA decode (bf16).
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
+attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void *v,
+                         const int32_t *seq_len, void *o, int B, int Hq, int Hkv, int Lmax,
+                         int D, float scale, void *ws, size_t ws_bytes);
+
+// tcgen05 (tensor-core) flash attention, bf16: full and neighborhood.
+attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v, void *o,
+                      int B, int H, int Nq, int Nkv, int D, float scale);
+bool tc_full_supported(int B, int H, int Nq, int Nkv, int D);
+attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v, void *o,
+                      int B, int H, int T, int Hg, int W, int D, const int kernel[3],
+                      float scale);
+bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]);
+
+}  // namespace attn

@@ -1,0 +1,428 @@
+"""Throughput of the attention hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. FLUX joint text+image attention with 4-axis RoPE (512 text + 4096 image
+     tokens, 24 heads, D 128, bf16)                      -> attn_rope_joint_fwd
+  2. 3D neighborhood attention, grid [21, 60, 104], kernel [11, 11, 11],
+     8 heads, D 64, bf16                                  -> attn_na3d_fwd
+  3. Llama-style GQA decode, B 8, Hq 32, Hkv 8, D 128, bf16 KV cache of
+     4096 rows per sequence                               -> attn_decode_gqa
+
+value = algorithmic FLOPs of the step (4*N^2*H*D + 4*N*heads*window*D +
+4*B*Hq*L*D; masked or padded work never counted) / device time per step.
+The per-kernel breakdown reports the decode path as KV-read GB/s as well.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs the same step on its own GPU
+(replicas; the path needs no exchange between GPUs), "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_inputs, to_f64  # noqa: E402
+
+METRIC = "attention TFLOP/s and decode KV-read GB/s on 1×GB300, % of roofline"
+WL_JOINT, WL_NA, WL_DEC = WORKLOADS["flux_joint"], WORKLOADS["na3d_21x60x104_k11"], WORKLOADS["gqa_decode"]
+
+
+def flops_joint(w=WL_JOINT):
+    return 4.0 * w.B * w.H * w.N * w.N * w.D
+
+
+def na_window(w=WL_NA):
+    return int(np.prod([min(k, n) for k, n in zip(w.kernel, w.grid)]))
+
+
+def flops_na(w=WL_NA):
+    return 4.0 * w.B * w.H * w.N * na_window(w) * w.D
+
+
+def flops_dec(w=WL_DEC):
+    return 4.0 * w.B * w.H * w.Lmax * w.D
+
+
+def bytes_dec(w=WL_DEC):
+    # algorithmic bytes: the K and V cache rows read once, plus q in and o out
+    return 2.0 * w.B * w.Hkv * w.Lmax * w.D * 2 + 2.0 * w.B * w.H * w.D * 2
+
+
+STEP_FLOPS = flops_joint() + flops_na() + flops_dec()
+CONFIG = {
+    "workload": "flux_joint_rope_4608x24x128 + na3d_21x60x104_k11x11x11_h8_d64 + "
+                "gqa_decode_b8_hq32_hkv8_l4096_d128",
+    "dtype_inputs": "bf16",
+    "step_gflop_algorithmic": round(STEP_FLOPS / 1e9, 3),
+    "decode_kv_bytes": int(bytes_dec()),
+    "l2": "inputs larger than L2: each kernel's operands (113 MB joint incl. rotated copies, "
+          "537 MB neighborhood, 134 MB decode cache) cycle through the 126 MB L2 between "
+          "its successive launches",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- our arm
+
+def to_dev(x, dtype, dev):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+
+class Step:
+    """Resident inputs, outputs and workspaces of one step on one GPU."""
+
+    def __init__(self, ta, dev):
+        import torch
+        self.ta, self.dev = ta, dev
+        self.host = {"joint": make_inputs(WL_JOINT), "na": make_inputs(WL_NA), "dec": make_inputs(WL_DEC)}
+        hj, hn, hd = self.host["joint"], self.host["na"], self.host["dec"]
+        self.j = [to_dev(hj[n], "bf16", dev) for n in "qkv"]
+        self.jpos = torch.from_numpy(hj["pos"]).to(dev)
+        self.jo = torch.empty_like(self.j[0])
+        w = WL_JOINT
+        self.jws = torch.empty(ta.rope_joint_workspace_bytes(w.B, w.H, w.N, w.D, torch.bfloat16),
+                               dtype=torch.uint8, device=dev)
+        self.n = [to_dev(hn[n], "bf16", dev) for n in "qkv"]
+        self.no = torch.empty_like(self.n[0])
+        self.d = [to_dev(hd[n], "bf16", dev) for n in "qkv"]
+        self.dsl = torch.from_numpy(hd["seq_len"]).to(dev)
+        self.do = torch.empty_like(self.d[0])
+        w = WL_DEC
+        self.dws = torch.zeros(ta.decode_workspace_bytes(w.B, w.H, w.Hkv, w.Lmax, w.D),
+                               dtype=torch.uint8, device=dev)
+
+    def run(self, ev=None):
+        ta = self.ta
+        if ev: ev[0].record()
+        ta.rope_joint_fwd(*self.j, self.jpos, WL_JOINT.axes_dim, WL_JOINT.theta, o=self.jo,
+                          workspace=self.jws)
+        if ev: ev[1].record()
+        ta.na3d_fwd(*self.n, WL_NA.grid, WL_NA.kernel, o=self.no)
+        if ev: ev[2].record()
+        ta.decode_gqa(*self.d, self.dsl, o=self.do, workspace=self.dws)
+        if ev: ev[3].record()
+
+    def launches(self):
+        return sum(self.ta.launch_count(f) for f in self.ta.FAMILIES)
+
+
+class E2EStep:
+    """The same step through the public API with host buffers: pinned host
+    inputs copied in, outputs copied back, inside the timed region."""
+
+    def __init__(self, step: Step):
+        import torch
+        self.s = step
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+        self.h_in = [(pin(t), t) for t in step.j + [step.jpos] + step.n + step.d + [step.dsl]]
+        self.h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t)
+                      for t in (step.jo, step.no, step.do)]
+        self.h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
+        self.d2h = sum(h.numel() * h.element_size() for h, _ in self.h_out)
+
+    def run(self):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.s.run()
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+
+
+def ours(args, rank, world, dev_index):
+    import torch
+    import transformer_attention_tcgen05_gb300 as ta
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    ta.lib()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    step = Step(ta, dev)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert ta.device_status() == 0
+
+    # ---- timed region: K steps, per-kernel events inside each step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev_index)
+    clocks.start()
+    if dist: dist.barrier()
+    torch.cuda.synchronize()
+    n0 = step.launches()
+    start.record()
+    for i in range(args.steps):
+        step.run(evs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    n1 = step.launches()
+    if dist: dist.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(stop) / args.steps
+    kt = {"joint": [], "na": [], "decode": []}
+    for e in evs:
+        kt["joint"].append(e[0].elapsed_time(e[1]))
+        kt["na"].append(e[1].elapsed_time(e[2]))
+        kt["decode"].append(e[2].elapsed_time(e[3]))
+    kms = {k: statistics.mean(v) for k, v in kt.items()}
+    assert ta.device_status() == 0
+
+    # ---- end to end through the API with host buffers
+    e2e = E2EStep(step)
+    for _ in range(max(1, args.warmup // 2)):
+        e2e.run()
+    torch.cuda.synchronize()
+    if dist: dist.barrier()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, args.steps // 3)
+    e_start.record()
+    for _ in range(e_steps):
+        e2e.run()
+    e_stop.record()
+    torch.cuda.synchronize()
+    e_ms = e_start.elapsed_time(e_stop) / e_steps
+
+    if dist:
+        t = torch.tensor([ms, e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        if dist: dist.destroy_process_group()
+        return None
+
+    tflops = STEP_FLOPS * world / (ms * 1e-3) / 1e12
+    comp = {
+        "joint": {"ms": kms["joint"], "tflops": flops_joint() / (kms["joint"] * 1e-3) / 1e12},
+        "na3d": {"ms": kms["na"], "tflops": flops_na() / (kms["na"] * 1e-3) / 1e12},
+        "decode": {"ms": kms["decode"], "tflops": flops_dec() / (kms["decode"] * 1e-3) / 1e12,
+                   "kv_gbs": bytes_dec() / (kms["decode"] * 1e-3) / 1e9},
+    }
+    for k in ("joint", "na3d"):
+        comp[k]["frac_of_bf16_peak"] = comp[k]["tflops"] / peaks["bf16"]
+    comp["decode"]["frac_of_hbm"] = comp["decode"]["kv_gbs"] / peaks["hbm"]
+    comp["decode"]["frac_of_8tbs"] = comp["decode"]["kv_gbs"] / 8000.0
+    dom = max(("joint", "na3d", "decode"), key=lambda k: comp[k]["ms"])
+    traffic = load_traffic(dom)
+    if dom == "decode":
+        roof = {"bound": "hbm", "achieved": comp[dom]["kv_gbs"], "peak": peaks["hbm"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": comp[dom]["tflops"], "peak": peaks["bf16"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peaks['src']} (burst; kernel timed inside a step of {ms:.2f} ms)"
+    line = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16)", "config": CONFIG,
+        "components": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in comp.items()},
+        "roofline": roof,
+        "e2e": {"value": round(STEP_FLOPS * world / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": e2e.h2d,
+                "d2h_bytes_per_step": e2e.d2h},
+        "gpu_launches": int(n1 - n0),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(step.host, budget_s=args.cpu_budget)
+    if dist: dist.destroy_process_group()
+    return line
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        return d.get(kernel, {}).get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class CpuSample:
+    """The fp64 oracle, as it stands, on this host's cores, on a bounded
+    sample of the same step: a seeded sample of query rows of the joint and
+    neighborhood workloads plus every decode row, timed, and scaled to
+    TFLOP/s by the algorithmic FLOPs of the rows computed."""
+
+    def __init__(self, host):
+        import oracle
+        self.oracle = oracle
+        hj, hn, hd = host["joint"], host["na"], host["dec"]
+        self.j = [to_f64(hj[n], "bf16") for n in "qkv"]
+        self.pos = hj["pos"]
+        self.n = [to_f64(hn[n], "bf16") for n in "qkv"]
+        self.d = [to_f64(hd[n], "bf16") for n in "qkv"]
+        self.sl = hd["seq_len"]
+        self.rows_j = WL_JOINT.B * WL_JOINT.H * WL_JOINT.N
+        self.rows_n = WL_NA.B * WL_NA.H * WL_NA.N
+        self.rng = np.random.default_rng(0)
+        self.frac = None
+
+    def run(self, frac):
+        o = self.oracle
+        rj = np.sort(self.rng.choice(self.rows_j, max(1, int(self.rows_j * frac)), replace=False))
+        rn = np.sort(self.rng.choice(self.rows_n, max(1, int(self.rows_n * frac)), replace=False))
+        t0 = time.perf_counter()
+        o.joint_fwd(*self.j, self.pos, WL_JOINT.axes_dim, WL_JOINT.theta, rows=rj)
+        o.na3d_fwd(*self.n, WL_NA.grid, WL_NA.kernel, rows=rn)
+        o.decode_gqa(*self.d, self.sl)
+        dt = time.perf_counter() - t0
+        fl = (flops_joint() * len(rj) / self.rows_j + flops_na() * len(rn) / self.rows_n +
+              flops_dec())
+        return dt, fl, len(rj), len(rn)
+
+    def measure(self, budget_s):
+        if self.frac is None:
+            dt, _, _, _ = self.run(0.001)                  # calibrate the sample size
+            self.frac = min(1.0, 0.001 * budget_s / max(dt, 1e-3))
+        dt, fl, nj, nn = self.run(self.frac)
+        return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s",
+                "cores": self.oracle.max_threads(), "kind": "oracle", "seconds": round(dt, 2),
+                "sample": f"fp64 C/OpenMP oracle on {nj} of {self.rows_j} joint rows (RoPE of all "
+                          f"Q/K included), {nn} of {self.rows_n} neighborhood rows and all "
+                          f"{WL_DEC.B * WL_DEC.H} decode rows; FLOPs scaled to the rows computed"}
+
+
+def cpu_baseline(host, budget_s=20.0):
+    return CpuSample(host).measure(budget_s)
+
+
+def reference(args, rank, world):
+    """The reference arm: the oracle as it stands on the host cores."""
+    if rank != 0:
+        return None
+    host = {"joint": make_inputs(WL_JOINT), "na": make_inputs(WL_NA), "dec": make_inputs(WL_DEC)}
+    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    cs = CpuSample(host)
+    for _ in range(args.warmup):
+        cs.measure(budget)
+    vals = []
+    last = None
+    for _ in range(args.steps):
+        last = cs.measure(budget)
+        vals.append(last["value"])
+    v = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * STEP_FLOPS / (v * 1e12), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16 inputs widened to f64)", "config": CONFIG,
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "no reference implementation exists (the pages ship no code); this arm times "
+                "the fp64 CPU oracle on a bounded sample per step",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = reference(args, rank, world)
+    else:
+        line = ours(args, rank, world, local)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

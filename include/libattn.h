@@ -152,6 +152,19 @@ ATTN_API attn_status_t attn_na3d_fwd(const void *q, const void *k, const void *v
 ATTN_API attn_status_t attn_na3d_window_starts(int T, int Hg, int W, const int kernel[3],
                                       int32_t *starts, void *stream);
 
+/*
+ * Tensor-core building-block check (testing): one CTA computes, for a single
+ * tile, S = q k^T and O = P v with the same tcgen05 MMA forms, shared-memory
+ * layouts and TMEM placement the bf16 attention kernels use.
+ *   q, k, v: DEVICE bf16 [128, D]; P: DEVICE bf16 [128, 128];
+ *   S: DEVICE f32 [128, 128]; O: DEVICE f32 [128, D]; D in {64, 128}.
+ * No counterpart on the pages: it isolates the matrix-descriptor and
+ * tensor-memory conventions so a layout error shows up as a wrong tile here.
+ */
+ATTN_API attn_status_t attn_debug_tc_tile(const void *q, const void *k, const void *v,
+                                          const void *P, float *S, float *O, int D,
+                                          void *stream);
+
 /* Human-readable name of a status code (static storage). */
 ATTN_API const char *attn_status_string(attn_status_t status);
 

@@ -255,3 +255,115 @@ def test_joint_fp32_full_compare(ta):
     o = ta.rope_joint_fwd(*_dev(x, w), pos)
     ref = oracle.joint_fwd(*_f64(x, w), x["pos"])
     assert_close(to_host64(o), ref, "f32", "joint fp32")
+
+
+# ------------------------------------------------- tensor-core (tcgen05) path
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tc_tile_building_blocks(ta, D):
+    """Both MMA forms on one tile: S = q k^T (smem x smem) and O = P v (TMEM x smem)."""
+    import ctypes
+    import torch
+    from workloads import bf16_round, bf16_to_f32
+    rng = np.random.Generator(np.random.PCG64(7400 + D))
+    q = bf16_round(rng.standard_normal((128, D), dtype=np.float32))
+    k = bf16_round(rng.standard_normal((128, D), dtype=np.float32))
+    v = bf16_round(rng.standard_normal((128, D), dtype=np.float32))
+    P = bf16_round(rng.random((128, 128), dtype=np.float32))
+    dq, dk, dv, dP = (to_dev(x, "bf16") for x in (q, k, v, P))
+    S = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    O = torch.empty((128, D), dtype=torch.float32, device="cuda")
+    L = ta.lib()
+    L.attn_debug_tc_tile.restype = ctypes.c_int
+    st = L.attn_debug_tc_tile(ctypes.c_void_p(dq.data_ptr()), ctypes.c_void_p(dk.data_ptr()),
+                              ctypes.c_void_p(dv.data_ptr()), ctypes.c_void_p(dP.data_ptr()),
+                              ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(O.data_ptr()), D,
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    assert ta.device_status() == 0
+    f = lambda x: bf16_to_f32(x).astype(np.float64)
+    np.testing.assert_allclose(S.cpu().numpy(), f(q) @ f(k).T, rtol=0, atol=1e-3)
+    np.testing.assert_allclose(O.cpu().numpy(), f(P) @ f(v), rtol=0, atol=1e-3)
+
+
+@pytest.mark.parametrize("Nq,Nkv,D", [(256, 128, 128), (256, 256, 64), (300, 1000, 128),
+                                      (1, 77, 64), (1000, 1, 128), (513, 4100, 64)])
+def test_tc_full_parity(ta, Nq, Nkv, D):
+    from workloads import draw
+    rng = np.random.Generator(np.random.PCG64(7500 + Nq + Nkv + D))
+    B, H = 2, 3
+    q = draw(rng, (B, H, Nq, D), "bf16")
+    k = draw(rng, (B, H, Nkv, D), "bf16")
+    v = draw(rng, (B, H, Nkv, D), "bf16")
+    with launched(ta, "tc_flash"):
+        o = ta.full_fwd(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
+    ref = oracle.full_fwd(to_f64(q, "bf16"), to_f64(k, "bf16"), to_f64(v, "bf16"))
+    assert_close(to_host64(o), ref, "bf16", f"tc full {Nq,Nkv,D}")
+    assert ta.device_status() == 0
+
+
+def test_tc_full_sharp_rows_rescale(ta):
+    # Q x 8 and a late key block with large scores: forces the lazy O rescale
+    from workloads import bf16_round
+    rng = np.random.Generator(np.random.PCG64(7600))
+    q = rng.standard_normal((1, 2, 256, 128), dtype=np.float32) * 8
+    k = rng.standard_normal((1, 2, 1024, 128), dtype=np.float32)
+    k[:, :, 700:720] *= 4
+    v = rng.standard_normal((1, 2, 1024, 128), dtype=np.float32)
+    q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
+    with launched(ta, "tc_flash"):
+        o = ta.full_fwd(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
+    ref = oracle.full_fwd(to_f64(q, "bf16"), to_f64(k, "bf16"), to_f64(v, "bf16"))
+    assert_close(to_host64(o), ref, "bf16", "tc sharp")
+
+
+def test_flux_joint_full_size_sampled_rows(ta):
+    import torch
+    w = WORKLOADS["flux_joint"]
+    x = make_inputs(w)
+    pos = torch.from_numpy(x["pos"]).cuda()
+    with launched(ta, "tc_flash"), launched(ta, "rope"):
+        o = ta.rope_joint_fwd(*_dev(x, w), pos)
+    rng = np.random.default_rng(11)
+    N = w.N
+    rows = np.concatenate([rng.choice(w.B * w.H * N, 2048, replace=False),
+                           [0, N - 1, 511, 512, 513, N * w.H - 1]])
+    rows = np.unique(rows)
+    ref = oracle.joint_fwd(*_f64(x, w), x["pos"], rows=rows)
+    got = to_host64(o).reshape(-1, w.D)[rows]
+    assert_close(got, ref, "bf16", "flux joint sampled")
+    assert ta.device_status() == 0
+
+
+@pytest.mark.parametrize("grid,kernel,H", [((6, 20, 24), (3, 7, 11), 2), ((9, 16, 16), (11, 11, 11), 1),
+                                           ((3, 9, 40), (5, 3, 9), 2), ((1, 4, 4), (3, 7, 7), 2),
+                                           ((13, 17, 19), (7, 9, 5), 1)])
+def test_tc_na3d_parity(ta, grid, kernel, H):
+    w = WORKLOADS["na3d_21x60x104_k11"].with_(grid=grid, kernel=kernel, H=H,
+                                             N=int(np.prod(grid)), seed=7700 + sum(grid))
+    x = make_inputs(w)
+    with launched(ta, "tc_na"):
+        o = ta.na3d_fwd(*_dev(x, w), w.grid, w.kernel)
+    ref = oracle.na3d_fwd(*_f64(x, w), w.grid, w.kernel)
+    assert_close(to_host64(o), ref, "bf16", f"tc na3d {grid} {kernel}")
+    assert ta.device_status() == 0
+
+
+def test_na3d_large_full_size_sampled_rows(ta):
+    w = WORKLOADS["na3d_21x60x104_k11"]
+    x = make_inputs(w)
+    with launched(ta, "tc_na"):
+        o = ta.na3d_fwd(*_dev(x, w), w.grid, w.kernel)
+    T, Hg, W = w.grid
+    rng = np.random.default_rng(12)
+    N = w.N
+    # a seeded sample plus rows on every face, edge and corner of the grid
+    picks = [(t, h, ww) for t in (0, 1, 5, 10, 15, 19, 20) for h in (0, 4, 5, 30, 54, 55, 59)
+             for ww in (0, 3, 5, 50, 98, 100, 103)]
+    edge = np.array([(t * Hg + h) * W + ww for t, h, ww in picks])
+    rows = np.unique(np.concatenate([rng.choice(w.B * w.H * N, 3000, replace=False),
+                                     edge, edge + 3 * N, edge + 7 * N]))
+    ref = oracle.na3d_fwd(*_f64(x, w), w.grid, w.kernel, rows=rows)
+    got = to_host64(o).reshape(-1, w.D)[rows]
+    assert_close(got, ref, "bf16", "na3d large sampled")
+    assert ta.device_status() == 0

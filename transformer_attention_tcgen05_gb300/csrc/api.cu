@@ -274,4 +274,15 @@ attn_status_t attn_na3d_window_starts(int T, int Hg, int W, const int kernel[3],
     return na_starts(c, T, Hg, W, kernel, starts);
 }
 
+attn_status_t attn_debug_tc_tile(const void *q, const void *k, const void *v, const void *P,
+                                 float *S, float *O, int D, void *stream) {
+    if (!q || !k || !v || !P || !S || !O) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(P)) return ATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
+    Ctx c;
+    attn_status_t st = get_ctx(stream, &c);
+    if (st != ATTN_OK) return st;
+    return tc_selftest(c, q, k, v, P, S, O, D);
+}
+
 }  // extern "C"

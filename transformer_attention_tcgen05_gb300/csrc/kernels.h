@@ -63,5 +63,8 @@ attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v,
                       int B, int H, int T, int Hg, int W, int D, const int kernel[3],
                       float scale);
 bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]);
+// One 128 x 128 tile through both tcgen05 MMA forms (testing).
+attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,
+                          const void *P, float *S, float *O, int D);
 
 }  // namespace attn

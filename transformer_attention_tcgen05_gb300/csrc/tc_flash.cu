@@ -1,21 +1,807 @@
-// tcgen05 flash attention (bf16) -- under construction.
+// Tensor-core (tcgen05 + TMEM + TMA) flash attention for bf16, sm_103a.
+//
+// S = Q K^T * scale, row softmax, O = P V, streamed over key tiles with an
+// online softmax (the attention of iris.c issue #15 "CUDA codepath !" and the
+// neighborhood attention of candle PR #11).  The pages compute it as cuBLAS
+// GEMM -> softmax kernel -> GEMM with S in HBM, or as a one-block-per-query
+// SIMT kernel; here S and P never leave the SM.
+//
+// One CTA = two 128-row query tiles (Q0, Q1) of one (batch, head), 10 warps:
+//   warps 0-3   softmax warpgroup of Q0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax warpgroup of Q1
+//   warp  8     MMA issuer (one elected thread) and TMEM owner
+//   warp  9     TMA loader (one elected thread)
+// Tensor memory (512 columns): S_t at [128 t, 128 t + 128), O_t at
+// [256 + D t, 256 + D (t + 1)).  P_t (bf16, two per column) overwrites the
+// first 64 columns of S_t after the softmax has read S_t into registers; the
+// P V MMA takes P straight from TMEM (A operand) and V from shared memory.
+//
+// Per key tile j the MMA thread issues, in order,
+//     PV0(j), QK0(j+1), PV1(j), QK1(j+1)
+// so each softmax warpgroup has one PV and one QK of the other tile to hide
+// behind.  tcgen05 MMAs of one thread execute in issue order, which is what
+// makes reusing S_t for QK_t(j+1) right after PV_t(j) (which reads P_t) safe.
+//
+// Softmax (base 2): x = s * scale * log2(e); the running max m is only moved
+// when the tile max exceeds it by more than 8 (P stays <= 2^8); only then is
+// O_t rescaled in TMEM, after waiting for the previous PV_t to complete.
+//
+// Full attention: both query tiles share each K/V tile (one stream).
+// Neighborhood attention: the two query tiles are two 3D boxes adjacent in w;
+// each streams the union of its queries' clamped windows as (1, KH, 16)
+// (t, h, w) key sub-boxes loaded by 5D TMA, masked per element.
+//
+// All spin-waits are bounded (1 s); on a timeout the CTA raises the device
+// error word, drains what it issued, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace attn {
+namespace {
 
-bool tc_full_supported(int, int, int, int, int) { return false; }
+constexpr int kBM = 128;      // query rows per tile (MMA M)
+constexpr int kNQ = 2;        // query tiles per CTA
+constexpr int kBN = 128;      // max keys per key tile (MMA N of S)
+constexpr int kKW = 16;       // neighborhood key sub-box width along w
 
-attn_status_t tc_full(const Ctx &, const void *, const void *, const void *, void *, int, int,
-                      int, int, int, float) {
-    return ATTN_ERR_UNSUPPORTED;
+template <int D, bool NA>
+struct TcCfg {
+    static constexpr int PANELS = D / 64;                  // 128-byte swizzle panels
+    static constexpr int PANEL_Q = kBM * 128;              // bytes per Q panel
+    static constexpr int PANEL_KV = kBN * 128;             // bytes per K/V panel
+    static constexpr int Q_BYTES = PANELS * PANEL_Q;
+    static constexpr int KV_BYTES = PANELS * PANEL_KV;
+    static constexpr int STREAMS = NA ? kNQ : 1;           // K/V streams per stage
+    static constexpr int STAGE_BYTES = 2 * STREAMS * KV_BYTES;
+    static constexpr int BUDGET = 227 * 1024 - 2048;
+    static constexpr int NS_RAW = (BUDGET - kNQ * Q_BYTES) / STAGE_BYTES;
+    static constexpr int NSTAGE = NS_RAW > 4 ? 4 : NS_RAW;
+    static_assert(NSTAGE >= 2, "at least two K/V stages");
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_KV = kNQ * Q_BYTES;
+    static constexpr int OFF_BAR = OFF_KV + NSTAGE * STAGE_BYTES;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;      // barriers + 1024 B alignment slack
+    static constexpr uint32_t TM_S = 0;                    // S_t at TM_S + t * kBN
+    static constexpr uint32_t TM_O = kNQ * kBN;            // O_t at TM_O + t * D
+    static constexpr uint32_t TM_COLS = 512;
+    static constexpr int NSOFT = 4 * kNQ;
+    static constexpr int W_MMA = NSOFT;
+    static constexpr int W_LOAD = NSOFT + 1;
+    static constexpr int NT = (NSOFT + 2) * 32;
+    // K (or V) tile of stream u in stage s
+    static constexpr int k_off(int s, int u) { return OFF_KV + s * STAGE_BYTES + u * KV_BYTES; }
+    static constexpr int v_off(int s, int u) {
+        return OFF_KV + s * STAGE_BYTES + (STREAMS + u) * KV_BYTES;
+    }
+};
+
+struct TcParams {
+    int Nq, Nkv;             // full attention: query / key tokens per (batch, head)
+    float c_log2;            // scale * log2(e)
+    __nv_bfloat16 *o;
+    unsigned *err;
+    // neighborhood attention (grid T x Hg x W, row-major)
+    int T, Hg, W;
+    int kt, kh, kw;          // requested kernel
+    int et, eh, ew;          // effective kernel
+    int bt, bh, bw;          // query box
+    int nbh, nbw2;           // boxes along h; box pairs along w
+    int nbw;                 // boxes along w
+    int KH;                  // key sub-box height (keys per tile = KH * 16)
+};
+
+// Barrier block at OFF_BAR.
+template <int NS>
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[NS], v_full[NS], kv_empty[NS];
+    uint64_t s_full[kNQ], p_ready[kNQ], o_done[kNQ];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Per-query-tile geometry of the neighborhood path.
+struct NaTile {
+    int t0, h0, w0;          // box origin
+    int u0t, u0h, u0w;       // union origin
+    int ut, nhc, nwc;        // union t extent, h chunks, w chunks
+    int ntiles;              // key tiles = ut * nhc * nwc (0 if the box is empty)
+};
+
+__device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t) {
+    NaTile g;
+    const int per_t = p.nbh * p.nbw2;
+    const int bi_t = pair / per_t, bi_h = (pair / p.nbw2) % p.nbh, bi_w = (pair % p.nbw2) * 2 + t;
+    g.t0 = bi_t * p.bt;
+    g.h0 = bi_h * p.bh;
+    g.w0 = bi_w * p.bw;
+    if (bi_w >= p.nbw) {
+        g.ntiles = 0;
+        g.u0t = g.u0h = g.u0w = g.ut = g.nhc = g.nwc = 0;
+        return g;
+    }
+    const int t1 = imin(g.t0 + p.bt, p.T) - 1, h1 = imin(g.h0 + p.bh, p.Hg) - 1,
+              w1 = imin(g.w0 + p.bw, p.W) - 1;
+    g.u0t = na_window_start(g.t0, p.T, p.kt);
+    g.u0h = na_window_start(g.h0, p.Hg, p.kh);
+    g.u0w = na_window_start(g.w0, p.W, p.kw);
+    g.ut = na_window_start(t1, p.T, p.kt) + p.et - g.u0t;
+    const int uh = na_window_start(h1, p.Hg, p.kh) + p.eh - g.u0h;
+    const int uw = na_window_start(w1, p.W, p.kw) + p.ew - g.u0w;
+    g.nhc = cdiv(uh, p.KH);
+    g.nwc = cdiv(uw, kKW);
+    g.ntiles = g.ut * g.nhc * g.nwc;
+    return g;
 }
 
-bool tc_na3d_supported(int, int, int, int, int, int, const int *) { return false; }
+// Key sub-box of tile j: origin (t, h, w).
+__device__ __forceinline__ void na_key_box(const NaTile &g, int KH, int j, int &t, int &h, int &w) {
+    const int wc = j % g.nwc;
+    const int hc = (j / g.nwc) % g.nhc;
+    const int tc = j / (g.nwc * g.nhc);
+    t = g.u0t + tc;
+    h = g.u0h + hc * KH;
+    w = g.u0w + wc * kKW;
+}
 
-attn_status_t tc_na3d(const Ctx &, const void *, const void *, const void *, void *, int, int,
-                      int, int, int, int, const int *, float) {
-    return ATTN_ERR_UNSUPPORTED;
+template <int D, bool NA>
+__global__ void __launch_bounds__(TcCfg<D, NA>::NT, 1)
+tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const TcParams p) {
+    using C = TcCfg<D, NA>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
+    Bars<C::NSTAGE> *bars = reinterpret_cast<Bars<C::NSTAGE> *>(smem + C::OFF_BAR);
+    volatile int *abort = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+
+    // ---- per-CTA work description (identical in every role)
+    int n_t[kNQ];
+    int steps;
+    NaTile g[kNQ];
+    int q0 = 0;
+    int BNt = kBN;                 // keys per tile
+    if constexpr (NA) {
+#pragma unroll
+        for (int t = 0; t < kNQ; ++t) {
+            g[t] = na_tile(p, blockIdx.x, t);
+            n_t[t] = g[t].ntiles;
+        }
+        BNt = p.KH * kKW;
+        steps = imax(n_t[0], n_t[1]);
+    } else {
+        q0 = blockIdx.x * (kNQ * kBM);
+        steps = cdiv(p.Nkv, kBN);
+        n_t[0] = n_t[1] = steps;
+    }
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            ptx::mbar_init(&bars->k_full[s], 1);
+            ptx::mbar_init(&bars->v_full[s], 1);
+            ptx::mbar_init(&bars->kv_empty[s], 1);
+        }
+        for (int t = 0; t < kNQ; ++t) {
+            ptx::mbar_init(&bars->s_full[t], 1);
+            ptx::mbar_init(&bars->p_ready[t], 128);
+            ptx::mbar_init(&bars->o_done[t], 1);
+        }
+        ptx::mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if constexpr (NA) {
+        // query rows past the box (box smaller than 128 rows) hold zeros, not stale data
+        const int rows = p.bt * p.bh * p.bw;
+        if (rows < kBM) {
+            for (int i = threadIdx.x; i < kNQ * C::PANELS * (kBM - rows) * 8; i += C::NT) {
+                const int chunk = i % 8, r = rows + (i / 8) % (kBM - rows);
+                const int pt = i / (8 * (kBM - rows));          // (tile, panel)
+                *reinterpret_cast<uint4 *>(smem + C::OFF_Q + pt * C::PANEL_Q + r * 128 + chunk * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            ptx::fence_proxy_async_smem();
+        }
+    }
+    if (warp == C::W_MMA) {
+        ptx::tmem_alloc(&bars->tmem_base, C::TM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == C::W_LOAD) {
+        // ================================================= TMA loader
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tq);
+            ptx::prefetch_tmap(&tk);
+            ptx::prefetch_tmap(&tv);
+            const uint64_t pol_q = ptx::l2_policy_evict_first();
+            const uint64_t pol_kv = ptx::l2_policy_evict_last();
+            // query tiles
+            uint32_t qbytes = 0;
+            if constexpr (NA) {
+                for (int t = 0; t < kNQ; ++t)
+                    if (n_t[t] > 0) qbytes += C::PANELS * p.bt * p.bh * p.bw * 128;
+            } else {
+                qbytes = kNQ * C::Q_BYTES;
+            }
+            ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+            for (int t = 0; t < kNQ; ++t)
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    uint8_t *dst = smem + C::OFF_Q + t * C::Q_BYTES + pn * C::PANEL_Q;
+                    if constexpr (NA) {
+                        if (n_t[t] > 0)
+                            ptx::tma_load_5d(dst, &tq, pn * 64, g[t].w0, g[t].h0, g[t].t0, bh,
+                                             &bars->q_full, pol_q);
+                    } else {
+                        ptx::tma_load_3d(dst, &tq, pn * 64, q0 + t * kBM, bh, &bars->q_full, pol_q);
+                    }
+                }
+            // key / value tiles
+            int issued = 0;
+            for (int j = 0; j < steps; ++j) {
+                const int s = j % C::NSTAGE;
+                if (j >= C::NSTAGE &&
+                    !ptx::mbar_wait_or_abort(&bars->kv_empty[s], ((j / C::NSTAGE) - 1) & 1, p.err,
+                                             abort))
+                    break;
+                issued = j + 1;
+                uint32_t bytes = 0;
+                for (int u = 0; u < C::STREAMS; ++u)
+                    if (j < n_t[u]) bytes += C::PANELS * BNt * 128;
+                for (int which = 0; which < 2; ++which) {
+                    uint64_t *bar = which == 0 ? &bars->k_full[s] : &bars->v_full[s];
+                    const CUtensorMap *tm = which == 0 ? &tk : &tv;
+                    ptx::mbar_arrive_expect_tx(bar, bytes);
+                    for (int u = 0; u < C::STREAMS; ++u) {
+                        if (j >= n_t[u]) continue;
+                        for (int pn = 0; pn < C::PANELS; ++pn) {
+                            uint8_t *dst = smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) +
+                                           pn * C::PANEL_KV;
+                            if constexpr (NA) {
+                                int kt_, kh_, kw_;
+                                na_key_box(g[u], p.KH, j, kt_, kh_, kw_);
+                                ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, bar, pol_kv);
+                            } else {
+                                ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bh, bar, pol_kv);
+                            }
+                        }
+                    }
+                }
+            }
+            // after a timeout elsewhere: let the copies this thread issued land
+            // (bounded) before the CTA's shared memory is released
+            if (*abort) {
+                ptx::mbar_wait(&bars->q_full, 0, nullptr);
+                for (int j = imax(0, issued - C::NSTAGE); j < issued; ++j) {
+                    ptx::mbar_wait(&bars->k_full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
+                    ptx::mbar_wait(&bars->v_full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
+                }
+            }
+        }
+    } else if (warp == C::W_MMA) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = ptx::idesc_bf16_f32(kBM, BNt, false);
+            const uint32_t id_pv = ptx::idesc_bf16_f32(kBM, D, true);
+            const uint32_t q_base = ptx::smem_addr(smem + C::OFF_Q);
+            auto issue_qk = [&](int t, int j) {
+                const int s = j % C::NSTAGE;
+                const uint32_t k_base = ptx::smem_addr(smem + C::k_off(s, C::STREAMS == 1 ? 0 : t));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 0 + (kk & 3) * 32;
+                    const uint64_t a = ptx::smem_desc_sw128(
+                        q_base + t * C::Q_BYTES + (kk >> 2) * C::PANEL_Q + off, 16, 1024);
+                    const uint64_t b =
+                        ptx::smem_desc_sw128(k_base + (kk >> 2) * C::PANEL_KV + off, 16, 1024);
+                    ptx::mma_ss(tmem + C::TM_S + t * kBN, a, b, id_qk, kk > 0);
+                }
+                ptx::tc_commit(&bars->s_full[t]);
+            };
+            auto issue_pv = [&](int t, int j) {
+                const int s = j % C::NSTAGE;
+                const uint32_t v_base = ptx::smem_addr(smem + C::v_off(s, C::STREAMS == 1 ? 0 : t));
+                for (int kk = 0; kk < BNt / 16; ++kk) {
+                    const uint64_t b =
+                        ptx::smem_desc_sw128(v_base + kk * 2048, C::PANEL_KV, 1024);
+                    ptx::mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_S + t * kBN + kk * 8, b, id_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::tc_commit(&bars->o_done[t]);
+            };
+            bool ok = ptx::mbar_wait_or_abort(&bars->q_full, 0, p.err, abort) &&
+                      (steps == 0 || ptx::mbar_wait_or_abort(&bars->k_full[0], 0, p.err, abort));
+            ptx::tc_fence_after();
+            if (ok)
+                for (int t = 0; t < kNQ; ++t)
+                    if (n_t[t] > 0) issue_qk(t, 0);
+            for (int j = 0; ok && j < steps; ++j) {
+                const int s = j % C::NSTAGE;
+                const uint32_t ph = (j / C::NSTAGE) & 1;
+                const int s1 = (j + 1) % C::NSTAGE;
+                const uint32_t ph1 = ((j + 1) / C::NSTAGE) & 1;
+                bool v_ready = false, k1_ready = false;
+                for (int t = 0; t < kNQ && ok; ++t) {
+                    if (j >= n_t[t]) continue;
+                    ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
+                    if (ok && !v_ready) {
+                        ok = ptx::mbar_wait_or_abort(&bars->v_full[s], ph, p.err, abort);
+                        v_ready = true;
+                    }
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_pv(t, j);
+                    if (j + 1 < n_t[t]) {
+                        if (!k1_ready) {
+                            ok = ptx::mbar_wait_or_abort(&bars->k_full[s1], ph1, p.err, abort);
+                            k1_ready = true;
+                            ptx::tc_fence_after();
+                        }
+                        if (ok) issue_qk(t, j + 1);
+                    }
+                }
+                ptx::tc_commit(&bars->kv_empty[s]);
+            }
+            // drain: every MMA this thread issued has completed before TMEM is freed
+            ptx::tc_commit(&bars->drain);
+            ptx::mbar_wait(&bars->drain, 0, p.err);
+        }
+    } else {
+        // ================================================= softmax warpgroups
+        const int t = warp >> 2;                 // query tile
+        const int quarter = warp & 3;            // TMEM lanes [32 quarter, 32 quarter + 32)
+        const int row = quarter * 32 + lane;     // query row within the tile
+        const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+        const uint32_t s_addr = lane_base + C::TM_S + t * kBN;
+        const uint32_t o_addr = lane_base + C::TM_O + t * D;
+        const float cl = p.c_log2;
+
+        // query of this row (neighborhood path) and its window
+        int qt = 0, qh = 0, qw = 0, wst = 0, wsh = 0, wsw = 0;
+        bool qvalid;
+        if constexpr (NA) {
+            const int dt = row / (p.bh * p.bw), dh = (row / p.bw) % p.bh, dw = row % p.bw;
+            qt = g[t].t0 + dt;
+            qh = g[t].h0 + dh;
+            qw = g[t].w0 + dw;
+            qvalid = n_t[t] > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
+            wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
+            wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
+            wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
+        } else {
+            qvalid = q0 + t * kBM + row < p.Nq;
+        }
+
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        const int nt = n_t[t];
+        for (int j = 0; j < nt; ++j) {
+            if (!ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t sv[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c)
+                if (c * 32 < BNt)
+                    ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+            ptx::tmem_wait_ld();
+
+            // ---- mask and tile maximum
+            float tmax = -INFINITY;
+            if constexpr (NA) {
+                int kt_, kh_, kw_;
+                na_key_box(g[t], p.KH, j, kt_, kh_, kw_);
+                const bool tv_ok = unsigned(kt_ - wst) < unsigned(p.et);
+                // valid w columns of this tile for this query (16-bit mask)
+                uint32_t wbits = 0;
+#pragma unroll
+                for (int c = 0; c < kKW; ++c)
+                    wbits |= (unsigned(kw_ + c - wsw) < unsigned(p.ew) ? 1u : 0u) << c;
+#pragma unroll
+                for (int r = 0; r < kBN / kKW; ++r) {
+                    const bool hv = tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh);
+                    const uint32_t bits = hv ? wbits : 0u;
+#pragma unroll
+                    for (int c = 0; c < kKW; ++c) {
+                        const int e = r * kKW + c;
+                        const float x = ((bits >> c) & 1u) ? __uint_as_float(sv[e]) : -INFINITY;
+                        sv[e] = __float_as_uint(x);
+                        tmax = fmaxf(tmax, x);
+                    }
+                }
+            } else {
+                const int valid = p.Nkv - j * kBN;     // keys of this tile inside the sequence
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) {
+                    float x = __uint_as_float(sv[e]);
+                    if (e >= valid) x = -INFINITY;
+                    sv[e] = __float_as_uint(x);
+                    tmax = fmaxf(tmax, x);
+                }
+            }
+            const float mt = tmax * cl;        // cl > 0: max commutes with the scaling
+
+            // ---- running maximum (moved lazily) and O rescale in TMEM
+            if (j == 0) {
+                m = mt;
+            } else if (mt > m + 8.f) {
+                const float f = ptx::ex2(m - mt);     // m == -inf -> 0
+                if (!ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld32(o_addr + c * 32, ov);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                    ptx::tmem_st32(o_addr + c * 32, ov);
+                }
+                l *= f;
+                m = mt;
+            }
+            const float mu = (m == -INFINITY) ? 0.f : m;
+
+            // ---- P = 2^(x - m) in bf16 into TMEM (over S), row sum in fp32
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                if (c * 32 >= BNt) break;
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * e]), cl, -mu));
+                    const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * e + 1]), cl, -mu));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st16(s_addr + c * 16, pk);
+            }
+            l += sum0 + sum1;
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->p_ready[t]);
+        }
+
+        // ---- epilogue: O / l -> bf16 -> global
+        if (ok && nt > 0 &&
+            ptx::mbar_wait_or_abort(&bars->o_done[t], (nt - 1) & 1, p.err, abort)) {
+            ptx::tc_fence_after();
+            const float inv = 1.f / l;
+            __nv_bfloat16 *orow = nullptr;
+            if (qvalid) {
+                size_t idx;
+                if constexpr (NA)
+                    idx = (size_t(bh) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw;
+                else
+                    idx = size_t(bh) * p.Nq + q0 + t * kBM + row;
+                orow = p.o + idx * D;
+            }
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(o_addr + c * 32, ov);
+                ptx::tmem_wait_ld();
+                if (qvalid) {
+                    uint4 w4[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wp[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv,
+                                            __uint_as_float(ov[2 * e + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = w4[e];
+                }
+            }
+        }
+    }
+
+    // ---- teardown: all TMEM traffic done before the owner warp frees it
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::W_MMA) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+// ---------------------------------------------------- single-tile self test
+//
+// One CTA: S = Q K^T (both operands K-major in shared memory) and O = P V
+// (P from TMEM, V MN-major in shared memory) for one 128 x 128 tile, written
+// out in fp32 -- the two MMA forms of the attention kernel in isolation.
+template <int D>
+__global__ void __launch_bounds__(160, 1)
+tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __nv_bfloat16 *P, float *S_out,
+                   float *O_out, unsigned *err) {
+    constexpr int PANELS = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
+    uint8_t *sq = smem, *sk = smem + PANELS * 16384, *svv = smem + 2 * PANELS * 16384;
+    __shared__ uint64_t bar_load, bar_mma, bar_p;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar_load, 1);
+        ptx::mbar_init(&bar_mma, 1);
+        ptx::mbar_init(&bar_p, 128);
+        abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 4) {
+        ptx::tmem_alloc(&tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_base;   // S at col 0, O at col 256
+    if (warp == 4) {
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&bar_load, 3 * PANELS * 16384);
+            for (int pn = 0; pn < PANELS; ++pn) {
+                ptx::tma_load_3d(sq + pn * 16384, &tq, pn * 64, 0, 0, &bar_load, 0);
+                ptx::tma_load_3d(sk + pn * 16384, &tk, pn * 64, 0, 0, &bar_load, 0);
+                ptx::tma_load_3d(svv + pn * 16384, &tv, pn * 64, 0, 0, &bar_load, 0);
+            }
+            bool ok = ptx::mbar_wait_or_abort(&bar_load, 0, err, &abort);
+            ptx::tc_fence_after();
+            if (ok) {
+                const uint32_t id_qk = ptx::idesc_bf16_f32(128, 128, false);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t a = ptx::smem_desc_sw128(ptx::smem_addr(sq) + (kk >> 2) * 16384 + off, 16, 1024);
+                    const uint64_t b = ptx::smem_desc_sw128(ptx::smem_addr(sk) + (kk >> 2) * 16384 + off, 16, 1024);
+                    ptx::mma_ss(tmem, a, b, id_qk, kk > 0);
+                }
+                ptx::tc_commit(&bar_mma);
+                ok = ptx::mbar_wait_or_abort(&bar_p, 0, err, &abort);
+                ptx::tc_fence_after();
+                if (ok) {
+                    const uint32_t id_pv = ptx::idesc_bf16_f32(128, D, true);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t b = ptx::smem_desc_sw128(ptx::smem_addr(svv) + kk * 2048, 16384, 1024);
+                        ptx::mma_ts(tmem + 256, tmem + 128 + kk * 8, b, id_pv, kk > 0);
+                    }
+                }
+                ptx::tc_commit(&bar_mma);
+            }
+        }
+    } else {
+        // 128 threads: write P (bf16) into TMEM columns [128, 192) after S is done,
+        // then read S and O back.
+        const int row = warp * 32 + lane;
+        const uint32_t lb = tmem + (uint32_t(warp * 32) << 16);
+        bool ok = ptx::mbar_wait_or_abort(&bar_mma, 0, err, &abort);
+        ptx::tc_fence_after();
+        if (ok) {
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32];
+                ptx::tmem_ld32(lb + c * 32, sv);
+                ptx::tmem_wait_ld();
+                for (int e = 0; e < 32; ++e) S_out[row * 128 + c * 32 + e] = __uint_as_float(sv[e]);
+            }
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(P + row * 128 + c * 32);
+                for (int e = 0; e < 16; ++e) pk[e] = src[e];
+                ptx::tmem_st16(lb + 128 + c * 16, pk);
+            }
+            ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bar_p);
+        if (ok) ok = ptx::mbar_wait_or_abort(&bar_mma, 1, err, &abort);
+        ptx::tc_fence_after();
+        if (ok) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(lb + 256 + c * 32, ov);
+                ptx::tmem_wait_ld();
+                for (int e = 0; e < 32; ++e) O_out[row * D + c * 32 + e] = __uint_as_float(ov[e]);
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/box innermost first (dims[0] = D).
+bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+               const uint32_t *box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t bdim[5], estr[5];
+    uint64_t stride = 2;
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) gstride[i - 1] = stride;
+        stride *= dims[i];
+    }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gdim, gstride,
+              bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool NA>
+attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
+                        const CUtensorMap &tv, const TcParams &p, dim3 grid) {
+    using C = TcCfg<D, NA>;
+    static int done_mask = 0;
+    auto kern = tc_attn_kernel<D, NA>;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
+        return ATTN_ERR_RESOURCE;
+    kern<<<grid, C::NT, C::SMEM, c.stream>>>(tq, tk, tv, p);
+    return launch_status(NA ? kFamTcNa : kFamTcFlash);
+}
+
+// Query box and key sub-box height for the neighborhood path: at most 128
+// queries per box, w extent of every union <= 16 (one w chunk where possible),
+// minimising the key slots computed (boxes x tiles x KH*16) per query.
+bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KH) {
+    const int ext[3] = {T, Hg, W};
+    double best = -1;
+    for (int cbt = 1; cbt <= imin(T, 128); ++cbt)
+        for (int cbh = 1; cbh <= imin(Hg, 128 / cbt); ++cbh)
+            for (int cbw = 1; cbw <= imin(W, 128 / (cbt * cbh)); ++cbw) {
+                if (cbt * cbh * cbw < 64) continue;          // keep the MMA rows busy
+                for (int ckh = 1; ckh <= 8; ++ckh) {
+                    // total key slots over all boxes = sum_t(ut) * sum_h(nhc) * sum_w(nwc) * KH*16
+                    const int b[3] = {cbt, cbh, cbw};
+                    double axis[3];
+                    for (int a = 0; a < 3; ++a) {
+                        const int keff = imin(kern[a], ext[a]);
+                        double acc = 0;
+                        for (int i0 = 0; i0 < ext[a]; i0 += b[a]) {
+                            const int i1 = imin(i0 + b[a], ext[a]) - 1;
+                            const int u = na_window_start(i1, ext[a], kern[a]) + keff -
+                                          na_window_start(i0, ext[a], kern[a]);
+                            acc += a == 0 ? u : a == 1 ? cdiv(u, ckh) : cdiv(u, kKW);
+                        }
+                        axis[a] = acc;
+                    }
+                    const int nbw = cdiv(W, cbw);
+                    // odd box count along w leaves one query tile idle per (t, h) box row
+                    const double w_pairs_waste = (nbw & 1) ? double(nbw + 1) / nbw : 1.0;
+                    // every box is one 128-row query tile: computed (row, key) slots
+                    const double cost = axis[0] * axis[1] * axis[2] * ckh * kKW * w_pairs_waste;
+                    if (best < 0 || cost < best) {
+                        best = cost;
+                        bt = cbt; bh = cbh; bw = cbw; KH = ckh;
+                    }
+                }
+            }
+    return best > 0;
+}
+
+}  // namespace
+
+bool tc_full_supported(int B, int H, int Nq, int Nkv, int D) {
+    return (D == 64 || D == 128) && B * H <= 65535 && Nq >= 1 && Nkv >= 1 && encode_fn() != nullptr;
+}
+
+attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v, void *o, int B,
+                      int H, int Nq, int Nkv, int D, float scale) {
+    CUtensorMap tq, tk, tv;
+    const uint64_t dq[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
+    const uint64_t dk[3] = {uint64_t(D), uint64_t(Nkv), uint64_t(B) * H};
+    const uint32_t box[3] = {64, kBM, 1};
+    if (!make_tmap(&tq, q, 3, dq, box) || !make_tmap(&tk, k, 3, dk, box) ||
+        !make_tmap(&tv, v, 3, dk, box))
+        return ATTN_ERR_CUDA;
+    TcParams p{};
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.c_log2 = scale * kLog2e;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.err = c.err;
+    const dim3 grid(cdiv(Nq, kNQ * kBM), B * H);
+    return D == 128 ? launch_tc<128, false>(c, tq, tk, tv, p, grid)
+                    : launch_tc<64, false>(c, tq, tk, tv, p, grid);
+}
+
+bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]) {
+    (void)T; (void)Hg; (void)W; (void)kernel;
+    return D == 64 && B * H <= 65535 && encode_fn() != nullptr;
+}
+
+attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v, void *o, int B,
+                      int H, int T, int Hg, int W, int D, const int kernel[3], float scale) {
+    TcParams p{};
+    if (!plan_na(T, Hg, W, kernel, p.bt, p.bh, p.bw, p.KH)) return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tq, tk, tv;
+    const uint64_t dims[5] = {uint64_t(D), uint64_t(W), uint64_t(Hg), uint64_t(T), uint64_t(B) * H};
+    const uint32_t qbox[5] = {64, uint32_t(p.bw), uint32_t(p.bh), uint32_t(p.bt), 1};
+    const uint32_t kbox[5] = {64, uint32_t(kKW), uint32_t(p.KH), 1, 1};
+    if (!make_tmap(&tq, q, 5, dims, qbox) || !make_tmap(&tk, k, 5, dims, kbox) ||
+        !make_tmap(&tv, v, 5, dims, kbox))
+        return ATTN_ERR_CUDA;
+    p.c_log2 = scale * kLog2e;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.err = c.err;
+    p.T = T; p.Hg = Hg; p.W = W;
+    p.kt = kernel[0]; p.kh = kernel[1]; p.kw = kernel[2];
+    p.et = imin(kernel[0], T); p.eh = imin(kernel[1], Hg); p.ew = imin(kernel[2], W);
+    p.nbh = cdiv(Hg, p.bh);
+    p.nbw = cdiv(W, p.bw);
+    p.nbw2 = cdiv(p.nbw, 2);
+    const dim3 grid(cdiv(T, p.bt) * p.nbh * p.nbw2, B * H);
+    return launch_tc<64, true>(c, tq, tk, tv, p, grid);
+}
+
+attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,
+                          const void *P, float *S, float *O, int D) {
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tq, tk, tv;
+    const uint64_t dims[3] = {uint64_t(D), 128, 1};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!make_tmap(&tq, q, 3, dims, box) || !make_tmap(&tk, k, 3, dims, box) ||
+        !make_tmap(&tv, v, 3, dims, box))
+        return ATTN_ERR_CUDA;
+    const size_t smem = 3 * (D / 64) * 16384 + 1024;
+    static int done_mask = 0;
+    if (D == 128) {
+        if (!ensure_smem_attr(reinterpret_cast<const void *>(tc_selftest_kernel<128>), smem, c.device, &done_mask))
+            return ATTN_ERR_RESOURCE;
+        tc_selftest_kernel<128><<<1, 160, smem, c.stream>>>(
+            tq, tk, tv, static_cast<const __nv_bfloat16 *>(P), S, O, c.err);
+    } else {
+        static int done64 = 0;
+        if (!ensure_smem_attr(reinterpret_cast<const void *>(tc_selftest_kernel<64>), smem, c.device, &done64))
+            return ATTN_ERR_RESOURCE;
+        tc_selftest_kernel<64><<<1, 160, smem, c.stream>>>(
+            tq, tk, tv, static_cast<const __nv_bfloat16 *>(P), S, O, c.err);
+    }
+    return launch_status(kFamTcFlash);
 }
 
 }  // namespace attn

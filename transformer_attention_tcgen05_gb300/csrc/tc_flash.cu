@@ -390,8 +390,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         const int nt = n_t[t];
+        // tcgen05.ld / st / wait are warp-collective (.sync.aligned): every
+        // branch that leads to one is made uniform across the warp.
         for (int j = 0; j < nt; ++j) {
-            if (!ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort)) {
+            if (!__all_sync(0xffffffffu,
+                            ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort))) {
                 ok = false;
                 break;
             }
@@ -439,11 +442,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             const float mt = tmax * cl;        // cl > 0: max commutes with the scaling
 
             // ---- running maximum (moved lazily) and O rescale in TMEM
+            const bool want = j == 0 || mt > m + 8.f;   // this row moves its maximum
             if (j == 0) {
                 m = mt;
-            } else if (mt > m + 8.f) {
-                const float f = ptx::ex2(m - mt);     // m == -inf -> 0
-                if (!ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1, p.err, abort)) {
+            } else if (__any_sync(0xffffffffu, want)) {
+                // rows that move m scale their O row; the others multiply by 1
+                const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
+                                                                     p.err, abort))) {
                     ok = false;
                     break;
                 }
@@ -457,8 +463,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
                     ptx::tmem_st32(o_addr + c * 32, ov);
                 }
-                l *= f;
-                m = mt;
+                if (want) {
+                    l *= f;
+                    m = mt;
+                }
             }
             const float mu = (m == -INFINITY) ? 0.f : m;
 
@@ -486,7 +494,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
         // ---- epilogue: O / l -> bf16 -> global
         if (ok && nt > 0 &&
-            ptx::mbar_wait_or_abort(&bars->o_done[t], (nt - 1) & 1, p.err, abort)) {
+            __all_sync(0xffffffffu,
+                       ptx::mbar_wait_or_abort(&bars->o_done[t], (nt - 1) & 1, p.err, abort))) {
             ptx::tc_fence_after();
             const float inv = 1.f / l;
             __nv_bfloat16 *orow = nullptr;
@@ -596,7 +605,7 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         // then read S and O back.
         const int row = warp * 32 + lane;
         const uint32_t lb = tmem + (uint32_t(warp * 32) << 16);
-        bool ok = ptx::mbar_wait_or_abort(&bar_mma, 0, err, &abort);
+        bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bar_mma, 0, err, &abort));
         ptx::tc_fence_after();
         if (ok) {
             for (int c = 0; c < 4; ++c) {
@@ -615,7 +624,7 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bar_p);
-        if (ok) ok = ptx::mbar_wait_or_abort(&bar_mma, 1, err, &abort);
+        if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bar_mma, 1, err, &abort));
         ptx::tc_fence_after();
         if (ok) {
             for (int c = 0; c < D / 32; ++c) {

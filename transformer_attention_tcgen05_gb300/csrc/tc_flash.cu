@@ -694,16 +694,18 @@ attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
 }
 
 // Query box and key sub-box height for the neighborhood path: at most 128
-// queries per box, w extent of every union <= 16 (one w chunk where possible),
-// minimising the key slots computed (boxes x tiles x KH*16) per query.
+// queries per box, minimising the (query row, key) slots the MMAs compute over
+// all boxes (boxes x tiles x (KH*16 + per-tile overhead)).
 bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KH) {
     const int ext[3] = {T, Hg, W};
     double best = -1;
     for (int cbt = 1; cbt <= imin(T, 128); ++cbt)
         for (int cbh = 1; cbh <= imin(Hg, 128 / cbt); ++cbh)
             for (int cbw = 1; cbw <= imin(W, 128 / (cbt * cbh)); ++cbw) {
-                if (cbt * cbh * cbw < 64) continue;          // keep the MMA rows busy
-                for (int ckh = 1; ckh <= 8; ++ckh) {
+                if (cbt * cbh * cbw < imin(64, T * Hg * W)) continue;   // keep MMA rows busy
+                // key tiles of 64..128 keys keep the MMAs large enough to amortise
+                // the per-tile barrier round trips
+                for (int ckh = imin(4, imin(kern[1], Hg) + cbh - 1); ckh <= 8; ++ckh) {
                     // total key slots over all boxes = sum_t(ut) * sum_h(nhc) * sum_w(nwc) * KH*16
                     const int b[3] = {cbt, cbh, cbw};
                     double axis[3];
@@ -722,7 +724,8 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
                     // odd box count along w leaves one query tile idle per (t, h) box row
                     const double w_pairs_waste = (nbw & 1) ? double(nbw + 1) / nbw : 1.0;
                     // every box is one 128-row query tile: computed (row, key) slots
-                    const double cost = axis[0] * axis[1] * axis[2] * ckh * kKW * w_pairs_waste;
+                    // (a tile costs its key slots plus a fixed overhead of ~32 key slots)
+                    const double cost = axis[0] * axis[1] * axis[2] * (ckh * kKW + 32) * w_pairs_waste;
                     if (best < 0 || cost < best) {
                         best = cost;
                         bt = cbt; bh = cbh; bw = cbw; KH = ckh;
@@ -730,6 +733,35 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
                 }
             }
     return best > 0;
+}
+
+// Plans are cached per (grid, kernel): the search is a few thousand candidates.
+struct NaPlan {
+    int bt, bh, bw, KH;
+    bool ok;
+};
+
+NaPlan cached_plan(int T, int Hg, int W, const int kern[3]) {
+    struct Entry {
+        int key[6];
+        NaPlan plan;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    const int key[6] = {T, Hg, W, kern[0], kern[1], kern[2]};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        bool same = true;
+        for (int a = 0; a < 6; ++a) same = same && cache[i].key[a] == key[a];
+        if (same) return cache[i].plan;
+    }
+    NaPlan pl{};
+    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KH);
+    Entry &e = cache[used < 64 ? used++ : 63];
+    for (int a = 0; a < 6; ++a) e.key[a] = key[a];
+    e.plan = pl;
+    return pl;
 }
 
 }  // namespace
@@ -759,14 +791,16 @@ attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v,
 }
 
 bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]) {
-    (void)T; (void)Hg; (void)W; (void)kernel;
-    return D == 64 && B * H <= 65535 && encode_fn() != nullptr;
+    return D == 64 && B * H <= 65535 && encode_fn() != nullptr &&
+           cached_plan(T, Hg, W, kernel).ok;
 }
 
 attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v, void *o, int B,
                       int H, int T, int Hg, int W, int D, const int kernel[3], float scale) {
     TcParams p{};
-    if (!plan_na(T, Hg, W, kernel, p.bt, p.bh, p.bw, p.KH)) return ATTN_ERR_UNSUPPORTED;
+    const NaPlan pl = cached_plan(T, Hg, W, kernel);
+    if (!pl.ok) return ATTN_ERR_UNSUPPORTED;
+    p.bt = pl.bt; p.bh = pl.bh; p.bw = pl.bw; p.KH = pl.KH;
     CUtensorMap tq, tk, tv;
     const uint64_t dims[5] = {uint64_t(D), uint64_t(W), uint64_t(Hg), uint64_t(T), uint64_t(B) * H};
     const uint32_t qbox[5] = {64, uint32_t(p.bw), uint32_t(p.bh), uint32_t(p.bt), 1};

@@ -10,8 +10,13 @@
 // One pass over Q and K (HBM-bound: read 2, write 2 tensors) leaves the
 // rotated copies in the caller's workspace, so the attention kernel streams
 // pre-rotated K tiles instead of re-rotating every K tile in each of the
-// N/128 query-tile CTAs that read it.  Frequencies come from the host in
-// double precision; the angle is one fp32 product, reduced by sincosf.
+// N/128 query-tile CTAs that read it.
+//
+// Layout of the work: a thread owns 8 consecutive channels (4 pairs, one
+// 16-byte load for bf16) of one token row and applies them to the same row
+// of every head, so cos/sin of a (token, pair) is computed once per CTA column
+// instead of once per head.  Frequencies come from the host in double
+// precision; the angle is one fp32 product, reduced by sincosf.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,31 +29,75 @@ struct RopeParams {
     const void *q, *k;
     void *qr, *kr;
     const int32_t *pos;
-    long long total_pairs;       // BH * N * D/2
-    int N, Dh;                   // tokens, pairs per row (D/2)
+    int BH, N, D;
     float freq[kMaxPairs];       // per-pair frequency theta^(-2i/n_a)
     int8_t axis[kMaxPairs];      // per-pair axis index
 };
 
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const void *p) { u = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ void store(void *p) const { *reinterpret_cast<uint4 *>(p) = u; }
+    __device__ __forceinline__ float get(int i) const {
+        const uint32_t w = i < 2 ? u.x : i < 4 ? u.y : i < 6 ? u.z : u.w;
+        return (i & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    __device__ __forceinline__ void set2(int pr, float a, float b) {
+        const uint32_t w = pack_bf16x2(a, b);
+        if (pr == 0) u.x = w; else if (pr == 1) u.y = w; else if (pr == 2) u.z = w; else u.w = w;
+    }
+};
+template <> struct Vec8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void *p) {
+        a = reinterpret_cast<const float4 *>(p)[0];
+        b = reinterpret_cast<const float4 *>(p)[1];
+    }
+    __device__ __forceinline__ void store(void *p) const {
+        reinterpret_cast<float4 *>(p)[0] = a;
+        reinterpret_cast<float4 *>(p)[1] = b;
+    }
+    __device__ __forceinline__ float get(int i) const {
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        return v[i];
+    }
+    __device__ __forceinline__ void set2(int pr, float x, float y) {
+        if (pr == 0) { a.x = x; a.y = y; } else if (pr == 1) { a.z = x; a.w = y; }
+        else if (pr == 2) { b.x = x; b.y = y; } else { b.z = x; b.w = y; }
+    }
+};
+
+// grid: (ceil(N * D/8 / 256), ceil(BH / heads_per_cta)); thread -> (token, 8-channel group)
 template <typename T>
-__global__ void __launch_bounds__(256) rope_kernel(const RopeParams p) {
-    for (long long e = blockIdx.x * 256ll + threadIdx.x; e < p.total_pairs;
-         e += 256ll * gridDim.x) {
-        const int pair = int(e % p.Dh);
-        const long long row = e / p.Dh;           // (bh, t)
-        const int t = int(row % p.N);
-        const float ang = float(p.pos[t * 4 + p.axis[pair]]) * p.freq[pair];
-        float sn, cs;
-        sincosf(ang, &sn, &cs);
-        const size_t off = size_t(e) * 2;
-        const T *src[2] = {static_cast<const T *>(p.q), static_cast<const T *>(p.k)};
-        T *dst[2] = {static_cast<T *>(p.qr), static_cast<T *>(p.kr)};
+__global__ void __launch_bounds__(256) rope_kernel(const RopeParams p, int heads_per_cta) {
+    const int groups = p.D / 8;
+    const long long e = blockIdx.x * 256ll + threadIdx.x;
+    if (e >= (long long)p.N * groups) return;
+    const int t = int(e / groups), g = int(e % groups);
+    float cs[4], sn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int pr = g * 4 + i;
+        const float ang = float(p.pos[t * 4 + p.axis[pr]]) * p.freq[pr];
+        sincosf(ang, &sn[i], &cs[i]);
+    }
+    const int h0 = blockIdx.y * heads_per_cta, h1 = imin(h0 + heads_per_cta, p.BH);
+    const T *src[2] = {static_cast<const T *>(p.q), static_cast<const T *>(p.k)};
+    T *dst[2] = {static_cast<T *>(p.qr), static_cast<T *>(p.kr)};
+    for (int h = h0; h < h1; ++h) {
+        const size_t off = (size_t(h) * p.N + t) * p.D + g * 8;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-            const float x0 = Elem<T>::load(src[w] + off);
-            const float x1 = Elem<T>::load(src[w] + off + 1);
-            Elem<T>::store(dst[w] + off, x0 * cs - x1 * sn);
-            Elem<T>::store(dst[w] + off + 1, x0 * sn + x1 * cs);
+            Vec8<T> x;
+            x.load(src[w] + off);
+            Vec8<T> y = x;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = x.get(2 * i), x1 = x.get(2 * i + 1);
+                y.set2(i, x0 * cs[i] - x1 * sn[i], x0 * sn[i] + x1 * cs[i]);
+            }
+            y.store(dst[w] + off);
         }
     }
 }
@@ -60,9 +109,7 @@ attn_status_t rope_rotate_qk(const Ctx &c, attn_dtype_t dt, const void *q, const
                              const int axes_dim[4], float theta) {
     RopeParams p{};
     p.q = q; p.k = k; p.qr = qr; p.kr = kr; p.pos = pos;
-    p.N = N;
-    p.Dh = D / 2;
-    p.total_pairs = (long long)BH * N * (D / 2);
+    p.BH = BH; p.N = N; p.D = D;
     int ch = 0;
     for (int a = 0; a < 4; ++a) {
         for (int i = 0; i < axes_dim[a] / 2; ++i) {
@@ -72,13 +119,16 @@ attn_status_t rope_rotate_qk(const Ctx &c, attn_dtype_t dt, const void *q, const
         }
         ch += axes_dim[a];
     }
-    long long blocks = (p.total_pairs + 255) / 256;
-    if (blocks > 32ll * c.sm_count) blocks = 32ll * c.sm_count;
-    if (blocks < 1) blocks = 1;
+    // enough CTAs to fill the GPU several times over; each reuses its
+    // cos/sin across `heads_per_cta` heads
+    const long long cols = ((long long)N * (D / 8) + 255) / 256;
+    int hpc = 1;
+    while (hpc < BH && cols * cdiv(BH, hpc * 2) >= 8ll * c.sm_count) hpc *= 2;
+    const dim3 grid(unsigned(cols), unsigned(cdiv(BH, hpc)));
     if (dt == ATTN_F32)
-        rope_kernel<float><<<int(blocks), 256, 0, c.stream>>>(p);
+        rope_kernel<float><<<grid, 256, 0, c.stream>>>(p, hpc);
     else
-        rope_kernel<__nv_bfloat16><<<int(blocks), 256, 0, c.stream>>>(p);
+        rope_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(p, hpc);
     return launch_status(kFamRope);
 }
 

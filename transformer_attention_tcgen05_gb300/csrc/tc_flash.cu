@@ -6,30 +6,41 @@
 // GEMM -> softmax kernel -> GEMM with S in HBM, or as a one-block-per-query
 // SIMT kernel; here S and P never leave the SM.
 //
-// One CTA = two 128-row query tiles (Q0, Q1) of one (batch, head), 10 warps:
+// One CTA = two 128-row query tiles (Q0, Q1) of one (batch, head), 12 warps:
 //   warps 0-3   softmax warpgroup of Q0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax warpgroup of Q1
 //   warp  8     MMA issuer (one elected thread) and TMEM owner
-//   warp  9     TMA loader (one elected thread)
+//   warp  9     TMA loader (one elected thread); warps 10-11 only donate
+//               registers: the third warpgroup drops to 56 registers per
+//               thread (setmaxnreg) so the softmax warpgroups can hold a whole
+//               128-column S row in registers (224 per thread).
 // Tensor memory (512 columns): S_t at [128 t, 128 t + 128), O_t at
-// [256 + D t, 256 + D (t + 1)).  P_t (bf16, two per column) overwrites the
-// first 64 columns of S_t after the softmax has read S_t into registers; the
-// P V MMA takes P straight from TMEM (A operand) and V from shared memory.
+// [256 + D t, 256 + D (t + 1)).  With D = 128 the columns are full and P_t
+// (bf16, two per column) overwrites the first 64 columns of S_t once the
+// softmax has read S_t; with D = 64 P_t has columns of its own
+// ([384 + 64 t, 448 + 64 t)).  The P V MMA takes P straight from TMEM
+// (A operand) and V from shared memory (MN-major B operand).
 //
-// Per key tile j the MMA thread issues, in order,
-//     PV0(j), QK0(j+1), PV1(j), QK1(j+1)
-// so each softmax warpgroup has one PV and one QK of the other tile to hide
-// behind.  tcgen05 MMAs of one thread execute in issue order, which is what
-// makes reusing S_t for QK_t(j+1) right after PV_t(j) (which reads P_t) safe.
+// Issue order of the MMA thread per key tile j:
+//   D = 128 (P over S):  PV0(j), QK0(j+1), PV1(j), QK1(j+1)   -- QK_t(j+1)
+//       overwrites S_t only after PV_t(j) has read P_t (MMAs of one thread
+//       execute in issue order), so each softmax warpgroup hides behind the
+//       other tile's PV and QK;
+//   D = 64 (separate P): QK0(j+1), QK1(j+1) as soon as the softmax has read
+//       S_t(j) into registers, then PV0(j), PV1(j) -- the next S is computed
+//       while the softmax of the current tile runs.
 //
 // Softmax (base 2): x = s * scale * log2(e); the running max m is only moved
 // when the tile max exceeds it by more than 8 (P stays <= 2^8); only then is
 // O_t rescaled in TMEM, after waiting for the previous PV_t to complete.
+// Every branch that leads to a warp-collective tcgen05.ld / st is uniform
+// across the warp.
 //
 // Full attention: both query tiles share each K/V tile (one stream).
 // Neighborhood attention: the two query tiles are two 3D boxes adjacent in w;
 // each streams the union of its queries' clamped windows as (1, KH, 16)
-// (t, h, w) key sub-boxes loaded by 5D TMA, masked per element.
+// (t, h, w) key sub-boxes loaded by 5D TMA, masked per element; a warp whose
+// 32 rows are all outside a key tile's window skips the exponentials.
 //
 // All spin-waits are bounded (1 s); on a timeout the CTA raises the device
 // error word, drains what it issued, frees TMEM and exits.
@@ -69,11 +80,20 @@ struct TcCfg {
     static constexpr int SMEM = OFF_BAR + 512 + 1024;      // barriers + 1024 B alignment slack
     static constexpr uint32_t TM_S = 0;                    // S_t at TM_S + t * kBN
     static constexpr uint32_t TM_O = kNQ * kBN;            // O_t at TM_O + t * D
+    static constexpr bool SEP_P = kNQ * (kBN + D + kBN / 2) <= 512;   // P_t has its own columns
+    static constexpr uint32_t TM_P = SEP_P ? TM_O + kNQ * D : TM_S;   // P_t at TM_P + t * PSTRIDE
+    static constexpr uint32_t PSTRIDE = SEP_P ? kBN / 2 : kBN;
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int NSOFT = 4 * kNQ;
     static constexpr int W_MMA = NSOFT;
     static constexpr int W_LOAD = NSOFT + 1;
-    static constexpr int NT = (NSOFT + 2) * 32;
+    static constexpr int NT = (NSOFT + 4) * 32;            // 3 warpgroups
+    // register split: launch 168 x 384 = 64512; 2 x 128 x 224 + 128 x 56 = 64512
+    static constexpr int REGS_LAUNCH = 168;
+    static constexpr int REGS_SOFTMAX = 224;
+    static constexpr int REGS_OTHER = 56;
+    static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= NT * REGS_LAUNCH,
+                  "setmaxnreg split must fit the launch's register file share");
     // K (or V) tile of stream u in stage s
     static constexpr int k_off(int s, int u) { return OFF_KV + s * STAGE_BYTES + u * KV_BYTES; }
     static constexpr int v_off(int s, int u) {
@@ -101,7 +121,7 @@ template <int NS>
 struct Bars {
     uint64_t q_full;
     uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-    uint64_t s_full[kNQ], p_ready[kNQ], o_done[kNQ];
+    uint64_t s_full[kNQ], s_free[kNQ], p_ready[kNQ], o_done[kNQ];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -194,6 +214,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         }
         for (int t = 0; t < kNQ; ++t) {
             ptx::mbar_init(&bars->s_full[t], 1);
+            ptx::mbar_init(&bars->s_free[t], 128);
             ptx::mbar_init(&bars->p_ready[t], 128);
             ptx::mbar_init(&bars->o_done[t], 1);
         }
@@ -223,15 +244,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == C::W_LOAD) {
-        // ================================================= TMA loader
-        if (lane == 0) {
+    if (warp >= C::NSOFT) {
+        ptx::regs_decrease<C::REGS_OTHER>();
+        if (warp == C::W_LOAD && lane == 0) {
+            // ============================================= TMA loader
             ptx::prefetch_tmap(&tq);
             ptx::prefetch_tmap(&tk);
             ptx::prefetch_tmap(&tv);
             const uint64_t pol_q = ptx::l2_policy_evict_first();
             const uint64_t pol_kv = ptx::l2_policy_evict_last();
-            // query tiles
             uint32_t qbytes = 0;
             if constexpr (NA) {
                 for (int t = 0; t < kNQ; ++t)
@@ -251,7 +272,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         ptx::tma_load_3d(dst, &tq, pn * 64, q0 + t * kBM, bh, &bars->q_full, pol_q);
                     }
                 }
-            // key / value tiles
             int issued = 0;
             for (int j = 0; j < steps; ++j) {
                 const int s = j % C::NSTAGE;
@@ -292,10 +312,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     ptx::mbar_wait(&bars->v_full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
                 }
             }
-        }
-    } else if (warp == C::W_MMA) {
-        // ================================================= MMA issuer
-        if (lane == 0) {
+        } else if (warp == C::W_MMA && lane == 0) {
+            // ============================================= MMA issuer
             const uint32_t id_qk = ptx::idesc_bf16_f32(kBM, BNt, false);
             const uint32_t id_pv = ptx::idesc_bf16_f32(kBM, D, true);
             const uint32_t q_base = ptx::smem_addr(smem + C::OFF_Q);
@@ -304,7 +322,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 const uint32_t k_base = ptx::smem_addr(smem + C::k_off(s, C::STREAMS == 1 ? 0 : t));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 0 + (kk & 3) * 32;
+                    const uint32_t off = (kk & 3) * 32;
                     const uint64_t a = ptx::smem_desc_sw128(
                         q_base + t * C::Q_BYTES + (kk >> 2) * C::PANEL_Q + off, 16, 1024);
                     const uint64_t b =
@@ -317,10 +335,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 const int s = j % C::NSTAGE;
                 const uint32_t v_base = ptx::smem_addr(smem + C::v_off(s, C::STREAMS == 1 ? 0 : t));
                 for (int kk = 0; kk < BNt / 16; ++kk) {
-                    const uint64_t b =
-                        ptx::smem_desc_sw128(v_base + kk * 2048, C::PANEL_KV, 1024);
-                    ptx::mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_S + t * kBN + kk * 8, b, id_pv,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t b = ptx::smem_desc_sw128(v_base + kk * 2048, C::PANEL_KV, 1024);
+                    ptx::mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_P + t * C::PSTRIDE + kk * 8, b,
+                                id_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::tc_commit(&bars->o_done[t]);
             };
@@ -336,23 +353,50 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 const int s1 = (j + 1) % C::NSTAGE;
                 const uint32_t ph1 = ((j + 1) / C::NSTAGE) & 1;
                 bool v_ready = false, k1_ready = false;
-                for (int t = 0; t < kNQ && ok; ++t) {
-                    if (j >= n_t[t]) continue;
-                    ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
-                    if (ok && !v_ready) {
-                        ok = ptx::mbar_wait_or_abort(&bars->v_full[s], ph, p.err, abort);
+                auto wait_k1 = [&]() {
+                    if (!k1_ready) {
+                        ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[s1], ph1, p.err, abort);
+                        k1_ready = true;
+                    }
+                };
+                auto wait_v = [&]() {
+                    if (!v_ready) {
+                        ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[s], ph, p.err, abort);
                         v_ready = true;
                     }
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_pv(t, j);
-                    if (j + 1 < n_t[t]) {
-                        if (!k1_ready) {
-                            ok = ptx::mbar_wait_or_abort(&bars->k_full[s1], ph1, p.err, abort);
-                            k1_ready = true;
+                };
+                if constexpr (C::SEP_P) {
+                    // next S as soon as the softmax holds the current one in registers
+                    for (int t = 0; t < kNQ && ok; ++t) {
+                        if (j + 1 >= n_t[t]) continue;
+                        ok = ptx::mbar_wait_or_abort(&bars->s_free[t], j & 1, p.err, abort);
+                        wait_k1();
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_qk(t, j + 1);
+                    }
+                    for (int t = 0; t < kNQ && ok; ++t) {
+                        if (j >= n_t[t]) continue;
+                        ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
+                        wait_v();
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_pv(t, j);
+                    }
+                } else {
+                    for (int t = 0; t < kNQ && ok; ++t) {
+                        if (j >= n_t[t]) continue;
+                        ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
+                        wait_v();
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_pv(t, j);
+                        if (j + 1 < n_t[t]) {
+                            wait_k1();
+                            if (!ok) break;
                             ptx::tc_fence_after();
+                            issue_qk(t, j + 1);
                         }
-                        if (ok) issue_qk(t, j + 1);
                     }
                 }
                 ptx::tc_commit(&bars->kv_empty[s]);
@@ -363,11 +407,13 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         }
     } else {
         // ================================================= softmax warpgroups
+        ptx::regs_increase<C::REGS_SOFTMAX>();
         const int t = warp >> 2;                 // query tile
         const int quarter = warp & 3;            // TMEM lanes [32 quarter, 32 quarter + 32)
         const int row = quarter * 32 + lane;     // query row within the tile
         const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
         const uint32_t s_addr = lane_base + C::TM_S + t * kBN;
+        const uint32_t p_addr = lane_base + C::TM_P + t * C::PSTRIDE;
         const uint32_t o_addr = lane_base + C::TM_O + t * D;
         const float cl = p.c_log2;
 
@@ -390,8 +436,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         const int nt = n_t[t];
-        // tcgen05.ld / st / wait are warp-collective (.sync.aligned): every
-        // branch that leads to one is made uniform across the warp.
         for (int j = 0; j < nt; ++j) {
             if (!__all_sync(0xffffffffu,
                             ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort))) {
@@ -399,68 +443,90 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 break;
             }
             ptx::tc_fence_after();
-            uint32_t sv[kBN];
+            float sv[kBN];
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c)
                 if (c * 32 < BNt)
                     ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
             ptx::tmem_wait_ld();
+            if constexpr (C::SEP_P) {
+                // S_t is in registers: the next QK_t may overwrite it
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bars->s_free[t]);
+            }
 
-            // ---- mask and tile maximum
-            float tmax = -INFINITY;
+            // ---- mask and tile maximum (eight independent partial maxima)
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+            bool any_valid = true;
             if constexpr (NA) {
                 int kt_, kh_, kw_;
                 na_key_box(g[t], p.KH, j, kt_, kh_, kw_);
                 const bool tv_ok = unsigned(kt_ - wst) < unsigned(p.et);
-                // valid w columns of this tile for this query (16-bit mask)
-                uint32_t wbits = 0;
+                uint32_t wbits = 0;     // valid w columns of this tile for this query
 #pragma unroll
                 for (int c = 0; c < kKW; ++c)
                     wbits |= (unsigned(kw_ + c - wsw) < unsigned(p.ew) ? 1u : 0u) << c;
+                uint32_t hbits = 0;     // valid h rows
+#pragma unroll
+                for (int r = 0; r < kBN / kKW; ++r)
+                    hbits |= (tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh) ? 1u : 0u) << r;
+                any_valid = hbits != 0 && wbits != 0;
 #pragma unroll
                 for (int r = 0; r < kBN / kKW; ++r) {
-                    const bool hv = tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh);
-                    const uint32_t bits = hv ? wbits : 0u;
+                    const uint32_t bits = ((hbits >> r) & 1u) ? wbits : 0u;
 #pragma unroll
                     for (int c = 0; c < kKW; ++c) {
                         const int e = r * kKW + c;
-                        const float x = ((bits >> c) & 1u) ? __uint_as_float(sv[e]) : -INFINITY;
-                        sv[e] = __float_as_uint(x);
-                        tmax = fmaxf(tmax, x);
+                        sv[e] = ((bits >> c) & 1u) ? sv[e] : -INFINITY;
+                        mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
                     }
                 }
             } else {
                 const int valid = p.Nkv - j * kBN;     // keys of this tile inside the sequence
+                if (valid < kBN) {
 #pragma unroll
-                for (int e = 0; e < kBN; ++e) {
-                    float x = __uint_as_float(sv[e]);
-                    if (e >= valid) x = -INFINITY;
-                    sv[e] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
+                    for (int e = 0; e < kBN; ++e)
+                        if (e >= valid) sv[e] = -INFINITY;
                 }
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
             }
+            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float mt = tmax * cl;        // cl > 0: max commutes with the scaling
 
-            // ---- running maximum (moved lazily) and O rescale in TMEM
+            // ---- the previous P V must be done before O is rescaled or P_t rewritten
             const bool want = j == 0 || mt > m + 8.f;   // this row moves its maximum
-            if (j == 0) {
-                m = mt;
-            } else if (__any_sync(0xffffffffu, want)) {
-                // rows that move m scale their O row; the others multiply by 1
-                const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
+            const bool need_o = j > 0 && (C::SEP_P || __any_sync(0xffffffffu, want));
+            if (need_o) {
                 if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
                                                                      p.err, abort))) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
+            }
+            // ---- running maximum (moved lazily) and O rescale in TMEM
+            if (j == 0) {
+                m = mt;
+            } else if (__any_sync(0xffffffffu, want)) {
+                // rows that move m scale their O row; the others multiply by 1
+                const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
                     ptx::tmem_ld32(o_addr + c * 32, ov);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                    for (int e = 0; e < 32; e += 2) {
+                        float a0, a1;
+                        ptx::ffma2(a0, a1, __uint_as_float(ov[e]), __uint_as_float(ov[e + 1]), f, f,
+                                   0.f, 0.f);
+                        ov[e] = __float_as_uint(a0);
+                        ov[e + 1] = __float_as_uint(a1);
+                    }
                     ptx::tmem_st32(o_addr + c * 32, ov);
                 }
                 if (want) {
@@ -468,25 +534,35 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     m = mt;
                 }
             }
-            const float mu = (m == -INFINITY) ? 0.f : m;
+            const float nmu = (m == -INFINITY) ? 0.f : -m;
 
-            // ---- P = 2^(x - m) in bf16 into TMEM (over S), row sum in fp32
-            float sum0 = 0.f, sum1 = 0.f;
+            // ---- P = 2^(x - m) in bf16 into TMEM, row sum in fp32
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            const bool warp_any = __any_sync(0xffffffffu, any_valid);
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 if (c * 32 >= BNt) break;
                 uint32_t pk[16];
+                if (warp_any) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * e]), cl, -mu));
-                    const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * e + 1]), cl, -mu));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[e] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1;
+                        ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nmu,
+                                   nmu);
+                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                        ptx::fadd2(acc[(2 * e) & 7], acc[(2 * e + 1) & 7], acc[(2 * e) & 7],
+                                   acc[(2 * e + 1) & 7], p0, p1);
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
                 }
-                ptx::tmem_st16(s_addr + c * 16, pk);
+                ptx::tmem_st16(p_addr + c * 16, pk);
             }
-            l += sum0 + sum1;
+            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bars->p_ready[t]);
@@ -686,9 +762,21 @@ attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
     using C = TcCfg<D, NA>;
     static int done_mask = 0;
+    static int regs = -1;
     auto kern = tc_attn_kernel<D, NA>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
+    // The warpgroups re-split the launch's register file with setmaxnreg; the
+    // split is only valid for the per-thread count it was computed for.
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kern)) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        regs = fa.numRegs;
+    }
+    if (regs != C::REGS_LAUNCH) return ATTN_ERR_UNSUPPORTED;
     kern<<<grid, C::NT, C::SMEM, c.stream>>>(tq, tk, tv, p);
     return launch_status(NA ? kFamTcNa : kFamTcFlash);
 }

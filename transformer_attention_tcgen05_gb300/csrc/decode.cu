@@ -4,25 +4,32 @@
 // KV head's cache (fak "GPU - the in-kernel forward pass": device-resident KV
 // cache, section 0; the naive one-block-per-head decode attention that
 // section 4 lists as a gap).  The work is HBM-bound (4 FLOP per cache byte),
-// so the design is about streaming the cache once at full bandwidth:
+// so the design is about streaming the cache once at full bandwidth with few
+// instructions per byte:
 //
-//  * grid = splits x Hkv x B.  A CTA owns one contiguous row range of one
-//    (batch, kv-head) cache and serves all G = Hq/Hkv query heads of that KV
-//    head, so every cache byte is read exactly once (GQA head sharing).
-//  * a producer warp streams K and V rows with bulk TMA copies
-//    (cp.async.bulk, L2 evict-first) into a 3-stage shared-memory ring
-//    guarded by mbarriers; 8 consumer warps compute from shared memory.
-//  * consumer lane layout: D/8 lanes per cache row, each lane holding 8
-//    channels (one 128-bit shared load per row); a warp covers 32/(D/8) rows
-//    per instruction.  Partial dot products of 4 row-instructions x G heads
-//    are summed across the row's lanes with a transposing butterfly (each
-//    exchange halves the values a lane keeps), then the online softmax runs
-//    per head in base 2 and P V accumulates with the same lane layout.
+//  * grid = splits x Hkv x B, sized to about one wave of three CTAs per SM.
+//    A CTA owns one contiguous row range of one (batch, kv-head) cache and
+//    serves all G = Hq/Hkv query heads of that KV head, so every cache byte is
+//    read exactly once (GQA head sharing).
+//  * a producer warp streams 32-row chunks of K and V with TMA tensor copies
+//    (128-byte swizzle, L2 evict-first) into a 4-slot shared-memory ring;
+//    chunk i goes to slot i % 4 and is consumed by consumer warp i % 4.
+//  * Q K^T: lane = cache row.  Each lane reads its row in 16-byte chunks (the
+//    swizzle makes the 32 rows' reads bank-conflict free) against q held in
+//    shared memory as fp32 (broadcast reads), with packed fp32x2 FMAs.
+//  * online softmax per head across the warp's 32 rows (butterfly max), in
+//    base 2; P goes to shared memory.
+//  * P V: D/8 lanes per row, 8 channels per lane (one 16-byte swizzled read),
+//    2 or 4 rows per instruction, packed fp32x2 FMAs.
 //  * the CTA merges its warps (log-sum-exp) and writes one partial
 //    (m, l, o) per head to the workspace; the last CTA of a (batch, kv-head)
 //    to arrive (atomic ticket) merges all splits and writes the output, then
 //    resets its ticket so the workspace is ready for the next call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <float.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -31,82 +38,60 @@
 namespace attn {
 namespace {
 
+constexpr int kRowsPerChunk = 32;
+constexpr int kCW = 4;          // consumer warps
+constexpr int kSlots = 4;       // ring slots (one chunk each)
+constexpr int kMaxSplits = 256;
+
 template <int D, int GP>
 struct DecCfg {
-    static constexpr int LPR = D / 8;                 // lanes per cache row
-    static constexpr int LOG_LPR = (LPR == 16) ? 4 : 3;
-    static constexpr int RPI = 32 / LPR;               // rows per warp instruction
-    static constexpr int UNR = 4;                      // row-instructions per warp step
-    static constexpr int RPW = RPI * UNR;              // rows per warp step
-    static constexpr int CW = 8;                       // consumer warps
-    static constexpr int NT = (CW + 1) * 32;
-    static constexpr int SROWS = RPW * CW;             // rows per stage
-    static constexpr int NSTAGE = 3;
-    static constexpr int ROWB = D * 2;                 // bytes per cache row
-    static constexpr int KBYTES = SROWS * ROWB;        // bytes of K (or V) per stage
-    static constexpr int NV = UNR * GP;                // partial scores per lane
-    static constexpr int LOG_NV = (NV >= 32) ? 5 : (NV >= 16) ? 4 : (NV >= 8) ? 3 : (NV >= 4) ? 2 : 1;
-    static constexpr int NH = LOG_NV < LOG_LPR ? LOG_NV : LOG_LPR;   // halving exchanges
-    static constexpr int VPL = NV >> NH;               // values a lane keeps
-    static constexpr int SCORES = RPW * GP;            // scores per warp step
-    // shared memory carve-up (bytes)
+    static constexpr int PANELS = D / 64;
+    static constexpr int PANEL = kRowsPerChunk * 128;       // bytes per 64-channel panel
+    static constexpr int TILE = PANELS * PANEL;             // K (or V) bytes per chunk
+    static constexpr int LPR = D / 8;                       // P V: lanes per row
+    static constexpr int RPI = 32 / LPR;                    // P V: rows per instruction
+    static constexpr int NT = (kCW + 1) * 32;
+    // shared memory (bytes, from a 1024-aligned base)
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = NSTAGE * KBYTES;
-    static constexpr int OFF_S = 2 * NSTAGE * KBYTES;                  // [CW][SCORES] f32
-    static constexpr int OFF_BAR = OFF_S + CW * SCORES * 4;
-    static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 16;
-    // the warp-merge area [CW][GP][D+2] f32 reuses the K stages after the loop
+    static constexpr int OFF_V = kSlots * TILE;
+    static constexpr int OFF_Q = 2 * kSlots * TILE;                      // [GP][D] f32
+    static constexpr int OFF_P = OFF_Q + GP * D * 4;                     // [CW][32][GP] f32
+    static constexpr int OFF_BAR = OFF_P + kCW * kRowsPerChunk * GP * 4;
+    static constexpr int SMEM = OFF_BAR + 2 * kSlots * 8 + 16 + 1024;
+    // the warp-merge area [CW][GP][D+2] f32 reuses the K slots after the loop
     static constexpr int OFF_M = 0;
-    static_assert(CW * GP * (D + 2) * 4 <= NSTAGE * KBYTES, "merge area must fit the K stages");
-    static_assert(NV >= 4, "at least 4 partial scores per lane");
+    static_assert(kCW * GP * (D + 2) * 4 <= kSlots * TILE, "merge area must fit the K slots");
 };
 
 struct DecParams {
-    const __nv_bfloat16 *q, *k, *v;
+    const __nv_bfloat16 *q;
     const int32_t *seq_len;
     __nv_bfloat16 *o;
     int Hq, Hkv, Lmax, G;
-    int splits, split_rows;
+    int splits, split_rows, ws_splits;
     float qscale;
-    float *part_o;           // [units][splits][GP][D]
-    float *part_ml;          // [units][splits][GP][2]
+    float *part_o;           // [units][ws_splits][GP][D]
+    float *part_ml;          // [units][ws_splits][GP][2]
     unsigned *tickets;       // [units]
     unsigned *err;
 };
 
-template <int VN, int LN>
-struct Reduce {
-    // Halving butterfly over LN lanes (xor distances LN/2 .. 1, lane bits of
-    // `sub`): keeps the upper half of the values where the exchanged bit is
-    // set.  When values run out before lanes, the remaining exchanges are
-    // plain all-reduce steps.
-    static __device__ __forceinline__ void run(float *v, int sub) {
-        if constexpr (LN > 1) {
-            constexpr int half = LN / 2;
-            if constexpr (VN > 1) {
-                const bool up = (sub & half) != 0;
-#pragma unroll
-                for (int j = 0; j < VN / 2; ++j) {
-                    const float send = up ? v[j] : v[j + VN / 2];
-                    const float keep = up ? v[j + VN / 2] : v[j];
-                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-                }
-                Reduce<VN / 2, half>::run(v, sub);
-            } else {
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], half);
-                Reduce<1, half>::run(v, sub);
-            }
-        }
-    }
-};
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&x)[8]) {
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
+    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
+    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
 
 template <int D, int GP>
-__global__ void __launch_bounds__(DecCfg<D, GP>::NT, GP >= 8 ? 1 : 2)
-decode_kernel(const DecParams p) {
+__global__ void __launch_bounds__(DecCfg<D, GP>::NT)
+decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+              const DecParams p) {
     using C = DecCfg<D, GP>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *empty = full + C::NSTAGE;
+    uint64_t *empty = full + kSlots;
     __shared__ int s_abort;
     __shared__ unsigned s_last;
 
@@ -121,191 +106,173 @@ decode_kernel(const DecParams p) {
     }
     const int r0 = split * p.split_rows;
     const int r1 = imin(r0 + p.split_rows, L);
-    const int nchunks = r1 > r0 ? cdiv(r1 - r0, C::SROWS) : 0;
+    const int nchunks = r1 > r0 ? cdiv(r1 - r0, kRowsPerChunk) : 0;
 
+    float *q_s = reinterpret_cast<float *>(smem + C::OFF_Q);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NSTAGE; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], C::CW);
+            ptx::mbar_init(&empty[s], 1);
         }
         ptx::fence_barrier_init();
         s_abort = 0;
     }
+    // q of the G heads of this KV head, pre-scaled, fp32 (padding heads are zero)
+    for (int e = threadIdx.x; e < GP * D; e += C::NT) {
+        const int h = e / D, d = e % D;
+        float x = 0.f;
+        if (h < p.G) x = __bfloat162float(p.q[(size_t(b) * p.Hq + kvh * p.G + h) * D + d]) * p.qscale;
+        q_s[e] = x;
+    }
     __syncthreads();
 
-    const size_t cache_base = (size_t(unit) * p.Lmax) * D;
-    float *s_scores = reinterpret_cast<float *>(smem + C::OFF_S);
     float *s_merge = reinterpret_cast<float *>(smem + C::OFF_M);
 
-    if (warp == C::CW) {
+    if (warp == kCW) {
         // ------------------------------------------------ producer warp
         if (lane == 0) {
+            ptx::prefetch_tmap(&tk);
+            ptx::prefetch_tmap(&tv);
             const uint64_t pol = ptx::l2_policy_evict_first();
+            int issued = 0;
             for (int it = 0; it < nchunks; ++it) {
-                const int s = it % C::NSTAGE;
-                if (it >= C::NSTAGE &&
-                    !ptx::mbar_wait(&empty[s], ((it / C::NSTAGE) - 1) & 1, p.err)) {
+                const int s = it % kSlots;
+                if (it >= kSlots && !ptx::mbar_wait(&empty[s], ((it / kSlots) - 1) & 1, p.err)) {
                     s_abort = 1;
                     break;
                 }
-                const int j0 = r0 + it * C::SROWS;
-                const int rows = imin(C::SROWS, r1 - j0);
-                const uint32_t bytes = uint32_t(rows) * C::ROWB;
-                ptx::mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                ptx::bulk_g2s(smem + C::OFF_K + s * C::KBYTES, p.k + cache_base + size_t(j0) * D,
-                              bytes, &full[s], pol);
-                ptx::bulk_g2s(smem + C::OFF_V + s * C::KBYTES, p.v + cache_base + size_t(j0) * D,
-                              bytes, &full[s], pol);
+                const int j0 = r0 + it * kRowsPerChunk;
+                ptx::mbar_arrive_expect_tx(&full[s], 2 * C::TILE);
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                    ptx::tma_load_3d(smem + C::OFF_K + s * C::TILE + pn * C::PANEL, &tk, pn * 64, j0,
+                                     unit, &full[s], pol);
+                    ptx::tma_load_3d(smem + C::OFF_V + s * C::TILE + pn * C::PANEL, &tv, pn * 64, j0,
+                                     unit, &full[s], pol);
+                }
+                issued = it + 1;
+            }
+            if (s_abort) {
+                // let the copies already issued land (bounded) before exiting
+                for (int it = imax(0, issued - kSlots); it < issued; ++it)
+                    ptx::mbar_wait(&full[it % kSlots], (it / kSlots) & 1, nullptr);
             }
         }
     } else {
         // ------------------------------------------------ consumer warps
-        const int r = lane / C::LPR;       // row within a row-instruction
-        const int sub = lane % C::LPR;     // channel group: channels [8 sub, 8 sub + 8)
-        float qv[GP][8], acc[GP][8], m[GP];
-        float lpart = 0.f;                 // partial row sum of head (lane % GP)
+        float m[GP], lrow[GP], acc[GP][8];
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
             m[h] = -INFINITY;
-            const int hq = kvh * p.G + h;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (h < p.G)
-                u = *reinterpret_cast<const uint4 *>(p.q + (size_t(b) * p.Hq + hq) * D + sub * 8);
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                qv[h][2 * j] = bf16_lo(w4[j]) * p.qscale;
-                qv[h][2 * j + 1] = bf16_hi(w4[j]) * p.qscale;
-            }
+            lrow[h] = 0.f;
 #pragma unroll
             for (int d = 0; d < 8; ++d) acc[h][d] = 0.f;
         }
-        float *sc = s_scores + warp * C::SCORES;
+        float *p_s = reinterpret_cast<float *>(smem + C::OFF_P) + warp * kRowsPerChunk * GP;
+        const int grp = lane / C::LPR;       // P V: row within an instruction
+        const int sub = lane % C::LPR;       // P V: channels [8 sub, 8 sub + 8)
+        const int vpanel = sub / 8, vchunk = sub % 8;
 
-        for (int it = 0; it < nchunks; ++it) {
-            const int s = it % C::NSTAGE;
-            if (!ptx::mbar_wait(&full[s], (it / C::NSTAGE) & 1, p.err)) {
+        for (int it = warp; it < nchunks; it += kCW) {
+            const int s = it % kSlots;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[s], (it / kSlots) & 1, p.err))) {
                 s_abort = 1;
                 break;
             }
-            const uint8_t *Kst = smem + C::OFF_K + s * C::KBYTES;
-            const uint8_t *Vst = smem + C::OFF_V + s * C::KBYTES;
-            const int j0 = r0 + it * C::SROWS;
-            const int wrow0 = warp * C::RPW;               // first stage row of this warp
-            const int valid = imin(C::SROWS, r1 - j0) - wrow0;   // rows of this warp in range
-            if (valid > 0) {
-                // ---- partial scores: UNR row-instructions x GP heads
-                float v[C::NV];
+            const uint8_t *Kst = smem + C::OFF_K + s * C::TILE;
+            const uint8_t *Vst = smem + C::OFF_V + s * C::TILE;
+            const int j0 = r0 + it * kRowsPerChunk;
+            const int valid = imin(kRowsPerChunk, r1 - j0);
+
+            // ---- scores: lane = cache row
+            float sc[GP];
+            {
+                float a0[GP], a1[GP];
 #pragma unroll
-                for (int i = 0; i < C::UNR; ++i) {
-                    const int row = wrow0 + i * C::RPI + r;
-                    const uint4 u = *reinterpret_cast<const uint4 *>(Kst + row * C::ROWB + sub * 16);
-                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                for (int h = 0; h < GP; ++h) a0[h] = a1[h] = 0.f;
+                const int r = lane;
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const int pn = c / 8, cc = c % 8;
+                    const uint4 u = *reinterpret_cast<const uint4 *>(
+                        Kst + pn * C::PANEL + r * 128 + ((cc ^ (r & 7)) << 4));
                     float kx[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        kx[2 * j] = bf16_lo(w4[j]);
-                        kx[2 * j + 1] = bf16_hi(w4[j]);
-                    }
+                    bf16x8_to_f32(u, kx);
 #pragma unroll
                     for (int h = 0; h < GP; ++h) {
-                        float a = 0.f;
-#pragma unroll
-                        for (int d = 0; d < 8; ++d) a = fmaf(qv[h][d], kx[d], a);
-                        v[i * GP + h] = a;
+                        const float4 qa = *reinterpret_cast<const float4 *>(q_s + h * D + c * 8);
+                        const float4 qb = *reinterpret_cast<const float4 *>(q_s + h * D + c * 8 + 4);
+                        ptx::ffma2(a0[h], a1[h], kx[0], kx[1], qa.x, qa.y, a0[h], a1[h]);
+                        ptx::ffma2(a0[h], a1[h], kx[2], kx[3], qa.z, qa.w, a0[h], a1[h]);
+                        ptx::ffma2(a0[h], a1[h], kx[4], kx[5], qb.x, qb.y, a0[h], a1[h]);
+                        ptx::ffma2(a0[h], a1[h], kx[6], kx[7], qb.z, qb.w, a0[h], a1[h]);
                     }
                 }
-                Reduce<C::NV, C::LPR>::run(v, sub);
-                // lane keeps flat indices f = blk * VPL + j (f = i * GP + h)
-                const int blk = sub >> (C::LOG_LPR - C::NH);
 #pragma unroll
-                for (int j = 0; j < C::VPL; ++j) {
-                    const int f = blk * C::VPL + j;
-                    const int i = f / GP, h = f % GP;
-                    const int wr = i * C::RPI + r;         // row within the warp step
-                    sc[wr * GP + h] = (wr < valid) ? v[j] : -INFINITY;
-                }
-                __syncwarp();
-                // ---- per-head maximum of this step and the rescale factors
-                float mx = -INFINITY;
-#pragma unroll
-                for (int e = lane; e < C::SCORES; e += 32) mx = fmaxf(mx, sc[e]);
-#pragma unroll
-                for (int off = GP; off < 32; off <<= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                float alpha[GP];
-#pragma unroll
-                for (int h = 0; h < GP; ++h) {
-                    const float mh = __shfl_sync(0xffffffffu, mx, h);
-                    const float mn = fmaxf(m[h], mh);
-                    alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(m[h] - mn);
-                    m[h] = mn;
-                }
-                // ---- probabilities (in place) and the lane's row-sum share
-                const int myh = lane % GP;
-                float mine = m[0];
-#pragma unroll
-                for (int h = 1; h < GP; ++h)
-                    if (myh == h) mine = m[h];
-                float ps = 0.f;
-#pragma unroll
-                for (int e = lane; e < C::SCORES; e += 32) {
-                    const float pe = (mine == -INFINITY) ? 0.f : exp2f(sc[e] - mine);
-                    sc[e] = pe;
-                    ps += pe;
-                }
-                float amine = alpha[0];
-#pragma unroll
-                for (int h = 1; h < GP; ++h)
-                    if (myh == h) amine = alpha[h];
-                lpart = lpart * amine + ps;
-                __syncwarp();
-                // ---- O = O * alpha + P V
-#pragma unroll
-                for (int h = 0; h < GP; ++h)
-#pragma unroll
-                    for (int d = 0; d < 8; ++d) acc[h][d] *= alpha[h];
-#pragma unroll
-                for (int i = 0; i < C::UNR; ++i) {
-                    const int wr = i * C::RPI + r;
-                    if (wr < valid) {
-                        const uint4 u =
-                            *reinterpret_cast<const uint4 *>(Vst + (wrow0 + wr) * C::ROWB + sub * 16);
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-                        float vx[8];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            vx[2 * j] = bf16_lo(w4[j]);
-                            vx[2 * j + 1] = bf16_hi(w4[j]);
-                        }
-                        float pr[GP];
-#pragma unroll
-                        for (int h = 0; h < GP; ++h) pr[h] = sc[wr * GP + h];
-#pragma unroll
-                        for (int h = 0; h < GP; ++h)
-#pragma unroll
-                            for (int d = 0; d < 8; ++d) acc[h][d] = fmaf(pr[h], vx[d], acc[h][d]);
-                    }
-                }
-                __syncwarp();
+                for (int h = 0; h < GP; ++h) sc[h] = (lane < valid) ? a0[h] + a1[h] : -INFINITY;
             }
+
+            // ---- online softmax per head over the warp's 32 rows
+            float alpha[GP];
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                float mx = sc[h];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float mn = fmaxf(m[h], mx);
+                alpha[h] = (mn == -INFINITY) ? 1.f : ptx::ex2(m[h] - mn);
+                const float pr = (mn == -INFINITY) ? 0.f : ptx::ex2(sc[h] - mn);
+                m[h] = mn;
+                lrow[h] = lrow[h] * alpha[h] + pr;
+                p_s[lane * GP + h] = pr;
+            }
+            __syncwarp();
+
+            // ---- O = O * alpha + P V
+#pragma unroll
+            for (int h = 0; h < GP; ++h)
+#pragma unroll
+                for (int d = 0; d < 8; d += 2)
+                    ptx::ffma2(acc[h][d], acc[h][d + 1], acc[h][d], acc[h][d + 1], alpha[h], alpha[h],
+                               0.f, 0.f);
+#pragma unroll 4
+            for (int i = 0; i < kRowsPerChunk / C::RPI; ++i) {
+                const int r = i * C::RPI + grp;
+                if (r < valid) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(
+                        Vst + vpanel * C::PANEL + r * 128 + ((vchunk ^ (r & 7)) << 4));
+                    float vx[8];
+                    bf16x8_to_f32(u, vx);
+                    float pr[GP];
+#pragma unroll
+                    for (int h = 0; h < GP; ++h) pr[h] = p_s[r * GP + h];
+#pragma unroll
+                    for (int h = 0; h < GP; ++h)
+#pragma unroll
+                        for (int d = 0; d < 8; d += 2)
+                            ptx::ffma2(acc[h][d], acc[h][d + 1], vx[d], vx[d + 1], pr[h], pr[h],
+                                       acc[h][d], acc[h][d + 1]);
+                }
+            }
+            __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&empty[s]);
         }
 
-        // ---- warp totals: sum the row groups (lanes with equal `sub`)
+        // ---- warp totals: P V over the row groups, row sums over the lanes
 #pragma unroll
-        for (int h = 0; h < GP; ++h)
+        for (int h = 0; h < GP; ++h) {
 #pragma unroll
             for (int d = 0; d < 8; ++d)
 #pragma unroll
                 for (int off = C::LPR; off < 32; off <<= 1)
                     acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], off);
-        // row sums: lanes with equal (lane % GP) hold shares of one head
 #pragma unroll
-        for (int off = GP; off < 32; off <<= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
-        // every consumer warp is past its last stage read before the merge
-        // area (aliasing the K stages) is written
-        ptx::named_barrier_sync(1, C::CW * 32);
+            for (int off = 16; off > 0; off >>= 1)
+                lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], off);
+        }
+        // every consumer warp is past its last slot read before the merge
+        // area (aliasing the K slots) is written
+        ptx::named_barrier_sync(1, kCW * 32);
         float *wm = s_merge + warp * GP * (D + 2);
         if (lane < C::LPR) {
 #pragma unroll
@@ -313,9 +280,12 @@ decode_kernel(const DecParams p) {
 #pragma unroll
                 for (int d = 0; d < 8; ++d) wm[h * (D + 2) + sub * 8 + d] = acc[h][d];
         }
-        if (lane < GP) {
-            wm[lane * (D + 2) + D] = m[lane];
-            wm[lane * (D + 2) + D + 1] = lpart;
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                wm[h * (D + 2) + D] = m[h];
+                wm[h * (D + 2) + D + 1] = lrow[h];
+            }
         }
     }
     __syncthreads();
@@ -323,15 +293,15 @@ decode_kernel(const DecParams p) {
     // ---- CTA merge of the consumer warps -> one partial per head
     const bool aborted = s_abort != 0;
     if (!aborted) {
-        float *po = p.part_o + (size_t(unit) * p.splits + split) * GP * D;
-        float *pml = p.part_ml + (size_t(unit) * p.splits + split) * GP * 2;
+        float *po = p.part_o + (size_t(unit) * p.ws_splits + split) * GP * D;
+        float *pml = p.part_ml + (size_t(unit) * p.ws_splits + split) * GP * 2;
         for (int e = threadIdx.x; e < GP * D; e += C::NT) {
             const int h = e / D, d = e % D;
             float M = -INFINITY;
-            for (int w = 0; w < C::CW; ++w) M = fmaxf(M, s_merge[(w * GP + h) * (D + 2) + D]);
+            for (int w = 0; w < kCW; ++w) M = fmaxf(M, s_merge[(w * GP + h) * (D + 2) + D]);
             float O = 0.f, Lsum = 0.f;
             if (M != -INFINITY) {
-                for (int w = 0; w < C::CW; ++w) {
+                for (int w = 0; w < kCW; ++w) {
                     const float *wm = s_merge + (w * GP + h) * (D + 2);
                     const float f = exp2f(wm[D] - M);   // -inf -> 0
                     O += wm[d] * f;
@@ -359,8 +329,8 @@ decode_kernel(const DecParams p) {
     __threadfence();
     for (int e = threadIdx.x; e < p.G * D; e += C::NT) {
         const int h = e / D, d = e % D;
-        const float *pml = p.part_ml + size_t(unit) * p.splits * GP * 2;
-        const float *po = p.part_o + size_t(unit) * p.splits * GP * D;
+        const float *pml = p.part_ml + size_t(unit) * p.ws_splits * GP * 2;
+        const float *po = p.part_o + size_t(unit) * p.ws_splits * GP * D;
         float M = -INFINITY;
         for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(pml + (s * GP + h) * 2));
         float O = 0.f, Lsum = 0.f;
@@ -376,27 +346,59 @@ decode_kernel(const DecParams p) {
     if (threadIdx.x == 0) p.tickets[unit] = 0u;   // ready for the next call
 }
 
-int splits_for(int B, int Hkv, int Lmax, int srows) {
-    const int chunks = cdiv(Lmax, srows);
-    // about four stage-chunks per CTA; at least enough CTAs to cover the GPU
-    int splits = cdiv(chunks, 4);
+// Largest split count a call can use (sets the workspace layout).
+int max_splits_for(int Lmax) {
+    return imin(kMaxSplits, imax(1, cdiv(Lmax, kRowsPerChunk) / (2 * kCW)));
+}
+
+// Splits per (batch, kv-head): about one wave of three CTAs per SM, each CTA
+// at least two 32-row chunks per consumer warp.
+int splits_for(int B, int Hkv, int Lmax, int sm_count) {
     const int units = B * Hkv;
-    while (splits < chunks && units * splits < 2 * 152) ++splits;
-    return imax(1, imin(splits, 256));
+    const int splits = imax(1, (3 * sm_count) / imax(units, 1));
+    return imax(1, imin(splits, max_splits_for(Lmax)));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_dec() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 3D map over the cache [units][Lmax][D], box {64, 32, 1}, 128-byte swizzle.
+bool cache_tmap(CUtensorMap *m, const void *base, int units, int Lmax, int D) {
+    auto fn = encode_fn_dec();
+    if (!fn) return false;
+    const cuuint64_t gdim[3] = {cuuint64_t(D), cuuint64_t(Lmax), cuuint64_t(units)};
+    const cuuint64_t gstride[2] = {cuuint64_t(D) * 2, cuuint64_t(Lmax) * D * 2};
+    const cuuint32_t box[3] = {64, kRowsPerChunk, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, int GP>
-attn_status_t launch(const Ctx &c, DecParams p, int B) {
+attn_status_t launch(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv, DecParams p,
+                     int B) {
     using C = DecCfg<D, GP>;
     static int done_mask = 0;
     auto kern = decode_kernel<D, GP>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
-    kern<<<dim3(p.splits, p.Hkv, B), C::NT, C::SMEM, c.stream>>>(p);
+    kern<<<dim3(p.splits, p.Hkv, B), C::NT, C::SMEM, c.stream>>>(tk, tv, p);
     return launch_status(kFamDecode);
 }
-
-int srows_for(int D) { return D == 128 ? DecCfg<128, 4>::SROWS : DecCfg<64, 4>::SROWS; }
 
 int gp_for(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 
@@ -405,7 +407,7 @@ int gp_for(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D) {
     if (B < 1 || Hkv < 1 || Hq < Hkv || Lmax < 1 || (D != 64 && D != 128)) return 0;
     const int GP = gp_for(Hq / Hkv);
-    const int splits = splits_for(B, Hkv, Lmax, srows_for(D));
+    const int splits = max_splits_for(Lmax);
     const size_t units = size_t(B) * Hkv;
     size_t bytes = units * splits * GP * D * sizeof(float);
     bytes = (bytes + 255) & ~size_t(255);
@@ -423,39 +425,40 @@ attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void 
     const size_t need = decode_workspace_bytes(B, Hq, Hkv, Lmax, D);
     if (ws_bytes < need) return ATTN_ERR_RESOURCE;
     if (B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tk, tv;
+    if (!cache_tmap(&tk, k, B * Hkv, Lmax, D) || !cache_tmap(&tv, v, B * Hkv, Lmax, D))
+        return ATTN_ERR_CUDA;
     DecParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.k = static_cast<const __nv_bfloat16 *>(k);
-    p.v = static_cast<const __nv_bfloat16 *>(v);
     p.seq_len = seq_len;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
-    const int srows = srows_for(D);
-    p.splits = splits_for(B, Hkv, Lmax, srows);
-    p.split_rows = cdiv(cdiv(Lmax, p.splits), srows) * srows;
+    p.ws_splits = max_splits_for(Lmax);
+    p.splits = splits_for(B, Hkv, Lmax, c.sm_count);
+    p.split_rows = cdiv(cdiv(Lmax, p.splits), kRowsPerChunk) * kRowsPerChunk;
     p.qscale = scale * kLog2e;
     const size_t units = size_t(B) * Hkv;
     uint8_t *w = static_cast<uint8_t *>(ws);
     size_t off = 0;
     p.part_o = reinterpret_cast<float *>(w + off);
-    off = (off + units * p.splits * GP * D * sizeof(float) + 255) & ~size_t(255);
+    off = (off + units * p.ws_splits * GP * D * sizeof(float) + 255) & ~size_t(255);
     p.part_ml = reinterpret_cast<float *>(w + off);
-    off = (off + units * p.splits * GP * 2 * sizeof(float) + 255) & ~size_t(255);
+    off = (off + units * p.ws_splits * GP * 2 * sizeof(float) + 255) & ~size_t(255);
     p.tickets = reinterpret_cast<unsigned *>(w + off);
     p.err = c.err;
     if (D == 128) {
         switch (GP) {
-            case 1: return launch<128, 1>(c, p, B);
-            case 2: return launch<128, 2>(c, p, B);
-            case 4: return launch<128, 4>(c, p, B);
-            default: return launch<128, 8>(c, p, B);
+            case 1: return launch<128, 1>(c, tk, tv, p, B);
+            case 2: return launch<128, 2>(c, tk, tv, p, B);
+            case 4: return launch<128, 4>(c, tk, tv, p, B);
+            default: return launch<128, 8>(c, tk, tv, p, B);
         }
     }
     switch (GP) {
-        case 1: return launch<64, 1>(c, p, B);
-        case 2: return launch<64, 2>(c, p, B);
-        case 4: return launch<64, 4>(c, p, B);
-        default: return launch<64, 8>(c, p, B);
+        case 1: return launch<64, 1>(c, tk, tv, p, B);
+        case 2: return launch<64, 2>(c, tk, tv, p, B);
+        case 4: return launch<64, 4>(c, tk, tv, p, B);
+        default: return launch<64, 8>(c, tk, tv, p, B);
     }
 }
 

@@ -314,6 +314,13 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Three-input fp32 maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_increase() {

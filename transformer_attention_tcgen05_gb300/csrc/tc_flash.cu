@@ -443,64 +443,89 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 break;
             }
             ptx::tc_fence_after();
-            float sv[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                if (c * 32 < BNt)
-                    ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
-            ptx::tmem_wait_ld();
-            if constexpr (C::SEP_P) {
-                // S_t is in registers: the next QK_t may overwrite it
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&bars->s_free[t]);
-            }
 
-            // ---- mask and tile maximum (eight independent partial maxima)
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-            bool any_valid = true;
+            // ---- neighborhood window of this row against the key tile:
+            //      additive 0 / -inf biases per w column and per h row
+            float wb[NA ? kKW : 1], hb[NA ? kBN / kKW : 1];
+            bool warp_any = true;
             if constexpr (NA) {
                 int kt_, kh_, kw_;
                 na_key_box(g[t], p.KH, j, kt_, kh_, kw_);
                 const bool tv_ok = unsigned(kt_ - wst) < unsigned(p.et);
-                uint32_t wbits = 0;     // valid w columns of this tile for this query
+                bool wany = false, hany = false;
 #pragma unroll
-                for (int c = 0; c < kKW; ++c)
-                    wbits |= (unsigned(kw_ + c - wsw) < unsigned(p.ew) ? 1u : 0u) << c;
-                uint32_t hbits = 0;     // valid h rows
-#pragma unroll
-                for (int r = 0; r < kBN / kKW; ++r)
-                    hbits |= (tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh) ? 1u : 0u) << r;
-                any_valid = hbits != 0 && wbits != 0;
+                for (int c = 0; c < kKW; ++c) {
+                    const bool v = unsigned(kw_ + c - wsw) < unsigned(p.ew);
+                    wb[c] = v ? 0.f : -INFINITY;
+                    wany |= v;
+                }
 #pragma unroll
                 for (int r = 0; r < kBN / kKW; ++r) {
-                    const uint32_t bits = ((hbits >> r) & 1u) ? wbits : 0u;
+                    const bool v = tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh);
+                    hb[r] = v ? 0.f : -INFINITY;
+                    hany |= v;
+                }
+                // a warp none of whose 32 windows reaches this tile skips it
+                warp_any = __any_sync(0xffffffffu, wany && hany);
+            }
+
+            float sv[kBN];
+            if (warp_any) {
 #pragma unroll
-                    for (int c = 0; c < kKW; ++c) {
-                        const int e = r * kKW + c;
-                        sv[e] = ((bits >> c) & 1u) ? sv[e] : -INFINITY;
-                        mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+                for (int c = 0; c < kBN / 32; ++c)
+                    if (c * 32 < BNt)
+                        ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                ptx::tmem_wait_ld();
+            }
+            if constexpr (C::SEP_P) {
+                // S_t is in registers (or not needed): the next QK_t may overwrite it
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bars->s_free[t]);
+            }
+
+            // ---- mask and tile maximum
+            float mt = -INFINITY;
+            if (warp_any) {
+                if constexpr (NA) {
+#pragma unroll
+                    for (int r = 0; r < kBN / kKW; ++r) {
+                        if (r < p.KH) {
+#pragma unroll
+                            for (int c = 0; c < kKW; c += 2) {
+                                float b0, b1;
+                                ptx::fadd2(b0, b1, wb[c], wb[c + 1], hb[r], hb[r]);
+                                ptx::fadd2(sv[r * kKW + c], sv[r * kKW + c + 1], sv[r * kKW + c],
+                                           sv[r * kKW + c + 1], b0, b1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < kKW; ++c) sv[r * kKW + c] = -INFINITY;
+                        }
+                    }
+                } else {
+                    const int valid = p.Nkv - j * kBN;     // keys of this tile inside the sequence
+                    if (valid < kBN) {
+#pragma unroll
+                        for (int e = 0; e < kBN; ++e)
+                            if (e >= valid) sv[e] = -INFINITY;
                     }
                 }
-            } else {
-                const int valid = p.Nkv - j * kBN;     // keys of this tile inside the sequence
-                if (valid < kBN) {
+                float mx[8];
 #pragma unroll
-                    for (int e = 0; e < kBN; ++e)
-                        if (e >= valid) sv[e] = -INFINITY;
-                }
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-                for (int e = 0; e < kBN; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+                for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = ptx::fmax3(mx[i], sv[e + i], sv[e + 8 + i]);
+                const float tmax = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
+                                              ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                mt = tmax * cl;        // cl > 0: max commutes with the scaling
             }
-            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float mt = tmax * cl;        // cl > 0: max commutes with the scaling
 
             // ---- the previous P V must be done before O is rescaled or P_t rewritten
             const bool want = j == 0 || mt > m + 8.f;   // this row moves its maximum
-            const bool need_o = j > 0 && (C::SEP_P || __any_sync(0xffffffffu, want));
-            if (need_o) {
+            const bool any_want = __any_sync(0xffffffffu, want);
+            if (j > 0 && (C::SEP_P || any_want)) {
                 if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
                                                                      p.err, abort))) {
                     ok = false;
@@ -511,7 +536,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             // ---- running maximum (moved lazily) and O rescale in TMEM
             if (j == 0) {
                 m = mt;
-            } else if (__any_sync(0xffffffffu, want)) {
+            } else if (any_want) {
                 // rows that move m scale their O row; the others multiply by 1
                 const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
 #pragma unroll
@@ -540,7 +565,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            const bool warp_any = __any_sync(0xffffffffu, any_valid);
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 if (c * 32 >= BNt) break;

@@ -436,6 +436,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         const int nt = n_t[t];
+        // neighborhood: key sub-box counters (w fastest, then h, then t) and the
+        // w-column biases, recomputed only when the w chunk changes
+        int tc = 0, hc = 0, wc = 0, cur_wc = -1;
+        float wb[NA ? kKW : 1];
+        bool wany = false;
         for (int j = 0; j < nt; ++j) {
             if (!__all_sync(0xffffffffu,
                             ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort))) {
@@ -446,19 +451,29 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
             // ---- neighborhood window of this row against the key tile:
             //      additive 0 / -inf biases per w column and per h row
-            float wb[NA ? kKW : 1], hb[NA ? kBN / kKW : 1];
+            float hb[NA ? kBN / kKW : 1];
             bool warp_any = true;
             if constexpr (NA) {
-                int kt_, kh_, kw_;
-                na_key_box(g[t], p.KH, j, kt_, kh_, kw_);
-                const bool tv_ok = unsigned(kt_ - wst) < unsigned(p.et);
-                bool wany = false, hany = false;
+                const int kt_ = g[t].u0t + tc, kh_ = g[t].u0h + hc * p.KH, kw_ = g[t].u0w + wc * kKW;
+                if (wc != cur_wc) {        // uniform: the same tile sequence in every thread
+                    wany = false;
 #pragma unroll
-                for (int c = 0; c < kKW; ++c) {
-                    const bool v = unsigned(kw_ + c - wsw) < unsigned(p.ew);
-                    wb[c] = v ? 0.f : -INFINITY;
-                    wany |= v;
+                    for (int c = 0; c < kKW; ++c) {
+                        const bool v = unsigned(kw_ + c - wsw) < unsigned(p.ew);
+                        wb[c] = v ? 0.f : -INFINITY;
+                        wany |= v;
+                    }
+                    cur_wc = wc;
                 }
+                if (++wc == g[t].nwc) {
+                    wc = 0;
+                    if (++hc == g[t].nhc) {
+                        hc = 0;
+                        ++tc;
+                    }
+                }
+                const bool tv_ok = unsigned(kt_ - wst) < unsigned(p.et);
+                bool hany = false;
 #pragma unroll
                 for (int r = 0; r < kBN / kKW; ++r) {
                     const bool v = tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh);

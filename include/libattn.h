@@ -127,6 +127,32 @@ ATTN_API attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const
 ATTN_API size_t attn_decode_gqa_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
 
 /*
+ * attn_decode_gqa without a workspace argument, for callers that cannot hand
+ * this library any device memory beyond the tensors themselves: a host that
+ * owns all device memory through its own allocator and gives plugins only
+ * inputs and outputs, or a steady-state decode loop that must not call
+ * cudaMalloc (it can synchronise the whole device) between tokens.  There is
+ * no counterpart on the pages; this is an interface convenience only.
+ *
+ * Arguments, layouts, math and results are those of attn_decode_gqa.  The
+ * split partials and arrival counters live in a 4 MiB array that is part of
+ * the library's device image: every GPU that loads the library holds it until
+ * the process exits.  Nothing is allocated per call.
+ *   - Limit: the call needs about B*Hkv*splits*G'*(D+2)*4 bytes (G' = Hq/Hkv
+ *     rounded up to a power of two; splits <= 3*SMs/(B*Hkv), at least 1); a
+ *     problem that does not fit the 4 MiB returns ATTN_ERR_RESOURCE.
+ *   - Every call on a device shares the array and leaves its contents behind;
+ *     each call zeroes the counters it uses first.  Calls that may overlap on
+ *     the GPU (other streams, other host threads) race: serialise them.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call outside any stream capture.
+ */
+ATTN_API attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_cache,
+                                               const void *v_cache, const int32_t *seq_len,
+                                               void *o, int B, int Hq, int Hkv, int Lmax, int D,
+                                               attn_dtype_t dtype, float scale, void *stream);
+
+/*
  * 3D neighborhood attention with NATTEN boundary windows.
  *   q, k, v, o [B, heads, N, D] with N = T * Hg * W tokens in row-major
  *   (t, h, w) order.  kernel: HOST int[3], the requested window per axis; each

@@ -28,6 +28,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <float.h>
+#include <math.h>
 
 #include <mutex>
 
@@ -462,4 +463,118 @@ attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void 
     }
 }
 
+// ------------------------------------------------ allocation-free variant
+//
+// Some callers cannot provide the workspace the split-KV combine needs: a host
+// that owns every byte of device memory through its own allocator and hands a
+// plugin nothing but input and output tensors, or a steady-state decode loop
+// that must not call cudaMalloc (which can synchronise the whole device) between
+// tokens.  attn_decode_gqa_noalloc serves them from a fixed scratch array that
+// is part of this library's device image: every GPU that loads the library
+// holds these kStaticScratchBytes until the process exits, and no call
+// allocates anything.
+//
+// The array is shared by every call on a device and keeps the previous call's
+// contents; each call clears the arrival counters it uses before launching.
+// Calls that overlap on the GPU (different streams, or several host threads)
+// race on the array: serialise them.
+//
+// The first call on a device looks the array's device address up
+// (cudaGetSymbolAddress, with that device current); make that first call
+// before any stream capture.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB per device
+
+__device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+uint8_t *g_scratch_ptr[kMaxScratchDevices];
+std::mutex g_scratch_mu;
+
+// Device address of g_decode_scratch on the current device (looked up once).
+attn_status_t scratch_address(int device, uint8_t **out) {
+    if (device < 0 || device >= kMaxScratchDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[device]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        g_scratch_ptr[device] = static_cast<uint8_t *>(ptr);
+    }
+    *out = g_scratch_ptr[device];
+    return ATTN_OK;
+}
+
+}  // namespace
+
 }  // namespace attn
+
+extern "C" attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_cache,
+                                                 const void *v_cache, const int32_t *seq_len,
+                                                 void *o, int B, int Hq, int Hkv, int Lmax, int D,
+                                                 attn_dtype_t dtype, float scale, void *stream) {
+    using namespace attn;
+    auto a16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+    if (!q || !k_cache || !v_cache || !seq_len || !o) return ATTN_ERR_INVALID_ARG;
+    if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(o)) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (D != 32 && D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_BF16 || D == 32 || Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)Lmax * D >= (1ll << 31) || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (o == q || o == k_cache || o == v_cache) return ATTN_ERR_INVALID_ARG;
+    Ctx c;
+    attn_status_t st = context_for(stream, &c);
+    if (st != ATTN_OK) return st;
+    uint8_t *scratch = nullptr;
+    st = scratch_address(c.device, &scratch);
+    if (st != ATTN_OK) return st;
+
+    const int G = Hq / Hkv;
+    const int GP = gp_for(G);
+    const size_t units = size_t(B) * Hkv;
+    DecParams p{};
+    p.splits = splits_for(B, Hkv, Lmax, c.sm_count);
+    p.ws_splits = p.splits;                     // tight layout: only the splits this call uses
+    size_t off_ml = (units * p.splits * GP * D * sizeof(float) + 255) & ~size_t(255);
+    size_t off_t = (off_ml + units * p.splits * GP * 2 * sizeof(float) + 255) & ~size_t(255);
+    const size_t need = off_t + units * sizeof(unsigned);
+    if (need > kStaticScratchBytes) return ATTN_ERR_RESOURCE;   // problem too large for the array
+
+    CUtensorMap tk, tv;
+    if (!cache_tmap(&tk, k_cache, B * Hkv, Lmax, D) || !cache_tmap(&tv, v_cache, B * Hkv, Lmax, D))
+        return ATTN_ERR_CUDA;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.seq_len = seq_len;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
+    p.split_rows = cdiv(cdiv(Lmax, p.splits), kRowsPerChunk) * kRowsPerChunk;
+    p.qscale = (scale > 0.f && isfinite(scale) ? scale : 1.0f / sqrtf(float(D))) * kLog2e;
+    p.part_o = reinterpret_cast<float *>(scratch);
+    p.part_ml = reinterpret_cast<float *>(scratch + off_ml);
+    p.tickets = reinterpret_cast<unsigned *>(scratch + off_t);
+    p.err = c.err;
+    // the arrival counters must start at zero whatever the previous call left
+    if (cudaMemsetAsync(p.tickets, 0, units * sizeof(unsigned), c.stream) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    if (D == 128) {
+        switch (GP) {
+            case 1: return launch<128, 1>(c, tk, tv, p, B);
+            case 2: return launch<128, 2>(c, tk, tv, p, B);
+            case 4: return launch<128, 4>(c, tk, tv, p, B);
+            default: return launch<128, 8>(c, tk, tv, p, B);
+        }
+    }
+    switch (GP) {
+        case 1: return launch<64, 1>(c, tk, tv, p, B);
+        case 2: return launch<64, 2>(c, tk, tv, p, B);
+        case 4: return launch<64, 4>(c, tk, tv, p, B);
+        default: return launch<64, 8>(c, tk, tv, p, B);
+    }
+}

@@ -28,6 +28,9 @@ enum KernelFamily : int {
 
 void count_launch(int family);
 
+// The per-device context (stream, device error word, SM count) of a call.
+attn_status_t context_for(void *stream, Ctx *c);
+
 // Converts the result of a launch into a status (and counts it on success).
 attn_status_t launch_status(int family);
 

@@ -311,13 +311,21 @@ def ours(args, rank, world, dev_index):
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None."""
+    """DRAM bytes (read + write) per launch of `kernel` from one ncu capture
+    recorded in profiles/traffic.json, or None when there is none or the
+    kernel's source file has changed since the counters were taken."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        d = json.load(open(p))
-        return d.get(kernel, {}).get("dram_bytes_per_launch")
+        e = json.load(open(p)).get(kernel)
+        if not e:
+            return None
+        src = os.path.join(ROOT, e["source"])
+        if hashlib.sha1(open(src, "rb").read()).hexdigest() != e["source_sha1"]:
+            return None
+        return e["dram_bytes_per_launch"]
     except Exception:
         return None
 

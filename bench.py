@@ -262,14 +262,12 @@ def ours(args, rank, world, dev_index):
     e_ms = e_start.elapsed_time(e_stop) / e_steps
 
     if dist:
-        t = torch.tensor([ms, e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e_ms = float(t[0]), float(t[1])
+        ms, e_ms = max_over_ranks([ms, e_ms], dist, dev)
     if rank != 0:
         if dist: dist.destroy_process_group()
         return None
 
-    tflops = STEP_FLOPS * world / (ms * 1e-3) / 1e12
+    tflops = job_throughput(STEP_FLOPS, world, ms)
     comp = {
         "joint": {"ms": kms["joint"], "tflops": flops_joint() / (kms["joint"] * 1e-3) / 1e12},
         "na3d": {"ms": kms["na"], "tflops": flops_na() / (kms["na"] * 1e-3) / 1e12},
@@ -298,7 +296,7 @@ def ours(args, rank, world, dev_index):
         "data": "synthetic (seeded N(0,1), bf16)", "config": CONFIG,
         "components": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in comp.items()},
         "roofline": roof,
-        "e2e": {"value": round(STEP_FLOPS * world / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_throughput(STEP_FLOPS, world, e_ms), 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": e2e.h2d,
                 "d2h_bytes_per_step": e2e.d2h},
         "gpu_launches": int(n1 - n0),
@@ -308,6 +306,20 @@ def ours(args, rank, world, dev_index):
         line["cpu_baseline"] = cpu_baseline(step.host, budget_s=args.cpu_budget)
     if dist: dist.destroy_process_group()
     return line
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    step time of a weak-scaling run)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(step_flops: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs the full step (replicas)."""
+    return step_flops * world / (ms_per_step * 1e-3) / 1e12
 
 
 def load_traffic(kernel: str):

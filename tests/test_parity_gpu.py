@@ -261,7 +261,8 @@ def test_joint_fp32_full_compare(ta):
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_tc_tile_building_blocks(ta, D):
-    """Both MMA forms on one tile: S = q k^T (smem x smem) and O = P v (TMEM x smem)."""
+    """The MMA forms on one tile: S = q k^T + q16 k16^T (128B- and 32B-swizzled smem
+    operands) and O = P v (TMEM x MN-major smem)."""
     import ctypes
     import torch
     from workloads import bf16_round, bf16_to_f32
@@ -282,7 +283,8 @@ def test_tc_tile_building_blocks(ta, D):
     assert st == 0
     assert ta.device_status() == 0
     f = lambda x: bf16_to_f32(x).astype(np.float64)
-    np.testing.assert_allclose(S.cpu().numpy(), f(q) @ f(k).T, rtol=0, atol=1e-3)
+    expect_s = f(q) @ f(k).T + f(q)[:, :16] @ f(k)[:, :16].T
+    np.testing.assert_allclose(S.cpu().numpy(), expect_s, rtol=0, atol=1e-3)
     np.testing.assert_allclose(O.cpu().numpy(), f(P) @ f(v), rtol=0, atol=1e-3)
 
 
@@ -366,4 +368,89 @@ def test_na3d_large_full_size_sampled_rows(ta):
     ref = oracle.na3d_fwd(*_f64(x, w), w.grid, w.kernel, rows=rows)
     got = to_host64(o).reshape(-1, w.D)[rows]
     assert_close(got, ref, "bf16", "na3d large sampled")
+    assert ta.device_status() == 0
+
+
+@pytest.mark.parametrize("scale", [0.01, 1.0])
+def test_tc_na3d_explicit_scale(ta, scale):
+    # the window penalty channels are sized from the scale: tiny and large scales
+    w = WORKLOADS["na3d_21x60x104_k11"].with_(grid=(5, 12, 20), kernel=(3, 5, 7), H=1, N=5 * 12 * 20,
+                                             seed=7800 + int(scale * 100))
+    x = make_inputs(w)
+    with launched(ta, "tc_na"):
+        o = ta.na3d_fwd(*_dev(x, w), w.grid, w.kernel, scale=scale)
+    ref = oracle.na3d_fwd(*_f64(x, w), w.grid, w.kernel, scale=scale)
+    assert_close(to_host64(o), ref, "bf16", f"tc na3d scale {scale}")
+
+
+# ------------------------------------------- graph-stable decode step (append)
+
+def test_kv_append_writes_at_device_position_and_advances(ta):
+    import torch
+    from workloads import draw
+    B, Hkv, Lmax, D = 3, 2, 40, 64
+    rng = np.random.Generator(np.random.PCG64(8100))
+    kc = to_dev(draw(rng, (B, Hkv, Lmax, D), "bf16"), "bf16")
+    vc = to_dev(draw(rng, (B, Hkv, Lmax, D), "bf16"), "bf16")
+    kn = to_dev(draw(rng, (B, Hkv, D), "bf16"), "bf16")
+    vn = to_dev(draw(rng, (B, Hkv, D), "bf16"), "bf16")
+    k0, v0 = kc.clone(), vc.clone()
+    sl = torch.tensor([0, 17, 39], dtype=torch.int32, device="cuda")
+    with launched(ta, "kv_append"):
+        ta.kv_append(kc, vc, kn, vn, sl)
+    assert sl.tolist() == [1, 18, 40]
+    for b, pos in enumerate([0, 17, 39]):
+        assert torch.equal(kc[b, :, pos], kn[b]) and torch.equal(vc[b, :, pos], vn[b])
+        k0[b, :, pos] = kn[b]
+        v0[b, :, pos] = vn[b]
+    assert torch.equal(kc, k0) and torch.equal(vc, v0)          # nothing else touched
+    # a full cache (position == Lmax) is refused on the device and left untouched
+    assert ta.device_status() == 0
+    ta.kv_append(kc, vc, kn, vn, torch.tensor([1, 18, 40], dtype=torch.int32, device="cuda"))
+    assert ta.device_status() == 6
+
+
+def test_decode_step_captured_once_and_replayed_per_token(ta):
+    """Append + decode captured in one CUDA graph, replayed for several tokens
+    with unchanged arguments (positions live on the device)."""
+    import torch
+    from workloads import draw
+    w = WORKLOADS["gqa_decode"].with_(B=2, Lmax=300, seq_len=(100, 257), seed=8200)
+    x = make_inputs(w)
+    rng = np.random.Generator(np.random.PCG64(8201))
+    kc, vc = to_dev(x["k"], "bf16"), to_dev(x["v"], "bf16")
+    kc_host, vc_host = to_f64(x["k"], "bf16"), to_f64(x["v"], "bf16")
+    lens = list(x["seq_len"])
+    sl = torch.from_numpy(x["seq_len"]).cuda()
+    B, Hq, Hkv, D = w.B, w.H, w.Hkv, w.D
+    q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    kn = torch.zeros((B, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    vn = torch.zeros_like(kn)
+    o = torch.empty_like(q)
+    ws = torch.zeros(ta.decode_workspace_bytes(B, Hq, Hkv, w.Lmax, D), dtype=torch.uint8,
+                     device="cuda")
+    # first calls outside the capture (per-device set-up of the library)
+    sl_warm = sl.clone()
+    kc_w, vc_w = kc.clone(), vc.clone()
+    ta.kv_append(kc_w, vc_w, kn, vn, sl_warm)
+    ta.decode_gqa(q, kc_w, vc_w, sl_warm, o=o, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ta.kv_append(kc, vc, kn, vn, sl)
+        ta.decode_gqa(q, kc, vc, sl, o=o, workspace=ws)
+    for step in range(3):
+        qh, knh, vnh = (draw(rng, shp, "bf16") for shp in ((B, Hq, D), (B, Hkv, D), (B, Hkv, D)))
+        q.copy_(to_dev(qh, "bf16"))
+        kn.copy_(to_dev(knh, "bf16"))
+        vn.copy_(to_dev(vnh, "bf16"))
+        g.replay()
+        torch.cuda.synchronize()
+        for b in range(B):
+            kc_host[b, :, lens[b]] = to_f64(knh, "bf16")[b]
+            vc_host[b, :, lens[b]] = to_f64(vnh, "bf16")[b]
+            lens[b] += 1
+        assert sl.tolist() == lens
+        ref = oracle.decode_gqa(to_f64(qh, "bf16"), kc_host, vc_host, np.array(lens, np.int32))
+        assert_close(to_host64(o), ref, "bf16", f"graph decode step {step}")
     assert ta.device_status() == 0

@@ -118,14 +118,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
         ptx::fence_barrier_init();
         s_abort = 0;
     }
-    // q of the G heads of this KV head, pre-scaled, fp32 (padding heads are zero)
-    for (int e = threadIdx.x; e < GP * D; e += C::NT) {
-        const int h = e / D, d = e % D;
-        float x = 0.f;
-        if (h < p.G) x = __bfloat162float(p.q[(size_t(b) * p.Hq + kvh * p.G + h) * D + d]) * p.qscale;
-        q_s[e] = x;
-    }
     __syncthreads();
+    if (warp < kCW) {
+        // q of the G heads of this KV head, pre-scaled, fp32 (padding heads are
+        // zero), loaded by the consumers while the producer's first copies fly
+        for (int e = threadIdx.x; e < GP * D / 8; e += kCW * 32) {
+            const int h = (e * 8) / D, d = (e * 8) % D;
+            float x[8];
+            if (h < p.G) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(
+                    p.q + (size_t(b) * p.Hq + kvh * p.G + h) * D + d);
+                bf16x8_to_f32(u, x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q_s[h * D + d + i] = x[i] * p.qscale;
+        }
+        ptx::named_barrier_sync(2, kCW * 32);
+    }
 
     float *s_merge = reinterpret_cast<float *>(smem + C::OFF_M);
 
@@ -326,23 +338,48 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
     __syncthreads();
     if (!s_last) return;
 
-    // ---- last CTA of this (batch, kv-head): merge all splits, write O
+    // ---- last CTA of this (batch, kv-head): merge all splits, write O.
+    // Split weights w[s][h] = 2^(m_s - M) / L first (all (m, l) pairs loaded
+    // at once into shared memory), then every output element sums its splits
+    // with independent loads.
     __threadfence();
+    float *wgt = reinterpret_cast<float *>(smem);        // [splits][GP] (slots are free now)
+    const float *pml = p.part_ml + size_t(unit) * p.ws_splits * GP * 2;
+    const float *po = p.part_o + size_t(unit) * p.ws_splits * GP * D;
+    for (int e = threadIdx.x; e < p.splits * GP; e += C::NT) {
+        wgt[e * 2] = __ldcg(pml + e * 2);
+        wgt[e * 2 + 1] = __ldcg(pml + e * 2 + 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < GP) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, wgt[(s * GP + h) * 2]);
+        float Lsum = 0.f;
+        for (int s = 0; s < p.splits; ++s) {
+            const float ms = wgt[(s * GP + h) * 2];
+            Lsum += (ms == -INFINITY) ? 0.f : wgt[(s * GP + h) * 2 + 1] * exp2f(ms - M);
+        }
+        const float inv = 1.f / Lsum;
+        for (int s = 0; s < p.splits; ++s) {
+            const float ms = wgt[(s * GP + h) * 2];
+            wgt[(s * GP + h) * 2 + 1] = (ms == -INFINITY) ? 0.f : exp2f(ms - M) * inv;
+        }
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < p.G * D; e += C::NT) {
         const int h = e / D, d = e % D;
-        const float *pml = p.part_ml + size_t(unit) * p.ws_splits * GP * 2;
-        const float *po = p.part_o + size_t(unit) * p.ws_splits * GP * D;
-        float M = -INFINITY;
-        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(pml + (s * GP + h) * 2));
-        float O = 0.f, Lsum = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-            const float ms = __ldcg(pml + (s * GP + h) * 2);
-            if (ms == -INFINITY) continue;
-            const float f = exp2f(ms - M);
-            O += __ldcg(po + (s * GP + h) * D + d) * f;
-            Lsum += __ldcg(pml + (s * GP + h) * 2 + 1) * f;
+        float O = 0.f;
+        int s = 0;
+        for (; s + 4 <= p.splits; s += 4) {
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __ldcg(po + ((s + i) * GP + h) * D + d);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) O += v[i] * wgt[((s + i) * GP + h) * 2 + 1];
         }
-        p.o[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] = __float2bfloat16_rn(O / Lsum);
+        for (; s < p.splits; ++s) O += __ldcg(po + (s * GP + h) * D + d) * wgt[(s * GP + h) * 2 + 1];
+        p.o[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] = __float2bfloat16_rn(O);
     }
     if (threadIdx.x == 0) p.tickets[unit] = 0u;   // ready for the next call
 }

@@ -229,6 +229,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
            (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor, 32-byte swizzle (layout type 6), version 1:
+// K-major rows of 32 bytes (16 bf16), 8-row atoms of 256 bytes; the 16-byte
+// half of row r holding channels [8c, 8c + 8) sits at r * 32 + ((c ^ ((r >> 2) & 1)) << 4).
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t sbo) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
+__host__ __device__ constexpr uint32_t sw32_offset(uint32_t row, uint32_t half) {
+    return row * 32u + ((half ^ ((row >> 2) & 1u)) << 4);
+}
+
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets columns
 // [col, col + 32) of lane (lane base + t).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {

@@ -69,13 +69,23 @@ struct TcCfg {
     static constexpr int Q_BYTES = PANELS * PANEL_Q;
     static constexpr int KV_BYTES = PANELS * PANEL_KV;
     static constexpr int STREAMS = NA ? kNQ : 1;           // K/V streams per stage
+    // neighborhood window-penalty channels: 16 bf16 per row, 32-byte swizzle.
+    // The key-side penalties of a key sub-box depend only on its h and w chunk,
+    // so each query box needs at most MAXV distinct penalty tiles, built once.
+    static constexpr int X_ROW = 32;
+    static constexpr int MAXV = NA ? 6 : 0;
+    static constexpr int QX_BYTES = NA ? kNQ * kBM * X_ROW : 0;
+    static constexpr int KX_BYTES = kBN * X_ROW;              // one penalty tile
+    static constexpr int KXV_BYTES = STREAMS * MAXV * KX_BYTES;
     static constexpr int STAGE_BYTES = 2 * STREAMS * KV_BYTES;
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int NS_RAW = (BUDGET - kNQ * Q_BYTES) / STAGE_BYTES;
+    static constexpr int NS_RAW = (BUDGET - kNQ * Q_BYTES - QX_BYTES - KXV_BYTES) / STAGE_BYTES;
     static constexpr int NSTAGE = NS_RAW > 4 ? 4 : NS_RAW;
     static_assert(NSTAGE >= 2, "at least two K/V stages");
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = kNQ * Q_BYTES;
+    static constexpr int OFF_QX = kNQ * Q_BYTES;
+    static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
+    static constexpr int OFF_KV = OFF_KXV + KXV_BYTES;
     static constexpr int OFF_BAR = OFF_KV + NSTAGE * STAGE_BYTES;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;      // barriers + 1024 B alignment slack
     static constexpr uint32_t TM_S = 0;                    // S_t at TM_S + t * kBN
@@ -99,6 +109,8 @@ struct TcCfg {
     static constexpr int v_off(int s, int u) {
         return OFF_KV + s * STAGE_BYTES + (STREAMS + u) * KV_BYTES;
     }
+    // penalty tile v (= h chunk * w chunks + w chunk) of stream u
+    static constexpr int kxv_off(int u, int v) { return OFF_KXV + (u * MAXV + v) * KX_BYTES; }
 };
 
 struct TcParams {
@@ -114,6 +126,7 @@ struct TcParams {
     int nbh, nbw2;           // boxes along h; box pairs along w
     int nbw;                 // boxes along w
     int KH;                  // key sub-box height (keys per tile = KH * 16)
+    float penalty;           // bf16-exact power of two; penalty * c_log2 >= 300
 };
 
 // Barrier block at OFF_BAR.
@@ -232,8 +245,54 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 *reinterpret_cast<uint4 *>(smem + C::OFF_Q + pt * C::PANEL_Q + r * 128 + chunk * 16) =
                     make_uint4(0, 0, 0, 0);
             }
-            ptx::fence_proxy_async_smem();
         }
+        // one-hot window-offset channels of every query row: channel dh, then
+        // bh + dw (rows past the box: all zero)
+        for (int i = threadIdx.x; i < kNQ * kBM * 2; i += C::NT) {
+            const int t = i / (kBM * 2), r = (i / 2) % kBM, half = i % 2;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (r < rows) {
+                const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
+                const int ch[2] = {dh, p.bh + dw};
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    const int c = ch[a] - half * 8;
+                    if (c >= 0 && c < 8) w[c >> 1] |= 0x3F80u << ((c & 1) * 16);   // bf16 1.0
+                }
+            }
+            *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW + ptx::sw32_offset(r, half)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        // key-side penalty tiles: for key (h, w) of the sub-box of h chunk hc and
+        // w chunk wc, channel dh holds -penalty if h lies outside the h window of
+        // query offset dh, channel bh + dw likewise for w
+        const uint32_t neg = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(-p.penalty)));
+        for (int u = 0; u < C::STREAMS; ++u) {
+            if (n_t[u] == 0) continue;
+            const int nv = g[u].nhc * g[u].nwc;
+            for (int i = threadIdx.x; i < nv * BNt * 2; i += C::NT) {
+                const int v = i / (BNt * 2), r = (i / 2) % BNt, half = i % 2;
+                const int kh = g[u].u0h + (v / g[u].nwc) * p.KH + r / kKW;
+                const int kw = g[u].u0w + (v % g[u].nwc) * kKW + r % kKW;
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const int c = half * 8 + cc;
+                    bool viol = false;
+                    if (c < p.bh) {
+                        const int sh = na_window_start(imin(g[u].h0 + c, p.Hg - 1), p.Hg, p.kh);
+                        viol = unsigned(kh - sh) >= unsigned(p.eh);
+                    } else if (c < p.bh + p.bw) {
+                        const int sw = na_window_start(imin(g[u].w0 + c - p.bh, p.W - 1), p.W, p.kw);
+                        viol = unsigned(kw - sw) >= unsigned(p.ew);
+                    }
+                    if (viol) w[cc >> 1] |= neg << ((cc & 1) * 16);
+                }
+                *reinterpret_cast<uint4 *>(smem + C::kxv_off(u, v) + ptx::sw32_offset(r, half)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        ptx::fence_proxy_async_smem();
     }
     if (warp == C::W_MMA) {
         ptx::tmem_alloc(&bars->tmem_base, C::TM_COLS);
@@ -328,6 +387,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     const uint64_t b =
                         ptx::smem_desc_sw128(k_base + (kk >> 2) * C::PANEL_KV + off, 16, 1024);
                     ptx::mma_ss(tmem + C::TM_S + t * kBN, a, b, id_qk, kk > 0);
+                }
+                if constexpr (NA) {
+                    // + window penalties: one more k-step over the 16 extra channels
+                    const uint64_t a = ptx::smem_desc_sw32(
+                        ptx::smem_addr(smem + C::OFF_QX + t * kBM * C::X_ROW), 256);
+                    const int v = j % (g[t].nhc * g[t].nwc);
+                    const uint64_t b = ptx::smem_desc_sw32(ptx::smem_addr(smem + C::kxv_off(t, v)), 256);
+                    ptx::mma_ss(tmem + C::TM_S + t * kBN, a, b, id_qk, 1u);
                 }
                 ptx::tc_commit(&bars->s_full[t]);
             };
@@ -436,11 +503,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         const int nt = n_t[t];
-        // neighborhood: key sub-box counters (w fastest, then h, then t) and the
-        // w-column biases, recomputed only when the w chunk changes
-        int tc = 0, hc = 0, wc = 0, cur_wc = -1;
-        float wb[NA ? kKW : 1];
-        bool wany = false;
+        // neighborhood: key sub-box counters (w fastest, then h, then t)
+        int tc = 0, hc = 0, wc = 0;
         for (int j = 0; j < nt; ++j) {
             if (!__all_sync(0xffffffffu,
                             ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort))) {
@@ -449,22 +513,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             }
             ptx::tc_fence_after();
 
-            // ---- neighborhood window of this row against the key tile:
-            //      additive 0 / -inf biases per w column and per h row
-            float hb[NA ? kBN / kKW : 1];
-            bool warp_any = true;
+            // ---- neighborhood: the window penalties are already in S (extra MMA
+            //      channels); a warp none of whose 32 windows reaches this key
+            //      sub-box skips it
+            bool warp_any = true, t_ok = true;
             if constexpr (NA) {
                 const int kt_ = g[t].u0t + tc, kh_ = g[t].u0h + hc * p.KH, kw_ = g[t].u0w + wc * kKW;
-                if (wc != cur_wc) {        // uniform: the same tile sequence in every thread
-                    wany = false;
-#pragma unroll
-                    for (int c = 0; c < kKW; ++c) {
-                        const bool v = unsigned(kw_ + c - wsw) < unsigned(p.ew);
-                        wb[c] = v ? 0.f : -INFINITY;
-                        wany |= v;
-                    }
-                    cur_wc = wc;
-                }
                 if (++wc == g[t].nwc) {
                     wc = 0;
                     if (++hc == g[t].nhc) {
@@ -472,16 +526,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         ++tc;
                     }
                 }
-                const bool tv_ok = unsigned(kt_ - wst) < unsigned(p.et);
-                bool hany = false;
-#pragma unroll
-                for (int r = 0; r < kBN / kKW; ++r) {
-                    const bool v = tv_ok && r < p.KH && unsigned(kh_ + r - wsh) < unsigned(p.eh);
-                    hb[r] = v ? 0.f : -INFINITY;
-                    hany |= v;
-                }
-                // a warp none of whose 32 windows reaches this tile skips it
-                warp_any = __any_sync(0xffffffffu, wany && hany);
+                t_ok = qvalid && unsigned(kt_ - wst) < unsigned(p.et);
+                const bool reach = t_ok && kh_ < wsh + p.eh && wsh < kh_ + p.KH &&
+                                   kw_ < wsw + p.ew && wsw < kw_ + kKW;
+                warp_any = __any_sync(0xffffffffu, reach);
             }
 
             float sv[kBN];
@@ -502,21 +550,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             float mt = -INFINITY;
             if (warp_any) {
                 if constexpr (NA) {
+                    // columns past this tile's keys (N = KH * 16 < 128) hold stale
+                    // values: whole 16-column groups, warp-uniform
 #pragma unroll
-                    for (int r = 0; r < kBN / kKW; ++r) {
-                        if (r < p.KH) {
+                    for (int gq = 0; gq < kBN / 16; ++gq)
+                        if (gq * 16 >= BNt) {
 #pragma unroll
-                            for (int c = 0; c < kKW; c += 2) {
-                                float b0, b1;
-                                ptx::fadd2(b0, b1, wb[c], wb[c + 1], hb[r], hb[r]);
-                                ptx::fadd2(sv[r * kKW + c], sv[r * kKW + c + 1], sv[r * kKW + c],
-                                           sv[r * kKW + c + 1], b0, b1);
-                            }
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < kKW; ++c) sv[r * kKW + c] = -INFINITY;
+                            for (int i = 0; i < 16; ++i) sv[gq * 16 + i] = -INFINITY;
                         }
-                    }
                 } else {
                     const int valid = p.Nkv - j * kBN;     // keys of this tile inside the sequence
                     if (valid < kBN) {
@@ -534,7 +575,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     for (int i = 0; i < 8; ++i) mx[i] = ptx::fmax3(mx[i], sv[e + i], sv[e + 8 + i]);
                 const float tmax = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
                                               ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-                mt = tmax * cl;        // cl > 0: max commutes with the scaling
+                mt = t_ok ? tmax * cl : -INFINITY;   // cl > 0: max commutes with the scaling
             }
 
             // ---- the previous P V must be done before O is rescaled or P_t rewritten
@@ -574,7 +615,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     m = mt;
                 }
             }
-            const float nmu = (m == -INFINITY) ? 0.f : -m;
+            // (a row whose t window misses this key sub-box gets P = 0)
+            const float nmu = !t_ok ? -INFINITY : (m == -INFINITY) ? 0.f : -m;
 
             // ---- P = 2^(x - m) in bf16 into TMEM, row sum in fp32
             float acc[8];
@@ -585,8 +627,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 if (c * 32 >= BNt) break;
                 uint32_t pk[16];
                 if (warp_any) {
+                    // the upper 16 keys of the last 32-key chunk may lie past the tile
+                    const int ne = (c * 32 + 32 <= BNt) ? 16 : 8;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
+                        if (e >= 8 && ne == 8) {
+                            pk[e] = 0u;
+                            continue;
+                        }
                         float x0, x1;
                         ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nmu,
                                    nmu);
@@ -653,18 +701,31 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
 // ---------------------------------------------------- single-tile self test
 //
-// One CTA: S = Q K^T (both operands K-major in shared memory) and O = P V
+// One CTA: S = Q K^T + Q[:, :16] K[:, :16]^T (the first term from 128-byte
+// swizzled K-major operands, the second from 32-byte swizzled copies -- the
+// layout of the neighborhood kernel's window-penalty channels) and O = P V
 // (P from TMEM, V MN-major in shared memory) for one 128 x 128 tile, written
-// out in fp32 -- the two MMA forms of the attention kernel in isolation.
+// out in fp32: the MMA forms of the attention kernels in isolation.
 template <int D>
 __global__ void __launch_bounds__(160, 1)
 tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, const __nv_bfloat16 *P, float *S_out,
-                   float *O_out, unsigned *err) {
+                   const __grid_constant__ CUtensorMap tv, const __nv_bfloat16 *qg,
+                   const __nv_bfloat16 *kg, const __nv_bfloat16 *P, float *S_out, float *O_out,
+                   unsigned *err) {
     constexpr int PANELS = D / 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
     uint8_t *sq = smem, *sk = smem + PANELS * 16384, *svv = smem + 2 * PANELS * 16384;
+    // 32-byte-swizzled copies of the first 16 channels of q and k (the layout of
+    // the extra window-penalty operands of the neighborhood kernel)
+    uint8_t *sqx = smem + 3 * PANELS * 16384, *skx = sqx + 4096;
+    for (int i = threadIdx.x; i < 2 * 128 * 2; i += blockDim.x) {
+        const int which = i / 256, r = (i / 2) % 128, half = i % 2;
+        const __nv_bfloat16 *src = (which == 0 ? qg : kg) + r * D + half * 8;
+        *reinterpret_cast<uint4 *>((which == 0 ? sqx : skx) + ptx::sw32_offset(r, half)) =
+            *reinterpret_cast<const uint4 *>(src);
+    }
+    ptx::fence_proxy_async_smem();
     __shared__ uint64_t bar_load, bar_mma, bar_p;
     __shared__ uint32_t tmem_base;
     __shared__ int abort;
@@ -702,6 +763,8 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                     const uint64_t b = ptx::smem_desc_sw128(ptx::smem_addr(sk) + (kk >> 2) * 16384 + off, 16, 1024);
                     ptx::mma_ss(tmem, a, b, id_qk, kk > 0);
                 }
+                ptx::mma_ss(tmem, ptx::smem_desc_sw32(ptx::smem_addr(sqx), 256),
+                            ptx::smem_desc_sw32(ptx::smem_addr(skx), 256), id_qk, 1);
                 ptx::tc_commit(&bar_mma);
                 ok = ptx::mbar_wait_or_abort(&bar_p, 0, err, &abort);
                 ptx::tc_fence_after();
@@ -830,9 +893,14 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
         for (int cbh = 1; cbh <= imin(Hg, 128 / cbt); ++cbh)
             for (int cbw = 1; cbw <= imin(W, 128 / (cbt * cbh)); ++cbw) {
                 if (cbt * cbh * cbw < imin(64, T * Hg * W)) continue;   // keep MMA rows busy
+                if (cbh + cbw > 16) continue;                // h and w offsets fit 16 channels
                 // key tiles of 64..128 keys keep the MMAs large enough to amortise
                 // the per-tile barrier round trips
                 for (int ckh = imin(4, imin(kern[1], Hg) + cbh - 1); ckh <= 8; ++ckh) {
+                    // distinct key penalty tiles of a box (h chunks x w chunks) must fit
+                    const int nh_max = cdiv(imin(cbh + imin(kern[1], Hg) - 1, Hg), ckh);
+                    const int nw_max = cdiv(imin(cbw + imin(kern[2], W) - 1, W), kKW);
+                    if (nh_max * nw_max > 6) continue;
                     // total key slots over all boxes = sum_t(ut) * sum_h(nhc) * sum_w(nwc) * KH*16
                     const int b[3] = {cbt, cbh, cbw};
                     double axis[3];
@@ -936,6 +1004,9 @@ attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v,
         !make_tmap(&tv, v, 5, dims, kbox))
         return ATTN_ERR_CUDA;
     p.c_log2 = scale * kLog2e;
+    // penalty per violated axis: a power of two (exact in bf16) with
+    // penalty * scale * log2(e) >= 300, so 2^(x - m) underflows to exactly 0
+    p.penalty = exp2f(fminf(100.f, fmaxf(0.f, ceilf(log2f(300.f / p.c_log2)))));
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.err = c.err;
     p.T = T; p.Hg = Hg; p.W = W;
@@ -957,19 +1028,21 @@ attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void
     if (!make_tmap(&tq, q, 3, dims, box) || !make_tmap(&tk, k, 3, dims, box) ||
         !make_tmap(&tv, v, 3, dims, box))
         return ATTN_ERR_CUDA;
-    const size_t smem = 3 * (D / 64) * 16384 + 1024;
+    const size_t smem = 3 * (D / 64) * 16384 + 8192 + 1024;
     static int done_mask = 0;
     if (D == 128) {
         if (!ensure_smem_attr(reinterpret_cast<const void *>(tc_selftest_kernel<128>), smem, c.device, &done_mask))
             return ATTN_ERR_RESOURCE;
         tc_selftest_kernel<128><<<1, 160, smem, c.stream>>>(
-            tq, tk, tv, static_cast<const __nv_bfloat16 *>(P), S, O, c.err);
+            tq, tk, tv, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+            static_cast<const __nv_bfloat16 *>(P), S, O, c.err);
     } else {
         static int done64 = 0;
         if (!ensure_smem_attr(reinterpret_cast<const void *>(tc_selftest_kernel<64>), smem, c.device, &done64))
             return ATTN_ERR_RESOURCE;
         tc_selftest_kernel<64><<<1, 160, smem, c.stream>>>(
-            tq, tk, tv, static_cast<const __nv_bfloat16 *>(P), S, O, c.err);
+            tq, tk, tv, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+            static_cast<const __nv_bfloat16 *>(P), S, O, c.err);
     }
     return launch_status(kFamTcFlash);
 }

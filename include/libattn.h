@@ -100,6 +100,19 @@ ATTN_API attn_status_t attn_rope_joint_fwd(const void *q, const void *k, const v
 ATTN_API size_t attn_rope_joint_workspace_bytes(int B, int H, int N, int D, attn_dtype_t dtype);
 
 /*
+ * Causal grouped-query prefill (self-attention over a prompt).
+ *   q, o [B, Hq, N, D]; k, v [B, Hkv, N, D]; Hq % Hkv == 0.  Query head hq
+ *   reads KV head hq / (Hq / Hkv); query position i attends to key positions
+ *   j <= i.  bf16 runs on the tensor cores for D in {64, 128}; fp32 (and bf16
+ *   with D = 32) on the exact-FFMA SIMT kernel.
+ * Passage: fak "GPU - the in-kernel forward pass", section 3 (Llama prefill
+ * workloads pp64 .. pp512 of a grouped-query model).
+ */
+ATTN_API attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const void *v, void *o,
+                                           int B, int Hq, int Hkv, int N, int D,
+                                           attn_dtype_t dtype, float scale, void *stream);
+
+/*
  * Single-token grouped-query decode attention over a KV cache.
  *   q [B, Hq, D], o [B, Hq, D]; k_cache, v_cache [B, Hkv, Lmax, D].
  *   seq_len: DEVICE int32 [B], 1 <= seq_len[b] <= Lmax (checked on the device;
@@ -153,6 +166,25 @@ ATTN_API attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_cach
                                                attn_dtype_t dtype, float scale, void *stream);
 
 /*
+ * Appends one token's K and V rows to a KV cache at the position the device
+ * holds, for a decode step that is captured once as a CUDA graph and replayed
+ * per token with unchanged arguments.
+ *   k_cache, v_cache [B, Hkv, Lmax, D] (written: row seq_len[b] of every KV
+ *   head of batch b); k_new, v_new [B, Hkv, D] (read).  seq_len: DEVICE int32
+ *   [B], the write position; if advance != 0 the kernel then sets
+ *   seq_len[b] += 1 (so a following attn_decode_gqa sees the new token).
+ *   A position outside [0, Lmax) writes nothing and sets ATTN_ERR_DEVICE_CHECK.
+ *   dtype ATTN_F32 or ATTN_BF16; D in {32, 64, 128}.
+ * Passage: fak "GPU - the in-kernel forward pass", section 3b, step 3 (a
+ * kernel-form KV append with a scalar offset replaces the cudaMemcpy whose
+ * moving destination forced a graph re-instantiation every token).
+ */
+ATTN_API attn_status_t attn_kv_append(void *k_cache, void *v_cache, const void *k_new,
+                                      const void *v_new, int32_t *seq_len, int B, int Hkv,
+                                      int Lmax, int D, attn_dtype_t dtype, int advance,
+                                      void *stream);
+
+/*
  * 3D neighborhood attention with NATTEN boundary windows.
  *   q, k, v, o [B, heads, N, D] with N = T * Hg * W tokens in row-major
  *   (t, h, w) order.  kernel: HOST int[3], the requested window per axis; each
@@ -180,8 +212,10 @@ ATTN_API attn_status_t attn_na3d_window_starts(int T, int Hg, int W, const int k
 
 /*
  * Tensor-core building-block check (testing): one CTA computes, for a single
- * tile, S = q k^T and O = P v with the same tcgen05 MMA forms, shared-memory
- * layouts and TMEM placement the bf16 attention kernels use.
+ * tile, S = q k^T + q[:, :16] k[:, :16]^T and O = P v with the same tcgen05
+ * MMA forms, shared-memory layouts (128-byte swizzle for q, k, v; 32-byte
+ * swizzle for the 16-channel term, as used by the neighborhood kernel's
+ * window-penalty channels) and TMEM placement the bf16 attention kernels use.
  *   q, k, v: DEVICE bf16 [128, D]; P: DEVICE bf16 [128, 128];
  *   S: DEVICE f32 [128, 128]; O: DEVICE f32 [128, D]; D in {64, 128}.
  * No counterpart on the pages: it isolates the matrix-descriptor and
@@ -205,7 +239,8 @@ ATTN_API attn_status_t attn_device_status(void *stream);
  * Number of kernel launches this process has made through the given kernel
  * family, for tests that must prove the path under test really ran.
  * ids: 0 = fp32/SIMT flash, 1 = tcgen05 flash, 2 = decode split-KV,
- *      3 = RoPE prologue, 4 = window-start export, 5 = tcgen05 neighborhood.
+ *      3 = RoPE prologue, 4 = window-start export, 5 = tcgen05 neighborhood,
+ *      6 = KV-cache append.
  * Returns 0 for an unknown id.
  */
 ATTN_API uint64_t attn_launch_count(int kernel_family);

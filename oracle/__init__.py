@@ -56,6 +56,8 @@ def lib():
                                        _d, _d, _vp, _i64, _i]
         L.oracle_decode_gqa.argtypes = [_f64p, _f64p, _f64p, _i32p, _f64p, _i, _i, _i, _i, _i,
                                         _d, _i]
+        L.oracle_causal_gqa_fwd.argtypes = [_f64p, _f64p, _f64p, _f64p, _i, _i, _i, _i, _i, _d,
+                                            _vp, _i64, _i]
         L.oracle_na_window_start.restype = _i
         L.oracle_na_window_start.argtypes = [_i, _i, _i]
         L.oracle_na3d_window_starts.argtypes = [_i, _i, _i, _i32p, _i32p]
@@ -140,6 +142,20 @@ def decode_gqa(q, kc, vc, seq_len, scale=None, threads=0):
     assert sl.shape == (B,) and np.all((sl >= 1) & (sl <= Lmax))
     o = np.empty_like(q)
     lib().oracle_decode_gqa(q, kc, vc, sl, o, B, Hq, Hkv, Lmax, D, _scale(scale, D), threads)
+    return o
+
+
+def causal_gqa_fwd(q, k, v, scale=None, rows: Optional[Sequence[int]] = None, threads=0):
+    """Causal GQA prefill: q [B,Hq,N,D], k/v [B,Hkv,N,D]; query i sees keys j <= i."""
+    q, k, v = _c(q), _c(k), _c(v)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape == (B, Hkv, N, D) and v.shape == k.shape and Hq % Hkv == 0
+    r = None if rows is None else _c(rows, np.int64)
+    o = np.empty_like(q) if r is None else np.empty((r.size, D))
+    lib().oracle_causal_gqa_fwd(q, k, v, o, B, Hq, Hkv, N, D, _scale(scale, D),
+                                None if r is None else r.ctypes.data, 0 if r is None else r.size,
+                                threads)
     return o
 
 

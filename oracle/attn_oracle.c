@@ -212,6 +212,41 @@ int oracle_joint_fwd(const double *q, const double *k, const double *v, double *
     return 0;
 }
 
+/* ------------------------------------------------------ causal prefill -- */
+
+/*
+ * Causal grouped-query prefill (Llama prefill, the pp64..pp512 workloads of
+ * fak "GPU - the in-kernel forward pass", section 3): q [B, Hq, N, D],
+ * k, v [B, Hkv, N, D]; query head hq reads KV head hq / (Hq / Hkv) and query
+ * position i attends to key positions j <= i.  If rows != NULL only those
+ * flattened rows (b*Hq*N + hq*N + i) are produced into o ([nrows, D]).
+ */
+void oracle_causal_gqa_fwd(const double *q, const double *k, const double *v, double *o,
+                           int B, int Hq, int Hkv, int N, int D, double scale,
+                           const int64_t *rows, int64_t nrows, int nthreads)
+{
+    set_threads(nthreads);
+    const int group = Hq / Hkv;
+    const int64_t total = rows ? nrows : (int64_t)B * Hq * N;
+#pragma omp parallel
+    {
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < total; ++r) {
+            const int64_t row = rows ? rows[r] : r;
+            const int64_t i = row % N, bh = row / N;
+            const int64_t b = bh / Hq, hq = bh % Hq;
+            const int64_t kvbase = (b * Hkv + hq / group) * (int64_t)N * D;
+            for (int64_t j = 0; j < N; ++j) keys[j] = j;
+            attend_row(q + row * D, k + kvbase, v + kvbase, keys, i + 1,
+                       D, scale, o + r * D, NULL, s);
+        }
+        free(keys);
+        free(s);
+    }
+}
+
 /* ---------------------------------------------------------------- decode -- */
 
 /*

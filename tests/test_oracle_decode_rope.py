@@ -152,3 +152,32 @@ def test_joint_equals_full_attention_on_rotated_q_k_only():
     rows = [0, 5, N, 2 * N - 1]
     np.testing.assert_array_equal(oracle.joint_fwd(q, k, v, pos, rows=rows),
                                   o.reshape(-1, 128)[rows])
+
+
+# -------------------------------------------------------- causal GQA prefill
+
+def test_causal_gqa_matches_sdpa_is_causal_with_repeated_kv():
+    B, Hq, Hkv, N, D = 2, 6, 2, 19, 16
+    q = _rand((B, Hq, N, D), 70)
+    k, v = _rand((B, Hkv, N, D), 71), _rand((B, Hkv, N, D), 72)
+    o = oracle.causal_gqa_fwd(q, k, v)
+    kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(kr), torch.from_numpy(vr), is_causal=True).numpy()
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-13)
+
+
+def test_causal_first_row_is_first_value_and_last_row_is_full_attention():
+    B, H, N, D = 1, 2, 11, 8
+    q, k, v = (_rand((B, H, N, D), s) for s in (73, 74, 75))
+    o = oracle.causal_gqa_fwd(q, k, v)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], atol=1e-15)
+    full = oracle.full_fwd(q[:, :, -1:], k, v)
+    np.testing.assert_allclose(o[:, :, -1:], full, atol=1e-14)
+    # future keys never matter: perturbing them leaves earlier rows unchanged
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, 6:] = np.nan
+    v2[:, :, 6:] = np.nan
+    np.testing.assert_array_equal(oracle.causal_gqa_fwd(q, k2, v2)[:, :, :6], o[:, :, :6])
+    rows = [0, 5, 10, 11, 21]
+    np.testing.assert_array_equal(oracle.causal_gqa_fwd(q, k, v, rows=rows), o.reshape(-1, D)[rows])

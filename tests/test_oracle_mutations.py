@@ -38,6 +38,9 @@ MUTATIONS = {
                        "for (int d = 0; d < D; ++d) o[d] += s[j] * vj[d];"),
     "decode_drops_last_row": ("const int64_t L = seq_len[b];",
                               "const int64_t L = seq_len[b] > 1 ? seq_len[b] - 1 : 1;"),
+    "causal_sees_one_future_key": ("attend_row(q + row * D, k + kvbase, v + kvbase, keys, i + 1,",
+                                   "attend_row(q + row * D, k + kvbase, v + kvbase, keys, i + (i + 1 < N ? 2 : 1),"),
+    "causal_gqa_interleaved": ("(b * Hkv + hq / group)", "(b * Hkv + hq % Hkv)"),
 }
 
 

@@ -454,3 +454,37 @@ def test_decode_step_captured_once_and_replayed_per_token(ta):
         ref = oracle.decode_gqa(to_f64(qh, "bf16"), kc_host, vc_host, np.array(lens, np.int32))
         assert_close(to_host64(o), ref, "bf16", f"graph decode step {step}")
     assert ta.device_status() == 0
+
+
+# ------------------------------------------------------ causal GQA prefill
+
+@pytest.mark.parametrize("dtype,B,Hq,Hkv,N,D", [
+    ("bf16", 1, 4, 1, 256, 128), ("bf16", 2, 8, 2, 300, 64), ("bf16", 1, 2, 2, 1000, 128),
+    ("bf16", 1, 6, 3, 1, 64), ("bf16", 1, 4, 2, 129, 32), ("f32", 2, 4, 2, 200, 64),
+    ("f32", 1, 3, 1, 70, 32),
+])
+def test_causal_gqa_parity(ta, dtype, B, Hq, Hkv, N, D):
+    from workloads import draw
+    rng = np.random.Generator(np.random.PCG64(8300 + N + D + Hq))
+    q = draw(rng, (B, Hq, N, D), dtype)
+    k = draw(rng, (B, Hkv, N, D), dtype)
+    v = draw(rng, (B, Hkv, N, D), dtype)
+    family = "tc_flash" if (dtype == "bf16" and D >= 64) else "simt"
+    with launched(ta, family):
+        o = ta.causal_gqa_fwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype))
+    ref = oracle.causal_gqa_fwd(to_f64(q, dtype), to_f64(k, dtype), to_f64(v, dtype))
+    assert_close(to_host64(o), ref, dtype, f"causal gqa {dtype} {B,Hq,Hkv,N,D}")
+    assert ta.device_status() == 0
+
+
+def test_causal_gqa_llama_prefill_sampled_rows(ta):
+    # a Llama-8B-like grouped prefill: 32 query heads on 8 KV heads, 4096 tokens
+    from workloads import draw
+    B, Hq, Hkv, N, D = 1, 32, 8, 4096, 128
+    rng = np.random.Generator(np.random.PCG64(8400))
+    q, k, v = (draw(rng, s, "bf16") for s in ((B, Hq, N, D), (B, Hkv, N, D), (B, Hkv, N, D)))
+    o = ta.causal_gqa_fwd(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"))
+    rows = np.unique(np.concatenate([np.random.default_rng(13).choice(B * Hq * N, 1500, replace=False),
+                                     [0, 1, 127, 128, 255, 256, N - 1, 31 * N + N - 1]]))
+    ref = oracle.causal_gqa_fwd(to_f64(q, "bf16"), to_f64(k, "bf16"), to_f64(v, "bf16"), rows=rows)
+    assert_close(to_host64(o).reshape(-1, D)[rows], ref, "bf16", "llama prefill sampled")

@@ -12,6 +12,8 @@ Entry points (names as in the C ABI, without the ``attn_`` prefix):
     decode_gqa(q, k_cache, v_cache, seq_len)   q [B, Hq, D], caches [B, Hkv, Lmax, D]
     na3d_fwd(q, k, v, grid, kernel)            q, k, v [B, heads, T*Hg*W, D]
     na3d_window_starts(grid, kernel)
+    kv_append(k_cache, v_cache, k_new, v_new, seq_len)   device-side position, graph-stable
+    causal_gqa_fwd(q, k, v)                    q [B, Hq, N, D], k/v [B, Hkv, N, D], causal
 """
 from __future__ import annotations
 
@@ -22,8 +24,8 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "AttnError", "lib", "full_fwd", "rope_joint_fwd", "decode_gqa", "na3d_fwd",
-    "na3d_window_starts", "decode_workspace_bytes", "rope_joint_workspace_bytes",
+    "AttnError", "lib", "full_fwd", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
+    "na3d_window_starts", "kv_append", "decode_workspace_bytes", "rope_joint_workspace_bytes",
     "device_status", "launch_count", "version", "FAMILIES", "LIB_PATH",
 ]
 
@@ -34,7 +36,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           3: "insufficient resources", 4: "CUDA error", 5: "device wait timed out",
           6: "device-side check failed"}
 #: kernel families of attn_launch_count
-FAMILIES = {"simt": 0, "tc_flash": 1, "decode": 2, "rope": 3, "na_starts": 4, "tc_na": 5}
+FAMILIES = {"simt": 0, "tc_flash": 1, "decode": 2, "rope": 3, "na_starts": 4, "tc_na": 5,
+            "kv_append": 6}
 
 
 class AttnError(RuntimeError):
@@ -67,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.attn_na3d_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                     ctypes.POINTER(_i), _i, _f, _vp]
         L.attn_na3d_window_starts.argtypes = [_i, _i, _i, ctypes.POINTER(_i), _vp, _vp]
+        L.attn_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
+        L.attn_causal_gqa_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
         L.attn_status_string.argtypes = [_i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_device_status.argtypes = [_vp]
@@ -74,7 +79,8 @@ def lib() -> ctypes.CDLL:
         L.attn_launch_count.restype = _u64
         L.attn_version.restype = ctypes.c_char_p
         for name in ("attn_full_fwd", "attn_rope_joint_fwd", "attn_decode_gqa", "attn_na3d_fwd",
-                     "attn_na3d_window_starts", "attn_device_status"):
+                     "attn_na3d_window_starts", "attn_device_status", "attn_kv_append",
+                     "attn_causal_gqa_fwd"):
             getattr(L, name).restype = _i
         _lib = L
     return _lib
@@ -136,6 +142,22 @@ def full_fwd(q, k, v, o=None, scale=None):
     return o
 
 
+def causal_gqa_fwd(q, k, v, o=None, scale=None):
+    """Causal GQA prefill: q [B,Hq,N,D], k/v [B,Hkv,N,D] -> o [B,Hq,N,D]."""
+    dev = _cuda(q, k, v)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, D) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k/v must be [B, Hkv, N, D] with q's dtype")
+    o = torch.empty_like(q) if o is None else o
+    _cuda(q, o)
+    with torch.cuda.device(dev):
+        _check(lib().attn_causal_gqa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         B, Hq, Hkv, N, D, _dtype(q), _scale(scale), _stream(dev)),
+               "attn_causal_gqa_fwd")
+    return o
+
+
 def rope_joint_workspace_bytes(B, H, N, D, dtype) -> int:
     return int(lib().attn_rope_joint_workspace_bytes(B, H, N, D, _dtype(torch.empty(0, dtype=dtype))))
 
@@ -190,6 +212,21 @@ def decode_gqa(q, k_cache, v_cache, seq_len, o=None, scale=None, workspace=None)
                                      workspace.numel(), _stream(dev)),
                "attn_decode_gqa")
     return o
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, seq_len, advance=True):
+    """Write k_new/v_new [B,Hkv,D] into row seq_len[b] of the caches [B,Hkv,Lmax,D]
+    (device-side position); with advance, seq_len[b] += 1 on the device."""
+    dev = _cuda(k_cache, v_cache, k_new, v_new, seq_len)
+    B, Hkv, Lmax, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape \
+            or seq_len.shape != (B,) or seq_len.dtype != torch.int32:
+        raise ValueError("caches [B,Hkv,Lmax,D], new rows [B,Hkv,D], seq_len int32 [B] required")
+    with torch.cuda.device(dev):
+        _check(lib().attn_kv_append(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                                    v_new.data_ptr(), seq_len.data_ptr(), B, Hkv, Lmax, D,
+                                    _dtype(k_cache), 1 if advance else 0, _stream(dev)),
+               "attn_kv_append")
 
 
 def na3d_fwd(q, k, v, grid, kernel, o=None, scale=None):

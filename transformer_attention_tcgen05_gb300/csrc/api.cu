@@ -168,6 +168,25 @@ attn_status_t attn_full_fwd(const void *q, const void *k, const void *v, void *o
     return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
 }
 
+attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const void *v, void *o, int B,
+                                  int Hq, int Hkv, int N, int D, attn_dtype_t dtype, float scale,
+                                  void *stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0 || !valid_d(D) || !valid_dtype(dtype))
+        return ATTN_ERR_INVALID_ARG;
+    if (!small_enough(N, D) || (long long)B * Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (o == q || o == k || o == v) return ATTN_ERR_INVALID_ARG;
+    Ctx c;
+    attn_status_t st = get_ctx(stream, &c);
+    if (st != ATTN_OK) return st;
+    const float sc = resolve_scale(scale, D);
+    if (dtype == ATTN_BF16 && tc_full_supported(B, Hq, N, N, D))
+        return tc_causal_gqa(c, q, k, v, o, B, Hq, Hkv, N, D, sc);
+    return simt_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc);
+}
+
 size_t attn_rope_joint_workspace_bytes(int B, int H, int N, int D, attn_dtype_t dtype) {
     if (B < 1 || H < 1 || N < 1 || !valid_d(D) || !valid_dtype(dtype)) return 0;
     const size_t one = ((size_t(B) * H * N * D * elem_size(dtype)) + 255) & ~size_t(255);
@@ -235,6 +254,21 @@ attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_
     if (st != ATTN_OK) return st;
     return decode_gqa(c, q, k_cache, v_cache, seq_len, o, B, Hq, Hkv, Lmax, D,
                       resolve_scale(scale, D), workspace, workspace_bytes);
+}
+
+attn_status_t attn_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                             int32_t *seq_len, int B, int Hkv, int Lmax, int D, attn_dtype_t dtype,
+                             int advance, void *stream) {
+    if (!k_cache || !v_cache || !k_new || !v_new || !seq_len) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hkv < 1 || Lmax < 1 || !valid_d(D) || !valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+    if (k_cache == v_cache || k_new == k_cache || v_new == v_cache) return ATTN_ERR_INVALID_ARG;
+    if ((long long)Lmax * D >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    Ctx c;
+    attn_status_t st = get_ctx(stream, &c);
+    if (st != ATTN_OK) return st;
+    return kv_append(c, dtype, k_cache, v_cache, k_new, v_new, seq_len, B, Hkv, Lmax, D, advance);
 }
 
 static attn_status_t check_na(int T, int Hg, int W, const int kernel[3]) {

@@ -41,7 +41,8 @@ namespace {
 
 constexpr int kRowsPerChunk = 32;
 constexpr int kCW = 4;          // consumer warps
-constexpr int kSlots = 4;       // ring slots (one chunk each)
+constexpr int kSlots = 4;       // ring slots (one chunk each); chunk i -> slot i % kSlots
+static_assert(kSlots % kCW == 0, "every slot must always feed the same consumer warp");
 constexpr int kMaxSplits = 256;
 
 template <int D, int GP>
@@ -389,11 +390,17 @@ int max_splits_for(int Lmax) {
     return imin(kMaxSplits, imax(1, cdiv(Lmax, kRowsPerChunk) / (2 * kCW)));
 }
 
-// Splits per (batch, kv-head): about one wave of three CTAs per SM, each CTA
-// at least two 32-row chunks per consumer warp.
+// CTAs of one configuration that fit an SM (shared memory is the limit).
+constexpr int ctas_per_sm(int smem_bytes) {
+    return (228 * 1024) / (smem_bytes + 1024) > 0 ? (228 * 1024) / (smem_bytes + 1024) : 1;
+}
+
+// Splits per (batch, kv-head): about one wave of resident CTAs, each CTA at
+// least two 32-row chunks per consumer warp.
 int splits_for(int B, int Hkv, int Lmax, int sm_count) {
     const int units = B * Hkv;
-    const int splits = imax(1, (3 * sm_count) / imax(units, 1));
+    const int per_sm = ctas_per_sm(DecCfg<128, 4>::SMEM);
+    const int splits = imax(1, (per_sm * sm_count) / imax(units, 1));
     return imax(1, imin(splits, max_splits_for(Lmax)));
 }
 

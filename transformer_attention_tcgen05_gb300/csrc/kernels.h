@@ -23,7 +23,8 @@ enum KernelFamily : int {
     kFamRope = 3,
     kFamNaStarts = 4,
     kFamTcNa = 5,
-    kFamCount = 6,
+    kFamKvAppend = 6,
+    kFamCount = 7,
 };
 
 void count_launch(int family);
@@ -52,6 +53,11 @@ attn_status_t rope_rotate_qk(const Ctx &c, attn_dtype_t dt, const void *q, const
                              void *qr, void *kr, int BH, int N, int D, const int32_t *pos,
                              const int axes_dim[4], float theta);
 
+// KV-cache append at the device-side position seq_len[b] (optionally advancing it).
+attn_status_t kv_append(const Ctx &c, attn_dtype_t dt, void *kc, void *vc, const void *kn,
+                        const void *vn, int32_t *seq_len, int B, int Hkv, int Lmax, int D,
+                        int advance);
+
 // Split-KV GQA decode (bf16).
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
 attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void *v,
@@ -62,6 +68,11 @@ attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void 
 attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v, void *o,
                       int B, int H, int Nq, int Nkv, int D, float scale);
 bool tc_full_supported(int B, int H, int Nq, int Nkv, int D);
+attn_status_t tc_causal_gqa(const Ctx &c, const void *q, const void *k, const void *v, void *o,
+                            int B, int Hq, int Hkv, int N, int D, float scale);
+attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                              const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
+                              float scale);
 attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v, void *o,
                       int B, int H, int T, int Hg, int W, int D, const int kernel[3],
                       float scale);

@@ -36,6 +36,8 @@ struct SimtParams {
     int et, eh, ew;          // effective kernel min(k, extent)
     int bt, bh, bw;          // query box
     int nbh, nbw;            // boxes along h and w
+    // causal grouped-query prefill (group > 1: KV head = query head / group)
+    int causal, Hq, Hkv, group;
 };
 
 template <int D>
@@ -71,9 +73,10 @@ simt_flash_kernel(const SimtParams p) {
     const size_t bh = blockIdx.y;
     const int tile = blockIdx.x;
 
+    const size_t bkv = p.group > 1 ? (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group : bh;
     const T *qg = static_cast<const T *>(p.q) + bh * size_t(p.Nq) * D;
-    const T *kg = static_cast<const T *>(p.k) + bh * size_t(p.Nkv) * D;
-    const T *vg = static_cast<const T *>(p.v) + bh * size_t(p.Nkv) * D;
+    const T *kg = static_cast<const T *>(p.k) + bkv * size_t(p.Nkv) * D;
+    const T *vg = static_cast<const T *>(p.v) + bkv * size_t(p.Nkv) * D;
     T *og = static_cast<T *>(p.o) + bh * size_t(p.Nq) * D;
 
     int qi = 0;
@@ -108,7 +111,8 @@ simt_flash_kernel(const SimtParams p) {
     } else {
         qi = tile * kRows + r;
         qvalid = qi < p.Nq;
-        nkeys = p.Nkv;
+        // causal: keys past the tile's last query are seen by no row of it
+        nkeys = p.causal ? imin(p.Nkv, (tile + 1) * kRows) : p.Nkv;
     }
 
     float qv[32], acc[32];
@@ -171,6 +175,7 @@ simt_flash_kernel(const SimtParams p) {
                 for (int off = 1; off < L::TPR; off <<= 1)
                     part += __shfl_xor_sync(0xffffffffu, part, off);
                 bool ok = kb + c0 + c < nkeys;
+                if (!NA && p.causal) ok = ok && kb + c0 + c <= qi;
                 if (NA) {
                     const int4 kq = kc[c0 + c];
                     ok = ok && unsigned(kq.x - wst) < unsigned(p.et) &&
@@ -295,6 +300,18 @@ attn_status_t simt_full(const Ctx &c, attn_dtype_t dt, const void *q, const void
     p.Nq = Nq; p.Nkv = Nkv;
     p.qscale = scale * kLog2e;
     return dispatch<false>(c, dt, D, p, cdiv(Nq, kRows), B * H);
+}
+
+attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                              const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
+                              float scale) {
+    SimtParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o;
+    p.Nq = p.Nkv = N;
+    p.qscale = scale * kLog2e;
+    p.causal = 1;
+    p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;   // group 1: every head reads its own K/V
+    return dispatch<false>(c, dt, D, p, cdiv(N, kRows), B * Hq);
 }
 
 attn_status_t simt_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,

@@ -127,6 +127,8 @@ struct TcParams {
     int nbw;                 // boxes along w
     int KH;                  // key sub-box height (keys per tile = KH * 16)
     float penalty;           // bf16-exact power of two; penalty * c_log2 >= 300
+    // causal grouped-query prefill
+    int Hq, Hkv, group;
 };
 
 // Barrier block at OFF_BAR.
@@ -184,11 +186,12 @@ __device__ __forceinline__ void na_key_box(const NaTile &g, int KH, int j, int &
     w = g.u0w + wc * kKW;
 }
 
-template <int D, bool NA>
+template <int D, bool NA, bool CAUSAL>
 __global__ void __launch_bounds__(TcCfg<D, NA>::NT, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams p) {
     using C = TcCfg<D, NA>;
+    static_assert(!(NA && CAUSAL), "causal prefill is a full-attention variant");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
@@ -197,6 +200,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
+    // K/V (batch, head) row of the tensor maps: the query head's KV head for
+    // grouped-query attention (contiguous groups of Hq / Hkv query heads)
+    const int bkv = CAUSAL ? (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group : bh;
 
     // ---- per-CTA work description (identical in every role)
     int n_t[kNQ];
@@ -211,6 +217,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             n_t[t] = g[t].ntiles;
         }
         BNt = p.KH * kKW;
+        steps = imax(n_t[0], n_t[1]);
+    } else if constexpr (CAUSAL) {
+        // heaviest query blocks first; query tile t sees key tiles 0 .. its diagonal
+        q0 = (gridDim.x - 1 - blockIdx.x) * (kNQ * kBM);
+        const int all = cdiv(p.Nkv, kBN);
+#pragma unroll
+        for (int t = 0; t < kNQ; ++t)   // a query tile past the sequence's end has no work
+            n_t[t] = q0 + t * kBM < p.Nq ? imin(all, (q0 + t * kBM) / kBN + 1) : 0;
         steps = imax(n_t[0], n_t[1]);
     } else {
         q0 = blockIdx.x * (kNQ * kBM);
@@ -339,15 +353,18 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                                              abort))
                     break;
                 issued = j + 1;
+                // a shared K/V stream (no neighborhood boxes) serves both query
+                // tiles, so it runs for the longer of the two tile counts
+                auto stream_has = [&](int u) { return NA ? j < n_t[u] : j < steps; };
                 uint32_t bytes = 0;
                 for (int u = 0; u < C::STREAMS; ++u)
-                    if (j < n_t[u]) bytes += C::PANELS * BNt * 128;
+                    if (stream_has(u)) bytes += C::PANELS * BNt * 128;
                 for (int which = 0; which < 2; ++which) {
                     uint64_t *bar = which == 0 ? &bars->k_full[s] : &bars->v_full[s];
                     const CUtensorMap *tm = which == 0 ? &tk : &tv;
                     ptx::mbar_arrive_expect_tx(bar, bytes);
                     for (int u = 0; u < C::STREAMS; ++u) {
-                        if (j >= n_t[u]) continue;
+                        if (!stream_has(u)) continue;
                         for (int pn = 0; pn < C::PANELS; ++pn) {
                             uint8_t *dst = smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) +
                                            pn * C::PANEL_KV;
@@ -356,7 +373,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                                 na_key_box(g[u], p.KH, j, kt_, kh_, kw_);
                                 ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, bar, pol_kv);
                             } else {
-                                ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bh, bar, pol_kv);
+                                ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bkv, bar, pol_kv);
                             }
                         }
                     }
@@ -559,7 +576,18 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                             for (int i = 0; i < 16; ++i) sv[gq * 16 + i] = -INFINITY;
                         }
                 } else {
-                    const int valid = p.Nkv - j * kBN;     // keys of this tile inside the sequence
+                    int valid = p.Nkv - j * kBN;           // keys of this tile inside the sequence
+                    if constexpr (CAUSAL) {
+                        // the last tile is the diagonal one (query tile and key tile
+                        // start at the same position): key e is visible to row `row`
+                        // iff e <= row
+                        if (j == nt - 1) {
+#pragma unroll
+                            for (int e = 0; e < kBN; ++e)
+                                if (e > row || e >= valid) sv[e] = -INFINITY;
+                            valid = kBN;
+                        }
+                    }
                     if (valid < kBN) {
 #pragma unroll
                         for (int e = 0; e < kBN; ++e)
@@ -859,13 +887,13 @@ bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool NA>
+template <int D, bool NA, bool CAUSAL = false>
 attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
     using C = TcCfg<D, NA>;
     static int done_mask = 0;
     static int regs = -1;
-    auto kern = tc_attn_kernel<D, NA>;
+    auto kern = tc_attn_kernel<D, NA, CAUSAL>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     // The warpgroups re-split the launch's register file with setmaxnreg; the
@@ -983,6 +1011,29 @@ attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v,
     const dim3 grid(cdiv(Nq, kNQ * kBM), B * H);
     return D == 128 ? launch_tc<128, false>(c, tq, tk, tv, p, grid)
                     : launch_tc<64, false>(c, tq, tk, tv, p, grid);
+}
+
+attn_status_t tc_causal_gqa(const Ctx &c, const void *q, const void *k, const void *v, void *o,
+                            int B, int Hq, int Hkv, int N, int D, float scale) {
+    CUtensorMap tq, tk, tv;
+    const uint64_t dq[3] = {uint64_t(D), uint64_t(N), uint64_t(B) * Hq};
+    const uint64_t dk[3] = {uint64_t(D), uint64_t(N), uint64_t(B) * Hkv};
+    const uint32_t box[3] = {64, kBM, 1};
+    if (!make_tmap(&tq, q, 3, dq, box) || !make_tmap(&tk, k, 3, dk, box) ||
+        !make_tmap(&tv, v, 3, dk, box))
+        return ATTN_ERR_CUDA;
+    TcParams p{};
+    p.Nq = N;
+    p.Nkv = N;
+    p.c_log2 = scale * kLog2e;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.err = c.err;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    const dim3 grid(cdiv(N, kNQ * kBM), B * Hq);
+    return D == 128 ? launch_tc<128, false, true>(c, tq, tk, tv, p, grid)
+                    : launch_tc<64, false, true>(c, tq, tk, tv, p, grid);
 }
 
 bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]) {

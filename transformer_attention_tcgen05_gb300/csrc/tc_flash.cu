@@ -96,7 +96,8 @@ struct TcCfg {
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int NSOFT = 4 * kNQ;
     static constexpr int W_MMA = NSOFT;
-    static constexpr int W_LOAD = NSOFT + 1;
+    static constexpr int W_LOAD = NSOFT + 1;              // Q and K copies
+    static constexpr int W_LOADV = NSOFT + 2;             // V copies
     static constexpr int NT = (NSOFT + 4) * 32;            // 3 warpgroups
     // register split: launch 168 x 384 = 64512; 2 x 128 x 224 + 128 x 56 = 64512
     static constexpr int REGS_LAUNCH = 168;
@@ -135,7 +136,9 @@ struct TcParams {
 template <int NS>
 struct Bars {
     uint64_t q_full;
-    uint64_t k_full[NS], v_full[NS], kv_empty[NS];
+    // K and V rings are released separately: a K stage as soon as the Q K^T
+    // products that read it have completed, a V stage after its P V
+    uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
     uint64_t s_full[kNQ], s_free[kNQ], p_ready[kNQ], o_done[kNQ];
     uint64_t drain;
     uint32_t tmem_base;
@@ -149,6 +152,17 @@ struct NaTile {
     int ut, nhc, nwc;        // union t extent, h chunks, w chunks
     int ntiles;              // key tiles = ut * nhc * nwc (0 if the box is empty)
 };
+
+// a[t] for a per-query-tile array and a run-time t, by selects: indexing
+// the array with a run-time value would place it in local memory
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[kNQ], int t) {
+    T r = a[0];
+#pragma unroll
+    for (int i = 1; i < kNQ; ++i)
+        if (t == i) r = a[i];
+    return r;
+}
 
 __device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t) {
     NaTile g;
@@ -192,6 +206,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                const __grid_constant__ CUtensorMap tv, const TcParams p) {
     using C = TcCfg<D, NA>;
     static_assert(!(NA && CAUSAL), "causal prefill is a full-attention variant");
+    static_assert(sizeof(Bars<C::NSTAGE>) <= 512, "barrier block must fit its reserved bytes");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
@@ -237,7 +252,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         for (int s = 0; s < C::NSTAGE; ++s) {
             ptx::mbar_init(&bars->k_full[s], 1);
             ptx::mbar_init(&bars->v_full[s], 1);
-            ptx::mbar_init(&bars->kv_empty[s], 1);
+            ptx::mbar_init(&bars->k_empty[s], 1);
+            ptx::mbar_init(&bars->v_empty[s], 1);
         }
         for (int t = 0; t < kNQ; ++t) {
             ptx::mbar_init(&bars->s_full[t], 1);
@@ -281,6 +297,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         // w chunk wc, channel dh holds -penalty if h lies outside the h window of
         // query offset dh, channel bh + dw likewise for w
         const uint32_t neg = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(-p.penalty)));
+#pragma unroll
         for (int u = 0; u < C::STREAMS; ++u) {
             if (n_t[u] == 0) continue;
             const int nv = g[u].nhc * g[u].nwc;
@@ -319,62 +336,69 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
     if (warp >= C::NSOFT) {
         ptx::regs_decrease<C::REGS_OTHER>();
-        if (warp == C::W_LOAD && lane == 0) {
-            // ============================================= TMA loader
-            ptx::prefetch_tmap(&tq);
-            ptx::prefetch_tmap(&tk);
-            ptx::prefetch_tmap(&tv);
-            const uint64_t pol_q = ptx::l2_policy_evict_first();
+        if ((warp == C::W_LOAD || warp == C::W_LOADV) && lane == 0) {
+            // ============================================= TMA loaders: one
+            // thread streams Q and the K ring, another the V ring, so each
+            // ring refills as soon as its own stage is released
+            const int which = warp == C::W_LOAD ? 0 : 1;
+            const CUtensorMap *tm = which == 0 ? &tk : &tv;
+            uint64_t *full = which == 0 ? bars->k_full : bars->v_full;
+            uint64_t *empty = which == 0 ? bars->k_empty : bars->v_empty;
+            ptx::prefetch_tmap(tm);
             const uint64_t pol_kv = ptx::l2_policy_evict_last();
-            uint32_t qbytes = 0;
-            if constexpr (NA) {
-                for (int t = 0; t < kNQ; ++t)
-                    if (n_t[t] > 0) qbytes += C::PANELS * p.bt * p.bh * p.bw * 128;
-            } else {
-                qbytes = kNQ * C::Q_BYTES;
-            }
-            ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
-            for (int t = 0; t < kNQ; ++t)
-                for (int pn = 0; pn < C::PANELS; ++pn) {
-                    uint8_t *dst = smem + C::OFF_Q + t * C::Q_BYTES + pn * C::PANEL_Q;
-                    if constexpr (NA) {
-                        if (n_t[t] > 0)
-                            ptx::tma_load_5d(dst, &tq, pn * 64, g[t].w0, g[t].h0, g[t].t0, bh,
-                                             &bars->q_full, pol_q);
-                    } else {
-                        ptx::tma_load_3d(dst, &tq, pn * 64, q0 + t * kBM, bh, &bars->q_full, pol_q);
-                    }
+            if (which == 0) {
+                ptx::prefetch_tmap(&tq);
+                const uint64_t pol_q = ptx::l2_policy_evict_first();
+                uint32_t qbytes = 0;
+                if constexpr (NA) {
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t)
+                        if (n_t[t] > 0) qbytes += C::PANELS * p.bt * p.bh * p.bw * 128;
+                } else {
+                    qbytes = kNQ * C::Q_BYTES;
                 }
+                ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+#pragma unroll
+                for (int t = 0; t < kNQ; ++t)
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        uint8_t *dst = smem + C::OFF_Q + t * C::Q_BYTES + pn * C::PANEL_Q;
+                        if constexpr (NA) {
+                            if (n_t[t] > 0)
+                                ptx::tma_load_5d(dst, &tq, pn * 64, g[t].w0, g[t].h0, g[t].t0, bh,
+                                                 &bars->q_full, pol_q);
+                        } else {
+                            ptx::tma_load_3d(dst, &tq, pn * 64, q0 + t * kBM, bh, &bars->q_full,
+                                             pol_q);
+                        }
+                    }
+            }
             int issued = 0;
             for (int j = 0; j < steps; ++j) {
                 const int s = j % C::NSTAGE;
                 if (j >= C::NSTAGE &&
-                    !ptx::mbar_wait_or_abort(&bars->kv_empty[s], ((j / C::NSTAGE) - 1) & 1, p.err,
-                                             abort))
+                    !ptx::mbar_wait_or_abort(&empty[s], ((j / C::NSTAGE) - 1) & 1, p.err, abort))
                     break;
                 issued = j + 1;
                 // a shared K/V stream (no neighborhood boxes) serves both query
                 // tiles, so it runs for the longer of the two tile counts
                 auto stream_has = [&](int u) { return NA ? j < n_t[u] : j < steps; };
                 uint32_t bytes = 0;
+#pragma unroll
                 for (int u = 0; u < C::STREAMS; ++u)
                     if (stream_has(u)) bytes += C::PANELS * BNt * 128;
-                for (int which = 0; which < 2; ++which) {
-                    uint64_t *bar = which == 0 ? &bars->k_full[s] : &bars->v_full[s];
-                    const CUtensorMap *tm = which == 0 ? &tk : &tv;
-                    ptx::mbar_arrive_expect_tx(bar, bytes);
-                    for (int u = 0; u < C::STREAMS; ++u) {
-                        if (!stream_has(u)) continue;
-                        for (int pn = 0; pn < C::PANELS; ++pn) {
-                            uint8_t *dst = smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) +
-                                           pn * C::PANEL_KV;
-                            if constexpr (NA) {
-                                int kt_, kh_, kw_;
-                                na_key_box(g[u], p.KH, j, kt_, kh_, kw_);
-                                ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, bar, pol_kv);
-                            } else {
-                                ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bkv, bar, pol_kv);
-                            }
+                ptx::mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+                for (int u = 0; u < C::STREAMS; ++u) {
+                    if (!stream_has(u)) continue;
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        uint8_t *dst =
+                            smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) + pn * C::PANEL_KV;
+                        if constexpr (NA) {
+                            int kt_, kh_, kw_;
+                            na_key_box(g[u], p.KH, j, kt_, kh_, kw_);
+                            ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, &full[s], pol_kv);
+                        } else {
+                            ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bkv, &full[s], pol_kv);
                         }
                     }
                 }
@@ -382,11 +406,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             // after a timeout elsewhere: let the copies this thread issued land
             // (bounded) before the CTA's shared memory is released
             if (*abort) {
-                ptx::mbar_wait(&bars->q_full, 0, nullptr);
-                for (int j = imax(0, issued - C::NSTAGE); j < issued; ++j) {
-                    ptx::mbar_wait(&bars->k_full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
-                    ptx::mbar_wait(&bars->v_full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
-                }
+                if (which == 0) ptx::mbar_wait(&bars->q_full, 0, nullptr);
+                for (int j = imax(0, issued - C::NSTAGE); j < issued; ++j)
+                    ptx::mbar_wait(&full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
             }
         } else if (warp == C::W_MMA && lane == 0) {
             // ============================================= MMA issuer
@@ -428,9 +450,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             bool ok = ptx::mbar_wait_or_abort(&bars->q_full, 0, p.err, abort) &&
                       (steps == 0 || ptx::mbar_wait_or_abort(&bars->k_full[0], 0, p.err, abort));
             ptx::tc_fence_after();
-            if (ok)
+            if (ok) {
+#pragma unroll
                 for (int t = 0; t < kNQ; ++t)
                     if (n_t[t] > 0) issue_qk(t, 0);
+                if (steps > 0) ptx::tc_commit(&bars->k_empty[0]);
+            }
             for (int j = 0; ok && j < steps; ++j) {
                 const int s = j % C::NSTAGE;
                 const uint32_t ph = (j / C::NSTAGE) & 1;
@@ -451,7 +476,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 };
                 if constexpr (C::SEP_P) {
                     // next S as soon as the softmax holds the current one in registers
-                    for (int t = 0; t < kNQ && ok; ++t) {
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t) {
+                        if (!ok) break;
                         if (j + 1 >= n_t[t]) continue;
                         ok = ptx::mbar_wait_or_abort(&bars->s_free[t], j & 1, p.err, abort);
                         wait_k1();
@@ -459,7 +486,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         ptx::tc_fence_after();
                         issue_qk(t, j + 1);
                     }
-                    for (int t = 0; t < kNQ && ok; ++t) {
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t) {
+                        if (!ok) break;
                         if (j >= n_t[t]) continue;
                         ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
                         wait_v();
@@ -468,7 +497,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         issue_pv(t, j);
                     }
                 } else {
-                    for (int t = 0; t < kNQ && ok; ++t) {
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t) {
+                        if (!ok) break;
                         if (j >= n_t[t]) continue;
                         ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
                         wait_v();
@@ -483,7 +514,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         }
                     }
                 }
-                ptx::tc_commit(&bars->kv_empty[s]);
+                // every Q K^T of step j + 1 and every P V of step j is issued
+                if (j + 1 < steps) ptx::tc_commit(&bars->k_empty[s1]);
+                ptx::tc_commit(&bars->v_empty[s]);
             }
             // drain: every MMA this thread issued has completed before TMEM is freed
             ptx::tc_commit(&bars->drain);
@@ -504,12 +537,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         // query of this row (neighborhood path) and its window
         int qt = 0, qh = 0, qw = 0, wst = 0, wsh = 0, wsw = 0;
         bool qvalid;
+        const NaTile gt = pick(g, t);           // this warp's tile, in registers
+        const int nt = pick(n_t, t);
         if constexpr (NA) {
             const int dt = row / (p.bh * p.bw), dh = (row / p.bw) % p.bh, dw = row % p.bw;
-            qt = g[t].t0 + dt;
-            qh = g[t].h0 + dh;
-            qw = g[t].w0 + dw;
-            qvalid = n_t[t] > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
+            qt = gt.t0 + dt;
+            qh = gt.h0 + dh;
+            qw = gt.w0 + dw;
+            qvalid = nt > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
             wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
             wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
             wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
@@ -519,7 +554,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        const int nt = n_t[t];
         // neighborhood: key sub-box counters (w fastest, then h, then t)
         int tc = 0, hc = 0, wc = 0;
         for (int j = 0; j < nt; ++j) {
@@ -535,10 +569,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             //      sub-box skips it
             bool warp_any = true, t_ok = true;
             if constexpr (NA) {
-                const int kt_ = g[t].u0t + tc, kh_ = g[t].u0h + hc * p.KH, kw_ = g[t].u0w + wc * kKW;
-                if (++wc == g[t].nwc) {
+                const int kt_ = gt.u0t + tc, kh_ = gt.u0h + hc * p.KH, kw_ = gt.u0w + wc * kKW;
+                if (++wc == gt.nwc) {
                     wc = 0;
-                    if (++hc == g[t].nhc) {
+                    if (++hc == gt.nhc) {
                         hc = 0;
                         ++tc;
                     }

@@ -237,6 +237,25 @@ __device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t sbo)
            (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
 }
 
+// The two 32-bit words of the descriptors above.  The high word (stride
+// offset, version, layout type) does not depend on the start address, so a
+// loop can keep only low words and move the start address with a 32-bit add.
+__host__ __device__ constexpr uint32_t desc_hi_sw128(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__host__ __device__ constexpr uint32_t desc_hi_sw32(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (6u << 29);
+}
+__device__ __forceinline__ uint32_t desc_lo_sw128(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint32_t desc_lo_sw32(uint32_t saddr) {
+    return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi) {
+    return (uint64_t(hi) << 32) | lo;
+}
+
 __host__ __device__ constexpr uint32_t sw32_offset(uint32_t row, uint32_t half) {
     return row * 32u + ((half ^ ((row >> 2) & 1u)) << 4);
 }

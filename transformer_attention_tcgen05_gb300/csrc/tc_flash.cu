@@ -10,10 +10,11 @@
 //   warps 0-3   softmax warpgroup of Q0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax warpgroup of Q1
 //   warp  8     MMA issuer (one elected thread) and TMEM owner
-//   warp  9     TMA loader (one elected thread); warps 10-11 only donate
-//               registers: the third warpgroup drops to 56 registers per
+//   warp  9     TMA loader of Q and K (one elected thread)
+//   warp 10     TMA loader of V (one elected thread); warp 11 only donates
+//               registers: the third warpgroup drops to 72 registers per
 //               thread (setmaxnreg) so the softmax warpgroups can hold a whole
-//               128-column S row in registers (224 per thread).
+//               128-column S row in registers (216 per thread).
 // Tensor memory (512 columns): S_t at [128 t, 128 t + 128), O_t at
 // [256 + D t, 256 + D (t + 1)).  With D = 128 the columns are full and P_t
 // (bf16, two per column) overwrites the first 64 columns of S_t once the
@@ -99,10 +100,10 @@ struct TcCfg {
     static constexpr int W_LOAD = NSOFT + 1;              // Q and K copies
     static constexpr int W_LOADV = NSOFT + 2;             // V copies
     static constexpr int NT = (NSOFT + 4) * 32;            // 3 warpgroups
-    // register split: launch 168 x 384 = 64512; 2 x 128 x 224 + 128 x 56 = 64512
+    // register split: launch 168 x 384 = 64512; 2 x 128 x 216 + 128 x 72 = 64512
     static constexpr int REGS_LAUNCH = 168;
-    static constexpr int REGS_SOFTMAX = 224;
-    static constexpr int REGS_OTHER = 56;
+    static constexpr int REGS_SOFTMAX = 216;
+    static constexpr int REGS_OTHER = 72;
     static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= NT * REGS_LAUNCH,
                   "setmaxnreg split must fit the launch's register file share");
     // K (or V) tile of stream u in stage s
@@ -414,36 +415,62 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             // ============================================= MMA issuer
             const uint32_t id_qk = ptx::idesc_bf16_f32(kBM, BNt, false);
             const uint32_t id_pv = ptx::idesc_bf16_f32(kBM, D, true);
-            const uint32_t q_base = ptx::smem_addr(smem + C::OFF_Q);
+            // Matrix descriptors are built once: a k-step, a stage or a tile only
+            // moves the start-address field (bits 0-13, byte address >> 4, no
+            // carry out of it below 256 KB), so each MMA costs one add here
+            // instead of a rebuilt 64-bit descriptor on this single thread.
+            constexpr uint32_t HI128 = ptx::desc_hi_sw128(1024), HI32 = ptx::desc_hi_sw32(256);
+            const uint32_t dq0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::OFF_Q), 16);
+            const uint32_t dk0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::k_off(0, 0)), 16);
+            const uint32_t dv0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::v_off(0, 0)), C::PANEL_KV);
+            uint32_t dqx0 = 0, dkx0 = 0;
+            int vq[kNQ], nv[kNQ];                // penalty tile of each tile's next Q K^T
+#pragma unroll
+            for (int t = 0; t < kNQ; ++t) {
+                vq[t] = 0;
+                nv[t] = 1;
+            }
+            if constexpr (NA) {
+                dqx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::OFF_QX));
+                dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(0, 0)));
+#pragma unroll
+                for (int t = 0; t < kNQ; ++t) nv[t] = imax(1, g[t].nhc * g[t].nwc);
+            }
+            const int nkv = BNt / 16;            // k-steps of P V
             auto issue_qk = [&](int t, int j) {
                 const int s = j % C::NSTAGE;
-                const uint32_t k_base = ptx::smem_addr(smem + C::k_off(s, C::STREAMS == 1 ? 0 : t));
+                const uint32_t a0 = dq0 + uint32_t((t * C::Q_BYTES) >> 4);
+                const uint32_t b0 =
+                    dk0 + uint32_t((s * C::STAGE_BYTES + (C::STREAMS == 1 ? 0 : t) * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t a = ptx::smem_desc_sw128(
-                        q_base + t * C::Q_BYTES + (kk >> 2) * C::PANEL_Q + off, 16, 1024);
-                    const uint64_t b =
-                        ptx::smem_desc_sw128(k_base + (kk >> 2) * C::PANEL_KV + off, 16, 1024);
-                    ptx::mma_ss(tmem + C::TM_S + t * kBN, a, b, id_qk, kk > 0);
+                    const uint32_t oa = ((kk >> 2) * C::PANEL_Q + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * C::PANEL_KV + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss(tmem + C::TM_S + t * kBN, ptx::desc_join(a0 + oa, HI128),
+                                ptx::desc_join(b0 + ob, HI128), id_qk, kk > 0);
                 }
                 if constexpr (NA) {
-                    // + window penalties: one more k-step over the 16 extra channels
-                    const uint64_t a = ptx::smem_desc_sw32(
-                        ptx::smem_addr(smem + C::OFF_QX + t * kBM * C::X_ROW), 256);
-                    const int v = j % (g[t].nhc * g[t].nwc);
-                    const uint64_t b = ptx::smem_desc_sw32(ptx::smem_addr(smem + C::kxv_off(t, v)), 256);
-                    ptx::mma_ss(tmem + C::TM_S + t * kBN, a, b, id_qk, 1u);
+                    // + window penalties: one more k-step over the 16 extra channels;
+                    // QK_t(j) uses penalty tile j mod (h chunks x w chunks)
+                    const uint32_t a = dqx0 + uint32_t((t * kBM * C::X_ROW) >> 4);
+                    const uint32_t b = dkx0 + uint32_t(((t * C::MAXV + vq[t]) * C::KX_BYTES) >> 4);
+                    if (++vq[t] == nv[t]) vq[t] = 0;
+                    ptx::mma_ss(tmem + C::TM_S + t * kBN, ptx::desc_join(a, HI32), ptx::desc_join(b, HI32),
+                                id_qk, 1u);
                 }
                 ptx::tc_commit(&bars->s_full[t]);
             };
             auto issue_pv = [&](int t, int j) {
                 const int s = j % C::NSTAGE;
-                const uint32_t v_base = ptx::smem_addr(smem + C::v_off(s, C::STREAMS == 1 ? 0 : t));
-                for (int kk = 0; kk < BNt / 16; ++kk) {
-                    const uint64_t b = ptx::smem_desc_sw128(v_base + kk * 2048, C::PANEL_KV, 1024);
-                    ptx::mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_P + t * C::PSTRIDE + kk * 8, b,
-                                id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                const uint32_t b0 =
+                    dv0 + uint32_t((s * C::STAGE_BYTES + (C::STREAMS == 1 ? 0 : t) * C::KV_BYTES) >> 4);
+                const uint32_t a0 = tmem + C::TM_P + t * C::PSTRIDE;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    if (kk >= nkv) break;
+                    ptx::mma_ts(tmem + C::TM_O + t * D, a0 + kk * 8,
+                                ptx::desc_join(b0 + uint32_t(kk * (2048 >> 4)), HI128), id_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::tc_commit(&bars->o_done[t]);
             };

@@ -562,7 +562,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         const float cl = p.c_log2;
 
         // query of this row (neighborhood path) and its window
-        int qt = 0, qh = 0, qw = 0, wst = 0, wsh = 0, wsw = 0;
+        int qt = 0, qh = 0, qw = 0, wst = 0;
         bool qvalid;
         const NaTile gt = pick(g, t);           // this warp's tile, in registers
         const int nt = pick(n_t, t);
@@ -573,8 +573,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             qw = gt.w0 + dw;
             qvalid = nt > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
             wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
-            wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
-            wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
         } else {
             qvalid = q0 + t * kBM + row < p.Nq;
         }
@@ -591,12 +589,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             }
             ptx::tc_fence_after();
 
-            // ---- neighborhood: the window penalties are already in S (extra MMA
-            //      channels); a warp none of whose 32 windows reaches this key
-            //      sub-box skips it
-            bool warp_any = true, t_ok = true;
+            // ---- neighborhood: the h and w window penalties are already in S
+            //      (extra MMA channels); a row whose t window misses this key
+            //      sub-box's frame gets P = 0 below.  (Skipping sub-boxes that
+            //      none of a warp's 32 windows reaches measured slower than
+            //      computing them: the MMAs run anyway and the test costs issue
+            //      slots on the critical path.)
+            bool t_ok = true;
             if constexpr (NA) {
-                const int kt_ = gt.u0t + tc, kh_ = gt.u0h + hc * p.KH, kw_ = gt.u0w + wc * kKW;
+                const int kt_ = gt.u0t + tc;
                 if (++wc == gt.nwc) {
                     wc = 0;
                     if (++hc == gt.nhc) {
@@ -605,28 +606,23 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     }
                 }
                 t_ok = qvalid && unsigned(kt_ - wst) < unsigned(p.et);
-                const bool reach = t_ok && kh_ < wsh + p.eh && wsh < kh_ + p.KH &&
-                                   kw_ < wsw + p.ew && wsw < kw_ + kKW;
-                warp_any = __any_sync(0xffffffffu, reach);
             }
 
             float sv[kBN];
-            if (warp_any) {
 #pragma unroll
-                for (int c = 0; c < kBN / 32; ++c)
-                    if (c * 32 < BNt)
-                        ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
-                ptx::tmem_wait_ld();
-            }
+            for (int c = 0; c < kBN / 32; ++c)
+                if (c * 32 < BNt)
+                    ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+            ptx::tmem_wait_ld();
             if constexpr (C::SEP_P) {
-                // S_t is in registers (or not needed): the next QK_t may overwrite it
+                // S_t is in registers: the next QK_t may overwrite it
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bars->s_free[t]);
             }
 
             // ---- mask and tile maximum
-            float mt = -INFINITY;
-            if (warp_any) {
+            float mt;
+            {
                 if constexpr (NA) {
                     // columns past this tile's keys (N = KH * 16 < 128) hold stale
                     // values: whole 16-column groups, warp-uniform
@@ -715,7 +711,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             for (int c = 0; c < kBN / 32; ++c) {
                 if (c * 32 >= BNt) break;
                 uint32_t pk[16];
-                if (warp_any) {
+                {
                     // the upper 16 keys of the last 32-key chunk may lie past the tile
                     const int ne = (c * 32 + 32 <= BNt) ? 16 : 8;
 #pragma unroll
@@ -732,9 +728,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                                    acc[(2 * e + 1) & 7], p0, p1);
                         pk[e] = pack_bf16x2(p0, p1);
                     }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
                 }
                 ptx::tmem_st16(p_addr + c * 16, pk);
             }

@@ -122,8 +122,11 @@ ATTN_API attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const v
  *   Requires Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}, D in {64, 128}.
  *   workspace: DEVICE scratch of attn_decode_gqa_workspace_bytes(...) bytes,
  *   256-byte aligned, ZERO-FILLED before its first use.  It holds per-split
- *   partial results and per-(batch, kv-head) arrival counters; every call that
- *   completes leaves the counters at zero again, so the same workspace serves
+ *   partial results and per-(batch, kv-head) arrival counters when the splits
+ *   merge through global memory; when the splits of every (batch, kv-head)
+ *   fit on the GPU at once as thread-block clusters they merge through
+ *   distributed shared memory instead and the workspace is not touched.
+ *   Every call that completes leaves the counters at zero, so the same workspace serves
  *   the next call without clearing.  Calls that share a workspace must not
  *   overlap on the GPU.  After a call that reported a device error, zero it
  *   again.

@@ -221,6 +221,16 @@ def test_decode_workspace_is_reusable_and_deterministic(ta):
     assert_close(to_host64(o2), ref, "bf16", "decode reuse")
 
 
+def test_decode_more_units_than_resident_clusters(ta):
+    """1280 (batch, kv-head) units are more than the GPU holds as clusters at
+    once, so the splits merge through the workspace (atomic ticket) rather
+    than through distributed shared memory; same parity bar."""
+    rng = np.random.default_rng(7401)
+    sl = tuple(int(x) for x in rng.integers(1, 97, size=160))
+    _decode_case(ta, WORKLOADS["gqa_decode"].with_(B=160, H=8, Hkv=8, D=64, Lmax=96, seq_len=sl,
+                                                   seed=7401))
+
+
 def test_decode_rejects_bad_seq_len_on_device(ta):
     import torch
     w = WORKLOADS["gqa_decode"].with_(B=2, Lmax=128)

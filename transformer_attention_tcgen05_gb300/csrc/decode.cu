@@ -44,6 +44,7 @@ constexpr int kCW = 4;          // consumer warps
 constexpr int kSlots = 4;       // ring slots (one chunk each); chunk i -> slot i % kSlots
 static_assert(kSlots % kCW == 0, "every slot must always feed the same consumer warp");
 constexpr int kMaxSplits = 256;
+constexpr int kMaxClusterSplits = 8;   // portable cluster size
 
 template <int D, int GP>
 struct DecCfg {
@@ -62,7 +63,10 @@ struct DecCfg {
     static constexpr int SMEM = OFF_BAR + 2 * kSlots * 8 + 16 + 1024;
     // the warp-merge area [CW][GP][D+2] f32 reuses the K slots after the loop
     static constexpr int OFF_M = 0;
-    static_assert(kCW * GP * (D + 2) * 4 <= kSlots * TILE, "merge area must fit the K slots");
+    // then (cluster merge) the CTA's own partial [GP][D] o and [GP][2] (m, l)
+    static constexpr int OFF_CP = OFF_M + kCW * GP * (D + 2) * 4;
+    static_assert(OFF_CP + GP * (D + 2) * 4 <= kSlots * TILE,
+                  "merge areas must fit the K slots");
 };
 
 struct DecParams {
@@ -85,7 +89,10 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&x)[8]) {
     x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
 }
 
-template <int D, int GP>
+// CL: the splits of one (batch, kv-head) form one thread-block cluster and
+// merge their partials through distributed shared memory (no workspace, no
+// atomics); otherwise the last CTA to arrive merges them from the workspace.
+template <int D, int GP, bool CL>
 __global__ void __launch_bounds__(DecCfg<D, GP>::NT)
 decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
               const DecParams p) {
@@ -306,6 +313,63 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
 
     // ---- CTA merge of the consumer warps -> one partial per head
     const bool aborted = s_abort != 0;
+    if constexpr (CL) {
+        // Partial into this CTA's shared memory (an aborted CTA's is garbage,
+        // the error word is already set); every CTA of the cluster passes both
+        // cluster barriers, so none leaves while another reads its memory.
+        float *cp_o = reinterpret_cast<float *>(smem + C::OFF_CP);   // [GP][D]
+        float *cp_ml = cp_o + GP * D;                                 // [GP][2]
+        for (int e = threadIdx.x; e < GP * D; e += C::NT) {
+            const int h = e / D, d = e % D;
+            float M = -INFINITY;
+            for (int w = 0; w < kCW; ++w) M = fmaxf(M, s_merge[(w * GP + h) * (D + 2) + D]);
+            float O = 0.f, Lsum = 0.f;
+            if (M != -INFINITY) {
+                for (int w = 0; w < kCW; ++w) {
+                    const float *wm = s_merge + (w * GP + h) * (D + 2);
+                    const float f = exp2f(wm[D] - M);   // -inf -> 0
+                    O += wm[d] * f;
+                    Lsum += wm[D + 1] * f;
+                }
+            }
+            cp_o[e] = O;
+            if (d == 0) {
+                cp_ml[h * 2] = M;
+                cp_ml[h * 2 + 1] = Lsum;
+            }
+        }
+        ptx::cluster_sync();
+        // CTA r of the cluster merges heads r, r + splits, ... over all CTAs,
+        // in rank order (the same order whichever CTA finishes first)
+        const int csz = gridDim.x;               // cluster = the splits of this unit
+        const uint32_t o_base = ptx::smem_addr(cp_o), ml_base = ptx::smem_addr(cp_ml);
+        for (int h = blockIdx.x; h < p.G; h += csz)
+            for (int d = threadIdx.x; d < D; d += C::NT) {
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits], os[kMaxClusterSplits];
+                float M = -INFINITY;
+#pragma unroll
+                for (int r = 0; r < kMaxClusterSplits; ++r) {
+                    ms[r] = -INFINITY;
+                    ls[r] = os[r] = 0.f;
+                    if (r < csz) {
+                        ms[r] = ptx::ld_cluster_f32(ptx::cluster_map(ml_base + h * 8, r));
+                        ls[r] = ptx::ld_cluster_f32(ptx::cluster_map(ml_base + h * 8 + 4, r));
+                        os[r] = ptx::ld_cluster_f32(ptx::cluster_map(o_base + (h * D + d) * 4, r));
+                    }
+                    M = fmaxf(M, ms[r]);
+                }
+                float O = 0.f, Lsum = 0.f;
+#pragma unroll
+                for (int r = 0; r < kMaxClusterSplits; ++r) {
+                    const float w = ms[r] == -INFINITY ? 0.f : exp2f(ms[r] - M);
+                    O += os[r] * w;
+                    Lsum += ls[r] * w;
+                }
+                p.o[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] = __float2bfloat16_rn(O / Lsum);
+            }
+        ptx::cluster_sync();
+        return;
+    }
     if (!aborted) {
         float *po = p.part_o + (size_t(unit) * p.ws_splits + split) * GP * D;
         float *pml = p.part_ml + (size_t(unit) * p.ws_splits + split) * GP * 2;
@@ -438,11 +502,96 @@ attn_status_t launch(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
                      int B) {
     using C = DecCfg<D, GP>;
     static int done_mask = 0;
-    auto kern = decode_kernel<D, GP>;
+    auto kern = decode_kernel<D, GP, false>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     kern<<<dim3(p.splits, p.Hkv, B), C::NT, C::SMEM, c.stream>>>(tk, tv, p);
     return launch_status(kFamDecode);
+}
+
+constexpr int kMaxDevices = 64;
+
+// Launch configuration of the cluster-merge kernel: one cluster of `splits`
+// CTAs per (batch, kv-head).
+template <int D, int GP>
+cudaLaunchConfig_t cluster_config(const Ctx &c, int splits, int Hkv, int B,
+                                  cudaLaunchAttribute *attr) {
+    using C = DecCfg<D, GP>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, Hkv, B);
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = c.stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = splits;
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Largest cluster size in [2, min(8, target)] for which the clusters of all
+// `units` (batch, kv-head) pairs are resident at once (one wave: no cluster
+// waits for another to finish), or 0.  The occupancy answer depends only on
+// the device and the kernel, so it is looked up once per size.
+template <int D, int GP>
+int cluster_splits(const Ctx &c, int units, int target) {
+    using C = DecCfg<D, GP>;
+    static std::mutex mu;
+    static int active[kMaxDevices][kMaxClusterSplits + 1];   // 0 = not looked up, -1 = none
+    static int done_mask = 0;
+    if (c.device < 0 || c.device >= kMaxDevices) return 0;
+    auto kern = decode_kernel<D, GP, true>;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int cs = imin(kMaxClusterSplits, target); cs >= 2; --cs) {
+        int &a = active[c.device][cs];
+        if (a == 0) {
+            cudaLaunchAttribute attr;
+            cudaLaunchConfig_t cfg = cluster_config<D, GP>(c, cs, 1, 1, &attr);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            a = n > 0 ? n : -1;
+        }
+        if (a >= units) return cs;
+    }
+    return 0;
+}
+
+template <int D, int GP>
+attn_status_t launch_cluster(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
+                             DecParams p, int B) {
+    static int done_mask = 0;
+    auto kern = decode_kernel<D, GP, true>;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), DecCfg<D, GP>::SMEM, c.device,
+                          &done_mask))
+        return ATTN_ERR_RESOURCE;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = cluster_config<D, GP>(c, p.splits, p.Hkv, B, &attr);
+    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
+    return launch_status(kFamDecode);
+}
+
+// Cluster merge when every unit's cluster fits one wave; else the workspace
+// (atomic ticket) merge.
+template <int D, int GP>
+attn_status_t launch_best(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
+                          DecParams p, int B, int Lmax) {
+    const int cs = cluster_splits<D, GP>(c, B * p.Hkv, p.splits);
+    if (cs >= 2) {
+        p.splits = cs;
+        p.split_rows = cdiv(cdiv(Lmax, cs), kRowsPerChunk) * kRowsPerChunk;
+        return launch_cluster<D, GP>(c, tk, tv, p, B);
+    }
+    return launch<D, GP>(c, tk, tv, p, B);
 }
 
 int gp_for(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
@@ -493,17 +642,17 @@ attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void 
     p.err = c.err;
     if (D == 128) {
         switch (GP) {
-            case 1: return launch<128, 1>(c, tk, tv, p, B);
-            case 2: return launch<128, 2>(c, tk, tv, p, B);
-            case 4: return launch<128, 4>(c, tk, tv, p, B);
-            default: return launch<128, 8>(c, tk, tv, p, B);
+            case 1: return launch_best<128, 1>(c, tk, tv, p, B, Lmax);
+            case 2: return launch_best<128, 2>(c, tk, tv, p, B, Lmax);
+            case 4: return launch_best<128, 4>(c, tk, tv, p, B, Lmax);
+            default: return launch_best<128, 8>(c, tk, tv, p, B, Lmax);
         }
     }
     switch (GP) {
-        case 1: return launch<64, 1>(c, tk, tv, p, B);
-        case 2: return launch<64, 2>(c, tk, tv, p, B);
-        case 4: return launch<64, 4>(c, tk, tv, p, B);
-        default: return launch<64, 8>(c, tk, tv, p, B);
+        case 1: return launch_best<64, 1>(c, tk, tv, p, B, Lmax);
+        case 2: return launch_best<64, 2>(c, tk, tv, p, B, Lmax);
+        case 4: return launch_best<64, 4>(c, tk, tv, p, B, Lmax);
+        default: return launch_best<64, 8>(c, tk, tv, p, B, Lmax);
     }
 }
 

@@ -83,6 +83,29 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     return true;
 }
 
+// ------------------------------------------------------------- clusters
+
+// Cluster-wide barrier (every non-exited thread of every CTA of the cluster);
+// release/acquire order shared-memory writes before it with reads after it,
+// also across CTAs.  Warp-converged (.aligned).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------- bulk copies
 
 // Contiguous global -> shared copy (TMA, non-tensor); completes `bytes` of

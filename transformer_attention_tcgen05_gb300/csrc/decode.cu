@@ -13,7 +13,11 @@
 //    read exactly once (GQA head sharing).
 //  * a producer warp streams 32-row chunks of K and V with TMA tensor copies
 //    (128-byte swizzle, L2 evict-first) into a 4-slot shared-memory ring;
-//    chunk i goes to slot i % 4 and is consumed by consumer warp i % 4.
+//    chunk i goes to slot i % 4 and is consumed by consumer warp i % 4.  The
+//    K and V halves of a slot have their own barriers and their own producer
+//    lane: a warp frees the K half right after Q K^T, so the next chunk's K
+//    arrives while it computes P V (with one barrier per slot every warp sat
+//    idle for a full load latency per chunk).
 //  * Q K^T: lane = cache row.  Each lane reads its row in 16-byte chunks (the
 //    swizzle makes the 32 rows' reads bank-conflict free) against q held in
 //    shared memory as fp32 (broadcast reads), with packed fp32x2 FMAs.
@@ -21,10 +25,12 @@
 //    base 2; P goes to shared memory.
 //  * P V: D/8 lanes per row, 8 channels per lane (one 16-byte swizzled read),
 //    2 or 4 rows per instruction, packed fp32x2 FMAs.
-//  * the CTA merges its warps (log-sum-exp) and writes one partial
-//    (m, l, o) per head to the workspace; the last CTA of a (batch, kv-head)
-//    to arrive (atomic ticket) merges all splits and writes the output, then
-//    resets its ticket so the workspace is ready for the next call.
+//  * the CTA merges its warps (log-sum-exp) into one partial (m, l, o) per
+//    head.  The splits of a (batch, kv-head) then merge either through
+//    distributed shared memory, as one thread-block cluster, or (when the
+//    clusters do not all fit on the GPU at once) through the workspace: the
+//    last CTA to arrive (atomic ticket) merges all splits and resets its
+//    ticket so the workspace is ready for the next call.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <float.h>
@@ -60,7 +66,7 @@ struct DecCfg {
     static constexpr int OFF_Q = 2 * kSlots * TILE;                      // [GP][D] f32
     static constexpr int OFF_P = OFF_Q + GP * D * 4;                     // [CW][32][GP] f32
     static constexpr int OFF_BAR = OFF_P + kCW * kRowsPerChunk * GP * 4;
-    static constexpr int SMEM = OFF_BAR + 2 * kSlots * 8 + 16 + 1024;
+    static constexpr int SMEM = OFF_BAR + 4 * kSlots * 8 + 16 + 1024;
     // the warp-merge area [CW][GP][D+2] f32 reuses the K slots after the loop
     static constexpr int OFF_M = 0;
     // then (cluster merge) the CTA's own partial [GP][D] o and [GP][2] (m, l)
@@ -99,8 +105,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
     using C = DecCfg<D, GP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *empty = full + kSlots;
+    // each slot's K and V halves fill and free separately: a warp frees the K
+    // half after Q K^T, so the next chunk's K loads while it computes P V
+    uint64_t *full_k = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *full_v = full_k + kSlots;
+    uint64_t *empty_k = full_v + kSlots;
+    uint64_t *empty_v = empty_k + kSlots;
     __shared__ int s_abort;
     __shared__ unsigned s_last;
 
@@ -119,10 +129,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
 
     float *q_s = reinterpret_cast<float *>(smem + C::OFF_Q);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSlots; ++s) {
-            ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
-        }
+        for (int s = 0; s < 4 * kSlots; ++s) ptx::mbar_init(&full_k[s], 1);
         ptx::fence_barrier_init();
         s_abort = 0;
     }
@@ -151,31 +158,33 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
 
     if (warp == kCW) {
         // ------------------------------------------------ producer warp
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tk);
-            ptx::prefetch_tmap(&tv);
+        // lane 0 streams the K halves of the slots, lane 1 the V halves
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap *tm = is_k ? &tk : &tv;
+            uint64_t *fb = is_k ? full_k : full_v;
+            uint64_t *eb = is_k ? empty_k : empty_v;
+            uint8_t *dst0 = smem + (is_k ? C::OFF_K : C::OFF_V);
+            ptx::prefetch_tmap(tm);
             const uint64_t pol = ptx::l2_policy_evict_first();
             int issued = 0;
             for (int it = 0; it < nchunks; ++it) {
                 const int s = it % kSlots;
-                if (it >= kSlots && !ptx::mbar_wait(&empty[s], ((it / kSlots) - 1) & 1, p.err)) {
+                if (it >= kSlots && !ptx::mbar_wait(&eb[s], ((it / kSlots) - 1) & 1, p.err)) {
                     s_abort = 1;
                     break;
                 }
                 const int j0 = r0 + it * kRowsPerChunk;
-                ptx::mbar_arrive_expect_tx(&full[s], 2 * C::TILE);
-                for (int pn = 0; pn < C::PANELS; ++pn) {
-                    ptx::tma_load_3d(smem + C::OFF_K + s * C::TILE + pn * C::PANEL, &tk, pn * 64, j0,
-                                     unit, &full[s], pol);
-                    ptx::tma_load_3d(smem + C::OFF_V + s * C::TILE + pn * C::PANEL, &tv, pn * 64, j0,
-                                     unit, &full[s], pol);
-                }
+                ptx::mbar_arrive_expect_tx(&fb[s], C::TILE);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    ptx::tma_load_3d(dst0 + s * C::TILE + pn * C::PANEL, tm, pn * 64, j0, unit, &fb[s],
+                                     pol);
                 issued = it + 1;
             }
             if (s_abort) {
                 // let the copies already issued land (bounded) before exiting
                 for (int it = imax(0, issued - kSlots); it < issued; ++it)
-                    ptx::mbar_wait(&full[it % kSlots], (it / kSlots) & 1, nullptr);
+                    ptx::mbar_wait(&fb[it % kSlots], (it / kSlots) & 1, nullptr);
             }
         }
     } else {
@@ -195,7 +204,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
 
         for (int it = warp; it < nchunks; it += kCW) {
             const int s = it % kSlots;
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full[s], (it / kSlots) & 1, p.err))) {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full_k[s], (it / kSlots) & 1, p.err))) {
                 s_abort = 1;
                 break;
             }
@@ -232,6 +241,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
                 for (int h = 0; h < GP; ++h) sc[h] = (lane < valid) ? a0[h] + a1[h] : -INFINITY;
             }
 
+            // the K half of the slot is free for the chunk kSlots ahead
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty_k[s]);
+
             // ---- online softmax per head over the warp's 32 rows
             float alpha[GP];
 #pragma unroll
@@ -249,6 +262,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
             }
             __syncwarp();
 
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full_v[s], (it / kSlots) & 1, p.err))) {
+                s_abort = 1;
+                break;
+            }
             // ---- O = O * alpha + P V
 #pragma unroll
             for (int h = 0; h < GP; ++h)
@@ -276,7 +293,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
                 }
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty[s]);
+            if (lane == 0) ptx::mbar_arrive(&empty_v[s]);
         }
 
         // ---- warp totals: P V over the row groups, row sums over the lanes

@@ -100,7 +100,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -108,7 +108,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.3)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -379,8 +379,14 @@ class CpuSample:
 
     def measure(self, budget_s):
         if self.frac is None:
-            dt, _, _, _ = self.run(0.001)                  # calibrate the sample size
-            self.frac = min(1.0, 0.001 * budget_s / max(dt, 1e-3))
+            # calibrate the sample size: time = fixed part (RoPE of all of Q and
+            # K, every decode row) + a part proportional to the sampled rows
+            f1, f2 = 0.01, 0.03
+            d1, _, _, _ = self.run(f1)
+            d2, _, _, _ = self.run(f2)
+            per = max((d2 - d1) / (f2 - f1), 1e-6)
+            fixed = max(0.0, d1 - per * f1)
+            self.frac = min(1.0, max(f2, (budget_s - fixed) / per))
         dt, fl, nj, nn = self.run(self.frac)
         return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s",
                 "cores": self.oracle.max_threads(), "kind": "oracle", "seconds": round(dt, 2),
@@ -425,7 +431,7 @@ def reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

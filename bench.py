@@ -386,7 +386,7 @@ class CpuSample:
             d2, _, _, _ = self.run(f2)
             per = max((d2 - d1) / (f2 - f1), 1e-6)
             fixed = max(0.0, d1 - per * f1)
-            self.frac = min(1.0, max(f2, (budget_s - fixed) / per))
+            self.frac = min(1.0, max(1e-4, (budget_s - fixed) / per))
         dt, fl, nj, nn = self.run(self.frac)
         return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s",
                 "cores": self.oracle.max_threads(), "kind": "oracle", "seconds": round(dt, 2),
@@ -404,7 +404,8 @@ def reference(args, rank, world):
     if rank != 0:
         return None
     host = {"joint": make_inputs(WL_JOINT), "na": make_inputs(WL_NA), "dec": make_inputs(WL_DEC)}
-    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    # about two minutes of host work for the whole --steps/--warmup run
+    budget = max(0.3, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     cs = CpuSample(host)
     for _ in range(args.warmup):
         cs.measure(budget)

@@ -201,7 +201,10 @@ __device__ __forceinline__ void na_key_box(const NaTile &g, int KH, int j, int &
     w = g.u0w + wc * kKW;
 }
 
-template <int D, bool NA, bool CAUSAL>
+// KHC > 0 fixes the neighborhood key sub-box height (keys per tile = 16 KHC)
+// at compile time, so the softmax's column loops and masks unroll without
+// run-time tests; KHC = 0 takes it from the parameters.
+template <int D, bool NA, bool CAUSAL, int KHC>
 __global__ void __launch_bounds__(TcCfg<D, NA>::NT, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams p) {
@@ -232,7 +235,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             g[t] = na_tile(p, blockIdx.x, t);
             n_t[t] = g[t].ntiles;
         }
-        BNt = p.KH * kKW;
+        BNt = (KHC > 0 ? KHC : p.KH) * kKW;
         steps = imax(n_t[0], n_t[1]);
     } else if constexpr (CAUSAL) {
         // heaviest query blocks first; query tile t sees key tiles 0 .. its diagonal
@@ -304,7 +307,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             const int nv = g[u].nhc * g[u].nwc;
             for (int i = threadIdx.x; i < nv * BNt * 2; i += C::NT) {
                 const int v = i / (BNt * 2), r = (i / 2) % BNt, half = i % 2;
-                const int kh = g[u].u0h + (v / g[u].nwc) * p.KH + r / kKW;
+                const int kh = g[u].u0h + (v / g[u].nwc) * (BNt / kKW) + r / kKW;
                 const int kw = g[u].u0w + (v % g[u].nwc) * kKW + r % kKW;
                 uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
@@ -396,7 +399,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                             smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) + pn * C::PANEL_KV;
                         if constexpr (NA) {
                             int kt_, kh_, kw_;
-                            na_key_box(g[u], p.KH, j, kt_, kh_, kw_);
+                            na_key_box(g[u], BNt / kKW, j, kt_, kh_, kw_);
                             ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, &full[s], pol_kv);
                         } else {
                             ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bkv, &full[s], pol_kv);
@@ -941,13 +944,13 @@ bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool NA, bool CAUSAL = false>
+template <int D, bool NA, bool CAUSAL = false, int KHC = 0>
 attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
     using C = TcCfg<D, NA>;
     static int done_mask = 0;
     static int regs = -1;
-    auto kern = tc_attn_kernel<D, NA, CAUSAL>;
+    auto kern = tc_attn_kernel<D, NA, CAUSAL, KHC>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     // The warpgroups re-split the launch's register file with setmaxnreg; the
@@ -1121,7 +1124,15 @@ attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v,
     p.nbw = cdiv(W, p.bw);
     p.nbw2 = cdiv(p.nbw, 2);
     const dim3 grid(cdiv(T, p.bt) * p.nbh * p.nbw2, B * H);
-    return launch_tc<64, true>(c, tq, tk, tv, p, grid);
+    // the planner's key sub-box heights (4..8) have compile-time kernels
+    switch (p.KH) {
+        case 4: return launch_tc<64, true, false, 4>(c, tq, tk, tv, p, grid);
+        case 5: return launch_tc<64, true, false, 5>(c, tq, tk, tv, p, grid);
+        case 6: return launch_tc<64, true, false, 6>(c, tq, tk, tv, p, grid);
+        case 7: return launch_tc<64, true, false, 7>(c, tq, tk, tv, p, grid);
+        case 8: return launch_tc<64, true, false, 8>(c, tq, tk, tv, p, grid);
+        default: return launch_tc<64, true>(c, tq, tk, tv, p, grid);
+    }
 }
 
 attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,

@@ -14,9 +14,11 @@
  *   - Tensors are DEVICE pointers to contiguous row-major arrays with the head
  *     dimension innermost.  Attention tensors are heads-major [B, H, N, D].
  *   - dtype ATTN_F32: float32 storage, exact fp32 FMA arithmetic (no TF32).
- *     dtype ATTN_BF16: bfloat16 storage; the contractions run on the tensor
- *     cores (tcgen05) with fp32 accumulation, the softmax in fp32; the output
- *     is rounded to bf16 (round to nearest even).
+ *     dtype ATTN_BF16 / ATTN_F16: bfloat16 / IEEE half storage (candle's
+ *     F32 / BF16 / F16 trio); the contractions run on the tensor cores
+ *     (tcgen05) with fp32 accumulation where the shapes allow (else the exact
+ *     SIMT kernel), the softmax in fp32, P rounded to the storage type for the
+ *     P V product; the output is rounded to the storage type (to nearest even).
  *   - D (head dimension) is 32, 64 or 128.
  *   - scale <= 0 selects 1/sqrt(D).
  *   - Inputs are never written.  The output must not alias any input.
@@ -50,7 +52,8 @@ extern "C" {
 
 typedef enum {
     ATTN_F32 = 0,
-    ATTN_BF16 = 1
+    ATTN_BF16 = 1,
+    ATTN_F16 = 2
 } attn_dtype_t;
 
 typedef enum {
@@ -103,8 +106,8 @@ ATTN_API size_t attn_rope_joint_workspace_bytes(int B, int H, int N, int D, attn
  * Causal grouped-query prefill (self-attention over a prompt).
  *   q, o [B, Hq, N, D]; k, v [B, Hkv, N, D]; Hq % Hkv == 0.  Query head hq
  *   reads KV head hq / (Hq / Hkv); query position i attends to key positions
- *   j <= i.  bf16 runs on the tensor cores for D in {64, 128}; fp32 (and bf16
- *   with D = 32) on the exact-FFMA SIMT kernel.
+ *   j <= i.  bf16 and f16 run on the tensor cores for D in {64, 128}; fp32
+ *   (and the 16-bit types with D = 32) on the exact-FFMA SIMT kernel.
  * Passage: fak "GPU - the in-kernel forward pass", section 3 (Llama prefill
  * workloads pp64 .. pp512 of a grouped-query model).
  */
@@ -119,7 +122,8 @@ ATTN_API attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const v
  *   a violation sets ATTN_ERR_DEVICE_CHECK and that batch's output is left
  *   unwritten).  Query head hq reads KV head hq / (Hq / Hkv) and attends to
  *   cache rows j < seq_len[b]; rows at or beyond seq_len[b] are never used.
- *   Requires Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}, D in {64, 128}.
+ *   Requires Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}, D in {64, 128}, dtype
+ *   ATTN_BF16 or ATTN_F16 (q, caches and o alike).
  *   workspace: DEVICE scratch of attn_decode_gqa_workspace_bytes(...) bytes,
  *   256-byte aligned, ZERO-FILLED before its first use.  It holds per-split
  *   partial results and per-(batch, kv-head) arrival counters when the splits
@@ -177,7 +181,7 @@ ATTN_API attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_cach
  *   [B], the write position; if advance != 0 the kernel then sets
  *   seq_len[b] += 1 (so a following attn_decode_gqa sees the new token).
  *   A position outside [0, Lmax) writes nothing and sets ATTN_ERR_DEVICE_CHECK.
- *   dtype ATTN_F32 or ATTN_BF16; D in {32, 64, 128}.
+ *   dtype ATTN_F32, ATTN_BF16 or ATTN_F16; D in {32, 64, 128}.
  * Passage: fak "GPU - the in-kernel forward pass", section 3b, step 3 (a
  * kernel-form KV append with a scalar offset replaces the cudaMemcpy whose
  * moving destination forced a graph re-instantiation every token).

@@ -75,6 +75,8 @@ def test_full_validation(L):
     assert _full(L, D=48) == 1
     assert _full(L, Nq=0) == 1
     assert _full(L, dt=7) == 1
+    assert _full(L, dt=3) == 1                           # only F32 / BF16 / F16
+    assert _full(L, dt=2, D=48) == 1                     # F16 is validated like the others
     assert _full(L, o=FAKE) == 1                         # output aliases an input
 
 
@@ -97,10 +99,11 @@ def test_decode_validation(L):
     f = ctypes.c_float(0.0)
     # Hq % Hkv != 0
     assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 6, 4, 64, 128, 1, f, ws, 1 << 20, None) == 1
-    # fp32 decode is not built (bf16 only)
+    # fp32 decode is not built (16-bit caches only)
     assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 0, f, ws, 1 << 20, None) == 2
-    # workspace too small
+    # workspace too small (bf16 and f16 caches alike)
     assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 1, f, ws, 16, None) == 3
+    assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 2, f, ws, 16, None) == 3
     # misaligned workspace
     assert L.attn_decode_gqa(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 1, f,
                              ctypes.c_void_p(0x40010), 1 << 20, None) == 1

@@ -31,7 +31,7 @@ __all__ = [
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libattn.so")
 
-ATTN_F32, ATTN_BF16 = 0, 1
+ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           3: "insufficient resources", 4: "CUDA error", 5: "device wait timed out",
           6: "device-side check failed"}
@@ -96,7 +96,9 @@ def _dtype(t: torch.Tensor) -> int:
         return ATTN_F32
     if t.dtype == torch.bfloat16:
         return ATTN_BF16
-    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float16)")
 
 
 def _cuda(*ts: torch.Tensor):

@@ -63,7 +63,10 @@ float resolve_scale(float scale, int D) {
 
 bool valid_d(int D) { return D == 32 || D == 64 || D == 128; }
 
-bool valid_dtype(attn_dtype_t dt) { return dt == ATTN_F32 || dt == ATTN_BF16; }
+bool valid_dtype(attn_dtype_t dt) { return dt == ATTN_F32 || dt == ATTN_BF16 || dt == ATTN_F16; }
+
+// bf16 and f16 run on the tensor cores where the shapes allow.
+bool half_dtype(attn_dtype_t dt) { return dt == ATTN_BF16 || dt == ATTN_F16; }
 
 size_t elem_size(attn_dtype_t dt) { return dt == ATTN_F32 ? 4 : 2; }
 
@@ -163,8 +166,8 @@ attn_status_t attn_full_fwd(const void *q, const void *k, const void *v, void *o
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (dtype == ATTN_BF16 && tc_full_supported(B, H, Nq, Nkv, D))
-        return tc_full(c, q, k, v, o, B, H, Nq, Nkv, D, sc);
+    if (half_dtype(dtype) && tc_full_supported(B, H, Nq, Nkv, D))
+        return tc_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
     return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
 }
 
@@ -182,8 +185,8 @@ attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const void *v, v
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (dtype == ATTN_BF16 && tc_full_supported(B, Hq, N, N, D))
-        return tc_causal_gqa(c, q, k, v, o, B, Hq, Hkv, N, D, sc);
+    if (half_dtype(dtype) && tc_full_supported(B, Hq, N, N, D))
+        return tc_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc);
     return simt_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc);
 }
 
@@ -222,8 +225,8 @@ attn_status_t attn_rope_joint_fwd(const void *q, const void *k, const void *v, v
     st = rope_rotate_qk(c, dtype, q, k, qr, kr, B * H, N, D, pos, axes_dim, theta);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (dtype == ATTN_BF16 && tc_full_supported(B, H, N, N, D))
-        return tc_full(c, qr, kr, v, o, B, H, N, N, D, sc);
+    if (half_dtype(dtype) && tc_full_supported(B, H, N, N, D))
+        return tc_full(c, dtype, qr, kr, v, o, B, H, N, N, D, sc);
     return simt_full(c, dtype, qr, kr, v, o, B, H, N, N, D, sc);
 }
 
@@ -243,7 +246,7 @@ attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_
     if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || !valid_dtype(dtype) || !valid_d(D))
         return ATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_BF16 || D == 32 || Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+    if (!half_dtype(dtype) || D == 32 || Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
     if ((long long)Lmax * D >= (1ll << 31) || B > 65535 || Hkv > 65535)
         return ATTN_ERR_UNSUPPORTED;
     if (o == q || o == k_cache || o == v_cache) return ATTN_ERR_INVALID_ARG;
@@ -252,7 +255,7 @@ attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_
     Ctx c;
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
-    return decode_gqa(c, q, k_cache, v_cache, seq_len, o, B, Hq, Hkv, Lmax, D,
+    return decode_gqa(c, dtype, q, k_cache, v_cache, seq_len, o, B, Hq, Hkv, Lmax, D,
                       resolve_scale(scale, D), workspace, workspace_bytes);
 }
 
@@ -294,8 +297,9 @@ attn_status_t attn_na3d_fwd(const void *q, const void *k, const void *v, void *o
     st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (dtype == ATTN_BF16 && tc_na3d_supported(B, heads, T, Hg, W, D, kernel))
-        return tc_na3d(c, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
+    if (half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel) &&
+        (dtype == ATTN_BF16 || tc_na3d_f16_scale_ok(sc)))
+        return tc_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
     return simt_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
 }
 

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "libattn.h"
@@ -38,6 +39,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// f16 <-> f32 (RNE for the narrowing).
+__device__ __forceinline__ float f16_lo(uint32_t packed) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(packed & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t packed) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(packed >> 16)));
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);               // .x = lo (low 16 bits), .y = hi
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The two 16-bit storage types behind one interface: H16<true> is f16,
+// H16<false> bf16.
+template <bool F16> struct H16;
+template <> struct H16<false> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ float lo(uint32_t w) { return bf16_lo(w); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return bf16_hi(w); }
+    static __device__ __forceinline__ uint32_t pack(float a, float b) { return pack_bf16x2(a, b); }
+    static __device__ __forceinline__ T from(float x) { return __float2bfloat16_rn(x); }
+    static constexpr uint16_t kOne = 0x3F80;             // 1.0
+};
+template <> struct H16<true> {
+    using T = __half;
+    static __device__ __forceinline__ float lo(uint32_t w) { return f16_lo(w); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return f16_hi(w); }
+    static __device__ __forceinline__ uint32_t pack(float a, float b) { return pack_f16x2(a, b); }
+    static __device__ __forceinline__ T from(float x) { return __float2half_rn(x); }
+    static constexpr uint16_t kOne = 0x3C00;             // 1.0
+};
+
 template <typename T> struct Elem;
 template <> struct Elem<float> {
     static __device__ __forceinline__ float load(const float *p) { return *p; }
@@ -46,6 +79,10 @@ template <> struct Elem<float> {
 template <> struct Elem<__nv_bfloat16> {
     static __device__ __forceinline__ float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
     static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+};
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float load(const __half *p) { return __half2float(*p); }
+    static __device__ __forceinline__ void store(__half *p, float x) { *p = __float2half_rn(x); }
 };
 
 // NATTEN boundary window along one axis (candle PR #11, "kernel exceeds grid

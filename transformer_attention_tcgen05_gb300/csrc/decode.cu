@@ -76,9 +76,9 @@ struct DecCfg {
 };
 
 struct DecParams {
-    const __nv_bfloat16 *q;
+    const void *q;           // [B][Hq][D], bf16 or f16 like the cache
     const int32_t *seq_len;
-    __nv_bfloat16 *o;
+    void *o;
     int Hq, Hkv, Lmax, G;
     int splits, split_rows, ws_splits;
     float qscale;
@@ -88,17 +88,20 @@ struct DecParams {
     unsigned *err;
 };
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&x)[8]) {
-    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
-    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
-    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+// eight 16-bit values (bf16, or f16 if F16) -> fp32
+template <bool F16>
+__device__ __forceinline__ void x8_to_f32(const uint4 &u, float (&x)[8]) {
+    using H = H16<F16>;
+    x[0] = H::lo(u.x); x[1] = H::hi(u.x);
+    x[2] = H::lo(u.y); x[3] = H::hi(u.y);
+    x[4] = H::lo(u.z); x[5] = H::hi(u.z);
+    x[6] = H::lo(u.w); x[7] = H::hi(u.w);
 }
 
 // CL: the splits of one (batch, kv-head) form one thread-block cluster and
 // merge their partials through distributed shared memory (no workspace, no
 // atomics); otherwise the last CTA to arrive merges them from the workspace.
-template <int D, int GP, bool CL>
+template <int D, int GP, bool CL, bool F16>
 __global__ void __launch_bounds__(DecCfg<D, GP>::NT)
 decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
               const DecParams p) {
@@ -142,8 +145,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
             float x[8];
             if (h < p.G) {
                 const uint4 u = *reinterpret_cast<const uint4 *>(
-                    p.q + (size_t(b) * p.Hq + kvh * p.G + h) * D + d);
-                bf16x8_to_f32(u, x);
+                    static_cast<const typename H16<F16>::T *>(p.q) +
+                    (size_t(b) * p.Hq + kvh * p.G + h) * D + d);
+                x8_to_f32<F16>(u, x);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x[i] = 0.f;
@@ -226,7 +230,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
                     const uint4 u = *reinterpret_cast<const uint4 *>(
                         Kst + pn * C::PANEL + r * 128 + ((cc ^ (r & 7)) << 4));
                     float kx[8];
-                    bf16x8_to_f32(u, kx);
+                    x8_to_f32<F16>(u, kx);
 #pragma unroll
                     for (int h = 0; h < GP; ++h) {
                         const float4 qa = *reinterpret_cast<const float4 *>(q_s + h * D + c * 8);
@@ -280,7 +284,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
                     const uint4 u = *reinterpret_cast<const uint4 *>(
                         Vst + vpanel * C::PANEL + r * 128 + ((vchunk ^ (r & 7)) << 4));
                     float vx[8];
-                    bf16x8_to_f32(u, vx);
+                    x8_to_f32<F16>(u, vx);
                     float pr[GP];
 #pragma unroll
                     for (int h = 0; h < GP; ++h) pr[h] = p_s[r * GP + h];
@@ -382,7 +386,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
                     O += os[r] * w;
                     Lsum += ls[r] * w;
                 }
-                p.o[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] = __float2bfloat16_rn(O / Lsum);
+                static_cast<typename H16<F16>::T *>(p.o)[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] =
+                    H16<F16>::from(O / Lsum);
             }
         ptx::cluster_sync();
         return;
@@ -461,7 +466,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
             for (int i = 0; i < 4; ++i) O += v[i] * wgt[((s + i) * GP + h) * 2 + 1];
         }
         for (; s < p.splits; ++s) O += __ldcg(po + (s * GP + h) * D + d) * wgt[(s * GP + h) * 2 + 1];
-        p.o[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] = __float2bfloat16_rn(O);
+        static_cast<typename H16<F16>::T *>(p.o)[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] =
+            H16<F16>::from(O);
     }
     if (threadIdx.x == 0) p.tickets[unit] = 0u;   // ready for the next call
 }
@@ -502,24 +508,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_dec() {
 }
 
 // 3D map over the cache [units][Lmax][D], box {64, 32, 1}, 128-byte swizzle.
-bool cache_tmap(CUtensorMap *m, const void *base, int units, int Lmax, int D) {
+bool cache_tmap(CUtensorMap *m, const void *base, int units, int Lmax, int D, bool f16) {
     auto fn = encode_fn_dec();
     if (!fn) return false;
     const cuuint64_t gdim[3] = {cuuint64_t(D), cuuint64_t(Lmax), cuuint64_t(units)};
     const cuuint64_t gstride[2] = {cuuint64_t(D) * 2, cuuint64_t(Lmax) * D * 2};
     const cuuint32_t box[3] = {64, kRowsPerChunk, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), gdim, gstride, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int GP>
+template <int D, int GP, bool F16>
 attn_status_t launch(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv, DecParams p,
                      int B) {
     using C = DecCfg<D, GP>;
     static int done_mask = 0;
-    auto kern = decode_kernel<D, GP, false>;
+    auto kern = decode_kernel<D, GP, false, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     kern<<<dim3(p.splits, p.Hkv, B), C::NT, C::SMEM, c.stream>>>(tk, tv, p);
@@ -552,14 +559,14 @@ cudaLaunchConfig_t cluster_config(const Ctx &c, int splits, int Hkv, int B,
 // `units` (batch, kv-head) pairs are resident at once (one wave: no cluster
 // waits for another to finish), or 0.  The occupancy answer depends only on
 // the device and the kernel, so it is looked up once per size.
-template <int D, int GP>
+template <int D, int GP, bool F16>
 int cluster_splits(const Ctx &c, int units, int target) {
     using C = DecCfg<D, GP>;
     static std::mutex mu;
     static int active[kMaxDevices][kMaxClusterSplits + 1];   // 0 = not looked up, -1 = none
     static int done_mask = 0;
     if (c.device < 0 || c.device >= kMaxDevices) return 0;
-    auto kern = decode_kernel<D, GP, true>;
+    auto kern = decode_kernel<D, GP, true, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return 0;
     std::lock_guard<std::mutex> lock(mu);
@@ -580,11 +587,11 @@ int cluster_splits(const Ctx &c, int units, int target) {
     return 0;
 }
 
-template <int D, int GP>
+template <int D, int GP, bool F16>
 attn_status_t launch_cluster(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
                              DecParams p, int B) {
     static int done_mask = 0;
-    auto kern = decode_kernel<D, GP, true>;
+    auto kern = decode_kernel<D, GP, true, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), DecCfg<D, GP>::SMEM, c.device,
                           &done_mask))
         return ATTN_ERR_RESOURCE;
@@ -599,16 +606,37 @@ attn_status_t launch_cluster(const Ctx &c, const CUtensorMap &tk, const CUtensor
 
 // Cluster merge when every unit's cluster fits one wave; else the workspace
 // (atomic ticket) merge.
-template <int D, int GP>
+template <int D, int GP, bool F16>
 attn_status_t launch_best(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
                           DecParams p, int B, int Lmax) {
-    const int cs = cluster_splits<D, GP>(c, B * p.Hkv, p.splits);
+    const int cs = cluster_splits<D, GP, F16>(c, B * p.Hkv, p.splits);
     if (cs >= 2) {
         p.splits = cs;
         p.split_rows = cdiv(cdiv(Lmax, cs), kRowsPerChunk) * kRowsPerChunk;
-        return launch_cluster<D, GP>(c, tk, tv, p, B);
+        return launch_cluster<D, GP, F16>(c, tk, tv, p, B);
     }
-    return launch<D, GP>(c, tk, tv, p, B);
+    return launch<D, GP, F16>(c, tk, tv, p, B);
+}
+
+// (D, group padding, dtype) dispatch; `best` picks the cluster or the
+// workspace merge, otherwise the workspace merge.
+template <bool F16>
+attn_status_t dispatch(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const DecParams &p, int B, int Lmax, int D, int GP, bool best) {
+    if (D == 128) {
+        switch (GP) {
+            case 1: return best ? launch_best<128, 1, F16>(c, tk, tv, p, B, Lmax) : launch<128, 1, F16>(c, tk, tv, p, B);
+            case 2: return best ? launch_best<128, 2, F16>(c, tk, tv, p, B, Lmax) : launch<128, 2, F16>(c, tk, tv, p, B);
+            case 4: return best ? launch_best<128, 4, F16>(c, tk, tv, p, B, Lmax) : launch<128, 4, F16>(c, tk, tv, p, B);
+            default: return best ? launch_best<128, 8, F16>(c, tk, tv, p, B, Lmax) : launch<128, 8, F16>(c, tk, tv, p, B);
+        }
+    }
+    switch (GP) {
+        case 1: return best ? launch_best<64, 1, F16>(c, tk, tv, p, B, Lmax) : launch<64, 1, F16>(c, tk, tv, p, B);
+        case 2: return best ? launch_best<64, 2, F16>(c, tk, tv, p, B, Lmax) : launch<64, 2, F16>(c, tk, tv, p, B);
+        case 4: return best ? launch_best<64, 4, F16>(c, tk, tv, p, B, Lmax) : launch<64, 4, F16>(c, tk, tv, p, B);
+        default: return best ? launch_best<64, 8, F16>(c, tk, tv, p, B, Lmax) : launch<64, 8, F16>(c, tk, tv, p, B);
+    }
 }
 
 int gp_for(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
@@ -628,21 +656,22 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D) {
     return (bytes + 255) & ~size_t(255);
 }
 
-attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void *v,
-                         const int32_t *seq_len, void *o, int B, int Hq, int Hkv, int Lmax,
-                         int D, float scale, void *ws, size_t ws_bytes) {
+attn_status_t decode_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                         const void *v, const int32_t *seq_len, void *o, int B, int Hq, int Hkv,
+                         int Lmax, int D, float scale, void *ws, size_t ws_bytes) {
+    const bool f16 = dt == ATTN_F16;
     const int G = Hq / Hkv;
     const int GP = gp_for(G);
     const size_t need = decode_workspace_bytes(B, Hq, Hkv, Lmax, D);
     if (ws_bytes < need) return ATTN_ERR_RESOURCE;
     if (B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
     CUtensorMap tk, tv;
-    if (!cache_tmap(&tk, k, B * Hkv, Lmax, D) || !cache_tmap(&tv, v, B * Hkv, Lmax, D))
+    if (!cache_tmap(&tk, k, B * Hkv, Lmax, D, f16) || !cache_tmap(&tv, v, B * Hkv, Lmax, D, f16))
         return ATTN_ERR_CUDA;
     DecParams p{};
-    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.q = q;
     p.seq_len = seq_len;
-    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.o = o;
     p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
     p.ws_splits = max_splits_for(Lmax);
     p.splits = splits_for(B, Hkv, Lmax, c.sm_count);
@@ -657,20 +686,8 @@ attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void 
     off = (off + units * p.ws_splits * GP * 2 * sizeof(float) + 255) & ~size_t(255);
     p.tickets = reinterpret_cast<unsigned *>(w + off);
     p.err = c.err;
-    if (D == 128) {
-        switch (GP) {
-            case 1: return launch_best<128, 1>(c, tk, tv, p, B, Lmax);
-            case 2: return launch_best<128, 2>(c, tk, tv, p, B, Lmax);
-            case 4: return launch_best<128, 4>(c, tk, tv, p, B, Lmax);
-            default: return launch_best<128, 8>(c, tk, tv, p, B, Lmax);
-        }
-    }
-    switch (GP) {
-        case 1: return launch_best<64, 1>(c, tk, tv, p, B, Lmax);
-        case 2: return launch_best<64, 2>(c, tk, tv, p, B, Lmax);
-        case 4: return launch_best<64, 4>(c, tk, tv, p, B, Lmax);
-        default: return launch_best<64, 8>(c, tk, tv, p, B, Lmax);
-    }
+    return f16 ? dispatch<true>(c, tk, tv, p, B, Lmax, D, GP, true)
+               : dispatch<false>(c, tk, tv, p, B, Lmax, D, GP, true);
 }
 
 // ------------------------------------------------ allocation-free variant
@@ -732,9 +749,10 @@ extern "C" attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_ca
     if (!q || !k_cache || !v_cache || !seq_len || !o) return ATTN_ERR_INVALID_ARG;
     if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(o)) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_INVALID_ARG;
     if (D != 32 && D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_BF16 || D == 32 || Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_F32 || D == 32 || Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+    const bool f16 = dtype == ATTN_F16;
     if ((long long)Lmax * D >= (1ll << 31) || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
     if (o == q || o == k_cache || o == v_cache) return ATTN_ERR_INVALID_ARG;
     Ctx c;
@@ -756,11 +774,12 @@ extern "C" attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_ca
     if (need > kStaticScratchBytes) return ATTN_ERR_RESOURCE;   // problem too large for the array
 
     CUtensorMap tk, tv;
-    if (!cache_tmap(&tk, k_cache, B * Hkv, Lmax, D) || !cache_tmap(&tv, v_cache, B * Hkv, Lmax, D))
+    if (!cache_tmap(&tk, k_cache, B * Hkv, Lmax, D, f16) ||
+        !cache_tmap(&tv, v_cache, B * Hkv, Lmax, D, f16))
         return ATTN_ERR_CUDA;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.q = q;
     p.seq_len = seq_len;
-    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.o = o;
     p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
     p.split_rows = cdiv(cdiv(Lmax, p.splits), kRowsPerChunk) * kRowsPerChunk;
     p.qscale = (scale > 0.f && isfinite(scale) ? scale : 1.0f / sqrtf(float(D))) * kLog2e;
@@ -773,18 +792,6 @@ extern "C" attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_ca
         cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
-    if (D == 128) {
-        switch (GP) {
-            case 1: return launch<128, 1>(c, tk, tv, p, B);
-            case 2: return launch<128, 2>(c, tk, tv, p, B);
-            case 4: return launch<128, 4>(c, tk, tv, p, B);
-            default: return launch<128, 8>(c, tk, tv, p, B);
-        }
-    }
-    switch (GP) {
-        case 1: return launch<64, 1>(c, tk, tv, p, B);
-        case 2: return launch<64, 2>(c, tk, tv, p, B);
-        case 4: return launch<64, 4>(c, tk, tv, p, B);
-        default: return launch<64, 8>(c, tk, tv, p, B);
-    }
+    return f16 ? dispatch<true>(c, tk, tv, p, B, Lmax, D, GP, false)
+               : dispatch<false>(c, tk, tv, p, B, Lmax, D, GP, false);
 }

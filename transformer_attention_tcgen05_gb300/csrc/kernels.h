@@ -58,25 +58,29 @@ attn_status_t kv_append(const Ctx &c, attn_dtype_t dt, void *kc, void *vc, const
                         const void *vn, int32_t *seq_len, int B, int Hkv, int Lmax, int D,
                         int advance);
 
-// Split-KV GQA decode (bf16).
+// Split-KV GQA decode (bf16 or f16 cache).
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
-attn_status_t decode_gqa(const Ctx &c, const void *q, const void *k, const void *v,
-                         const int32_t *seq_len, void *o, int B, int Hq, int Hkv, int Lmax,
-                         int D, float scale, void *ws, size_t ws_bytes);
+attn_status_t decode_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                         const void *v, const int32_t *seq_len, void *o, int B, int Hq, int Hkv,
+                         int Lmax, int D, float scale, void *ws, size_t ws_bytes);
 
-// tcgen05 (tensor-core) flash attention, bf16: full and neighborhood.
-attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v, void *o,
-                      int B, int H, int Nq, int Nkv, int D, float scale);
+// tcgen05 (tensor-core) flash attention, bf16 or f16: full and neighborhood.
+attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
+                      void *o, int B, int H, int Nq, int Nkv, int D, float scale);
 bool tc_full_supported(int B, int H, int Nq, int Nkv, int D);
-attn_status_t tc_causal_gqa(const Ctx &c, const void *q, const void *k, const void *v, void *o,
-                            int B, int Hq, int Hkv, int N, int D, float scale);
+attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                            const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
+                            float scale);
 attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                               const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
                               float scale);
-attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v, void *o,
-                      int B, int H, int T, int Hg, int W, int D, const int kernel[3],
+attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
+                      void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
                       float scale);
 bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]);
+// The f16 neighborhood kernel needs its window penalty (a power of two with
+// penalty * scale * log2(e) >= 300) to be representable in f16.
+bool tc_na3d_f16_scale_ok(float scale);
 // One 128 x 128 tile through both tcgen05 MMA forms (testing).
 attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,
                           const void *P, float *S, float *O, int D);

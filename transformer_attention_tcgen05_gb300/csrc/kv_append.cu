@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(128) kv_append_kernel(T *kc, T *vc, const T *k
 
 }  // namespace
 
+// f16 rows are 2-byte elements like bf16: the same 16-byte copies serve both.
 attn_status_t kv_append(const Ctx &c, attn_dtype_t dt, void *kc, void *vc, const void *kn,
                         const void *vn, int32_t *seq_len, int B, int Hkv, int Lmax, int D,
                         int advance) {

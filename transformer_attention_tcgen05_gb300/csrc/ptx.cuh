@@ -214,7 +214,7 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
         : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 or f16 in, fp32 accumulate).
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -225,7 +225,7 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16; A is M x K bf16 packed two per column.
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16; A is M x K 16-bit packed two per column.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -236,12 +236,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
+// Instruction descriptor of kind::f16 with bf16 (or f16) A/B and fp32 D.
+//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16, 1 = bf16), 10-12 B format,
 //   15 A major (0 = K), 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, bool b_mn_major, bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+    return idesc_16_f32(M, N, b_mn_major, false);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1.

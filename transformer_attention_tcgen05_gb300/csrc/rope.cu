@@ -35,19 +35,22 @@ struct RopeParams {
 };
 
 template <typename T> struct Vec8;
-template <> struct Vec8<__nv_bfloat16> {
+// eight 16-bit values (bf16 or f16) in one 16-byte vector
+template <bool F16> struct Vec8H {
     uint4 u;
     __device__ __forceinline__ void load(const void *p) { u = *reinterpret_cast<const uint4 *>(p); }
     __device__ __forceinline__ void store(void *p) const { *reinterpret_cast<uint4 *>(p) = u; }
     __device__ __forceinline__ float get(int i) const {
         const uint32_t w = i < 2 ? u.x : i < 4 ? u.y : i < 6 ? u.z : u.w;
-        return (i & 1) ? bf16_hi(w) : bf16_lo(w);
+        return (i & 1) ? H16<F16>::hi(w) : H16<F16>::lo(w);
     }
     __device__ __forceinline__ void set2(int pr, float a, float b) {
-        const uint32_t w = pack_bf16x2(a, b);
+        const uint32_t w = H16<F16>::pack(a, b);
         if (pr == 0) u.x = w; else if (pr == 1) u.y = w; else if (pr == 2) u.z = w; else u.w = w;
     }
 };
+template <> struct Vec8<__nv_bfloat16> : Vec8H<false> {};
+template <> struct Vec8<__half> : Vec8H<true> {};
 template <> struct Vec8<float> {
     float4 a, b;
     __device__ __forceinline__ void load(const void *p) {
@@ -127,6 +130,8 @@ attn_status_t rope_rotate_qk(const Ctx &c, attn_dtype_t dt, const void *q, const
     const dim3 grid(unsigned(cols), unsigned(cdiv(BH, hpc)));
     if (dt == ATTN_F32)
         rope_kernel<float><<<grid, 256, 0, c.stream>>>(p, hpc);
+    else if (dt == ATTN_F16)
+        rope_kernel<__half><<<grid, 256, 0, c.stream>>>(p, hpc);
     else
         rope_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(p, hpc);
     return launch_status(kFamRope);

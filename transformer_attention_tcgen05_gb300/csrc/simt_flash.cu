@@ -57,6 +57,10 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bf
     const uint2 u = *reinterpret_cast<const uint2 *>(p);
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
 }
+template <> __device__ __forceinline__ float4 load4<__half>(const __half *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(f16_lo(u.x), f16_hi(u.x), f16_lo(u.y), f16_hi(u.y));
+}
 
 template <typename T, int D, bool NA>
 __global__ void __launch_bounds__(SimtLayout<D>::NT)
@@ -282,6 +286,10 @@ attn_status_t dispatch(const Ctx &c, attn_dtype_t dt, int D, const SimtParams &p
         if (D == 32) return launch<float, 32, NA>(c, p, tiles, BH);
         if (D == 64) return launch<float, 64, NA>(c, p, tiles, BH);
         if (D == 128) return launch<float, 128, NA>(c, p, tiles, BH);
+    } else if (dt == ATTN_F16) {
+        if (D == 32) return launch<__half, 32, NA>(c, p, tiles, BH);
+        if (D == 64) return launch<__half, 64, NA>(c, p, tiles, BH);
+        if (D == 128) return launch<__half, 128, NA>(c, p, tiles, BH);
     } else {
         if (D == 32) return launch<__nv_bfloat16, 32, NA>(c, p, tiles, BH);
         if (D == 64) return launch<__nv_bfloat16, 64, NA>(c, p, tiles, BH);

@@ -118,7 +118,7 @@ struct TcCfg {
 struct TcParams {
     int Nq, Nkv;             // full attention: query / key tokens per (batch, head)
     float c_log2;            // scale * log2(e)
-    __nv_bfloat16 *o;
+    void *o;                 // bf16 or f16, like the inputs
     unsigned *err;
     // neighborhood attention (grid T x Hg x W, row-major)
     int T, Hg, W;
@@ -203,8 +203,9 @@ __device__ __forceinline__ void na_key_box(const NaTile &g, int KH, int j, int &
 
 // KHC > 0 fixes the neighborhood key sub-box height (keys per tile = 16 KHC)
 // at compile time, so the softmax's column loops and masks unroll without
-// run-time tests; KHC = 0 takes it from the parameters.
-template <int D, bool NA, bool CAUSAL, int KHC>
+// run-time tests; KHC = 0 takes it from the parameters.  F16: inputs, P and
+// output in f16 instead of bf16 (same layouts; the MMA operand format flips).
+template <int D, bool NA, bool CAUSAL, int KHC, bool F16>
 __global__ void __launch_bounds__(TcCfg<D, NA>::NT, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams p) {
@@ -291,7 +292,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 #pragma unroll
                 for (int a = 0; a < 2; ++a) {
                     const int c = ch[a] - half * 8;
-                    if (c >= 0 && c < 8) w[c >> 1] |= 0x3F80u << ((c & 1) * 16);   // bf16 1.0
+                    if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
                 }
             }
             *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW + ptx::sw32_offset(r, half)) =
@@ -300,7 +301,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         // key-side penalty tiles: for key (h, w) of the sub-box of h chunk hc and
         // w chunk wc, channel dh holds -penalty if h lies outside the h window of
         // query offset dh, channel bh + dw likewise for w
-        const uint32_t neg = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(-p.penalty)));
+        const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
+        const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
 #pragma unroll
         for (int u = 0; u < C::STREAMS; ++u) {
             if (n_t[u] == 0) continue;
@@ -416,8 +418,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             }
         } else if (warp == C::W_MMA && lane == 0) {
             // ============================================= MMA issuer
-            const uint32_t id_qk = ptx::idesc_bf16_f32(kBM, BNt, false);
-            const uint32_t id_pv = ptx::idesc_bf16_f32(kBM, D, true);
+            const uint32_t id_qk = ptx::idesc_16_f32(kBM, BNt, false, F16);
+            const uint32_t id_pv = ptx::idesc_16_f32(kBM, D, true, F16);
             // Matrix descriptors are built once: a k-step, a stage or a tile only
             // moves the start-address field (bits 0-13, byte address >> 4, no
             // carry out of it below 256 KB), so each MMA costs one add here
@@ -729,7 +731,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                         ptx::fadd2(acc[(2 * e) & 7], acc[(2 * e + 1) & 7], acc[(2 * e) & 7],
                                    acc[(2 * e + 1) & 7], p0, p1);
-                        pk[e] = pack_bf16x2(p0, p1);
+                        pk[e] = H16<F16>::pack(p0, p1);
                     }
                 }
                 ptx::tmem_st16(p_addr + c * 16, pk);
@@ -746,14 +748,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                        ptx::mbar_wait_or_abort(&bars->o_done[t], (nt - 1) & 1, p.err, abort))) {
             ptx::tc_fence_after();
             const float inv = 1.f / l;
-            __nv_bfloat16 *orow = nullptr;
+            typename H16<F16>::T *orow = nullptr;
             if (qvalid) {
                 size_t idx;
                 if constexpr (NA)
                     idx = (size_t(bh) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw;
                 else
                     idx = size_t(bh) * p.Nq + q0 + t * kBM + row;
-                orow = p.o + idx * D;
+                orow = static_cast<typename H16<F16>::T *>(p.o) + idx * D;
             }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -765,7 +767,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        wp[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv,
+                        wp[e] = H16<F16>::pack(__uint_as_float(ov[2 * e]) * inv,
                                             __uint_as_float(ov[2 * e + 1]) * inv);
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
@@ -924,9 +926,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims/box innermost first (dims[0] = D).
+// 16-bit (bf16 or f16) tensor map with 128-byte swizzle; dims/box innermost
+// first (dims[0] = D).
 bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-               const uint32_t *box) {
+               const uint32_t *box, bool f16 = false) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[5], gstride[4];
@@ -939,18 +942,19 @@ bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
         if (i > 0) gstride[i - 1] = stride;
         stride *= dims[i];
     }
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gdim, gstride,
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+              const_cast<void *>(base), gdim, gstride,
               bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool NA, bool CAUSAL = false, int KHC = 0>
+template <int D, bool NA, bool CAUSAL = false, int KHC = 0, bool F16 = false>
 attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
     using C = TcCfg<D, NA>;
     static int done_mask = 0;
     static int regs = -1;
-    auto kern = tc_attn_kernel<D, NA, CAUSAL, KHC>;
+    auto kern = tc_attn_kernel<D, NA, CAUSAL, KHC, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     // The warpgroups re-split the launch's register file with setmaxnreg; the
@@ -1050,45 +1054,54 @@ bool tc_full_supported(int B, int H, int Nq, int Nkv, int D) {
     return (D == 64 || D == 128) && B * H <= 65535 && Nq >= 1 && Nkv >= 1 && encode_fn() != nullptr;
 }
 
-attn_status_t tc_full(const Ctx &c, const void *q, const void *k, const void *v, void *o, int B,
-                      int H, int Nq, int Nkv, int D, float scale) {
+attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
+                      void *o, int B, int H, int Nq, int Nkv, int D, float scale) {
+    const bool f16 = dt == ATTN_F16;
     CUtensorMap tq, tk, tv;
     const uint64_t dq[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
     const uint64_t dk[3] = {uint64_t(D), uint64_t(Nkv), uint64_t(B) * H};
     const uint32_t box[3] = {64, kBM, 1};
-    if (!make_tmap(&tq, q, 3, dq, box) || !make_tmap(&tk, k, 3, dk, box) ||
-        !make_tmap(&tv, v, 3, dk, box))
+    if (!make_tmap(&tq, q, 3, dq, box, f16) || !make_tmap(&tk, k, 3, dk, box, f16) ||
+        !make_tmap(&tv, v, 3, dk, box, f16))
         return ATTN_ERR_CUDA;
     TcParams p{};
     p.Nq = Nq;
     p.Nkv = Nkv;
     p.c_log2 = scale * kLog2e;
-    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.o = o;
     p.err = c.err;
     const dim3 grid(cdiv(Nq, kNQ * kBM), B * H);
+    if (f16)
+        return D == 128 ? launch_tc<128, false, false, 0, true>(c, tq, tk, tv, p, grid)
+                        : launch_tc<64, false, false, 0, true>(c, tq, tk, tv, p, grid);
     return D == 128 ? launch_tc<128, false>(c, tq, tk, tv, p, grid)
                     : launch_tc<64, false>(c, tq, tk, tv, p, grid);
 }
 
-attn_status_t tc_causal_gqa(const Ctx &c, const void *q, const void *k, const void *v, void *o,
-                            int B, int Hq, int Hkv, int N, int D, float scale) {
+attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
+                            const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
+                            float scale) {
+    const bool f16 = dt == ATTN_F16;
     CUtensorMap tq, tk, tv;
     const uint64_t dq[3] = {uint64_t(D), uint64_t(N), uint64_t(B) * Hq};
     const uint64_t dk[3] = {uint64_t(D), uint64_t(N), uint64_t(B) * Hkv};
     const uint32_t box[3] = {64, kBM, 1};
-    if (!make_tmap(&tq, q, 3, dq, box) || !make_tmap(&tk, k, 3, dk, box) ||
-        !make_tmap(&tv, v, 3, dk, box))
+    if (!make_tmap(&tq, q, 3, dq, box, f16) || !make_tmap(&tk, k, 3, dk, box, f16) ||
+        !make_tmap(&tv, v, 3, dk, box, f16))
         return ATTN_ERR_CUDA;
     TcParams p{};
     p.Nq = N;
     p.Nkv = N;
     p.c_log2 = scale * kLog2e;
-    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.o = o;
     p.err = c.err;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
     const dim3 grid(cdiv(N, kNQ * kBM), B * Hq);
+    if (f16)
+        return D == 128 ? launch_tc<128, false, true, 0, true>(c, tq, tk, tv, p, grid)
+                        : launch_tc<64, false, true, 0, true>(c, tq, tk, tv, p, grid);
     return D == 128 ? launch_tc<128, false, true>(c, tq, tk, tv, p, grid)
                     : launch_tc<64, false, true>(c, tq, tk, tv, p, grid);
 }
@@ -1098,8 +1111,14 @@ bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kern
            cached_plan(T, Hg, W, kernel).ok;
 }
 
-attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v, void *o, int B,
-                      int H, int T, int Hg, int W, int D, const int kernel[3], float scale) {
+bool tc_na3d_f16_scale_ok(float scale) {
+    return exp2f(fminf(100.f, fmaxf(0.f, ceilf(log2f(300.f / (scale * kLog2e)))))) <= 32768.f;
+}
+
+attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
+                      void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
+                      float scale) {
+    const bool f16 = dt == ATTN_F16;
     TcParams p{};
     const NaPlan pl = cached_plan(T, Hg, W, kernel);
     if (!pl.ok) return ATTN_ERR_UNSUPPORTED;
@@ -1108,14 +1127,16 @@ attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v,
     const uint64_t dims[5] = {uint64_t(D), uint64_t(W), uint64_t(Hg), uint64_t(T), uint64_t(B) * H};
     const uint32_t qbox[5] = {64, uint32_t(p.bw), uint32_t(p.bh), uint32_t(p.bt), 1};
     const uint32_t kbox[5] = {64, uint32_t(kKW), uint32_t(p.KH), 1, 1};
-    if (!make_tmap(&tq, q, 5, dims, qbox) || !make_tmap(&tk, k, 5, dims, kbox) ||
-        !make_tmap(&tv, v, 5, dims, kbox))
+    if (!make_tmap(&tq, q, 5, dims, qbox, f16) || !make_tmap(&tk, k, 5, dims, kbox, f16) ||
+        !make_tmap(&tv, v, 5, dims, kbox, f16))
         return ATTN_ERR_CUDA;
     p.c_log2 = scale * kLog2e;
-    // penalty per violated axis: a power of two (exact in bf16) with
-    // penalty * scale * log2(e) >= 300, so 2^(x - m) underflows to exactly 0
+    // penalty per violated axis: a power of two (exact in bf16; in f16 up to
+    // 2^15) with penalty * scale * log2(e) >= 300, so 2^(x - m) underflows to
+    // exactly 0
     p.penalty = exp2f(fminf(100.f, fmaxf(0.f, ceilf(log2f(300.f / p.c_log2)))));
-    p.o = static_cast<__nv_bfloat16 *>(o);
+    if (f16 && p.penalty > 32768.f) return ATTN_ERR_UNSUPPORTED;   // scale too small for f16
+    p.o = o;
     p.err = c.err;
     p.T = T; p.Hg = Hg; p.W = W;
     p.kt = kernel[0]; p.kh = kernel[1]; p.kw = kernel[2];
@@ -1124,7 +1145,8 @@ attn_status_t tc_na3d(const Ctx &c, const void *q, const void *k, const void *v,
     p.nbw = cdiv(W, p.bw);
     p.nbw2 = cdiv(p.nbw, 2);
     const dim3 grid(cdiv(T, p.bt) * p.nbh * p.nbw2, B * H);
-    // the planner's key sub-box heights (4..8) have compile-time kernels
+    // the planner's key sub-box heights (4..8) have compile-time kernels (bf16)
+    if (f16) return launch_tc<64, true, false, 0, true>(c, tq, tk, tv, p, grid);
     switch (p.KH) {
         case 4: return launch_tc<64, true, false, 4>(c, tq, tk, tv, p, grid);
         case 5: return launch_tc<64, true, false, 5>(c, tq, tk, tv, p, grid);

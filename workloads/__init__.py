@@ -53,12 +53,15 @@ def bf16_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def draw(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
-    """One N(0,1) tensor: float32 for 'f32', uint16 bf16 bits for 'bf16'."""
+    """One N(0,1) tensor: float32 for 'f32', uint16 bf16 bits for 'bf16',
+    float16 (round to nearest even of the float32 draw) for 'f16'."""
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if dtype == "f32":
         return x
     if dtype == "bf16":
         return bf16_round(x)
+    if dtype == "f16":
+        return x.astype(np.float16)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
@@ -84,7 +87,7 @@ class Workload:
     """One synthetic workload.  ``kind`` selects the entry point."""
     name: str
     kind: str                 # "full" | "na3d" | "decode" | "joint"
-    dtype: str                # "f32" | "bf16"
+    dtype: str                # "f32" | "bf16" | "f16"
     seed: int
     B: int = 1
     H: int = 1                # heads (query heads for decode)

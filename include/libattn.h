@@ -79,6 +79,32 @@ ATTN_API attn_status_t attn_full_fwd(const void *q, const void *k, const void *v
                             attn_dtype_t dtype, float scale, void *stream);
 
 /*
+ * Full attention on strided views: the operation of attn_full_fwd, with each
+ * of q, k, v and o addressed through its own element strides instead of the
+ * contiguous [B, H, N, D] layout, so that transposed [B, N, H, D] tensors,
+ * slices of a packed QKV projection or a column block of a wider output are
+ * used in place, with no copy.
+ *   x_strides[3] = element strides of (batch, head, row); D is contiguous
+ *   (stride 1).  Element (b, h, n, d) of x is x[b*s[0] + h*s[1] + n*s[2] + d].
+ *   Every stride is >= 1 and a multiple of 16 bytes (8 elements for bf16 and
+ *   f16, 4 for f32), as the tensor-memory-access unit requires; a stride
+ *   whose extent is 1 is ignored.  Base pointers are 16-byte aligned.
+ *   q, k and v are read only and may overlap one another; o must not
+ *   overlap them, and its (batch, head, row) rows must be disjoint (checked:
+ *   sorted by stride, each stride covers the extent below it).
+ *   Same sizes, dtypes, scale and status codes as attn_full_fwd.
+ * Passage: the unmasked attention of attn_full_fwd; the layout is an
+ * addressing choice with no counterpart in the pages.
+ */
+ATTN_API attn_status_t attn_full_fwd_strided(const void *q, const void *k, const void *v,
+                                            void *o, int B, int H, int Nq, int Nkv, int D,
+                                            const int64_t q_strides[3],
+                                            const int64_t k_strides[3],
+                                            const int64_t v_strides[3],
+                                            const int64_t o_strides[3],
+                                            attn_dtype_t dtype, float scale, void *stream);
+
+/*
  * Joint text+image attention with a multi-axis rotary embedding on Q and K.
  *   q, k, v, o [B, H, N, D]; N = text + image tokens in the caller's order.
  *   pos: DEVICE int32 [N, 4], the 4 position ids of each token.
@@ -190,6 +216,38 @@ ATTN_API attn_status_t attn_kv_append(void *k_cache, void *v_cache, const void *
                                       const void *v_new, int32_t *seq_len, int B, int Hkv,
                                       int Lmax, int D, attn_dtype_t dtype, int advance,
                                       void *stream);
+
+/*
+ * Ring KV cache: the pair attn_kv_append_ring / attn_decode_gqa_ring keeps the
+ * most recent Lmax tokens of a sequence in a cache of Lmax rows, so a decode
+ * loop captured once as a CUDA graph runs past the cache capacity instead of
+ * stopping at it (a sliding attention window of Lmax tokens).
+ *   seq_len[b] counts every token appended to sequence b so far (it may
+ *   exceed Lmax); token t lives in row t % Lmax until token t + Lmax
+ *   overwrites it.
+ *   attn_kv_append_ring: as attn_kv_append, writing row seq_len[b] % Lmax;
+ *   seq_len[b] must be >= 0 and below INT32_MAX, else nothing is written and
+ *   ATTN_ERR_DEVICE_CHECK is set.
+ *   attn_decode_gqa_ring: as attn_decode_gqa, attending to the
+ *   min(seq_len[b], Lmax) rows that hold tokens, i.e. to tokens
+ *   [seq_len[b] - Lmax, seq_len[b]) once the ring has wrapped; seq_len[b] >= 1
+ *   with no upper bound.  The row order does not change the result: the
+ *   softmax-weighted sum runs over a set of keys, whose positions are already
+ *   in their rotated K rows.  Same workspace contract as attn_decode_gqa.
+ * Passage: fak "GPU - the in-kernel forward pass", section 3b (the device KV
+ * of fixed capacity, with a dynamic / ring device KV named as the follow-up).
+ * With Lmax a call argument, a larger capacity is a new cache and a new
+ * capture; the ring is what lets one capture run indefinitely.
+ */
+ATTN_API attn_status_t attn_kv_append_ring(void *k_cache, void *v_cache, const void *k_new,
+                                           const void *v_new, int32_t *seq_len, int B, int Hkv,
+                                           int Lmax, int D, attn_dtype_t dtype, int advance,
+                                           void *stream);
+ATTN_API attn_status_t attn_decode_gqa_ring(const void *q, const void *k_cache,
+                                            const void *v_cache, const int32_t *seq_len,
+                                            void *o, int B, int Hq, int Hkv, int Lmax, int D,
+                                            attn_dtype_t dtype, float scale, void *workspace,
+                                            size_t workspace_bytes, void *stream);
 
 /*
  * 3D neighborhood attention with NATTEN boundary windows.

@@ -15,7 +15,9 @@ Pins (checked by ``tests/test_oracle_*.py``, all on the CPU):
   * brute force with an independent window characterisation on tiny inputs;
   * torch's float64 CPU scaled_dot_product_attention (with a boolean mask);
   * invariants (rows sum to 1, constant V, Q = 0, k >= extent == full,
-    decode == full with Nq = 1, RoPE norm / identity / relative shift);
+    decode == full with Nq = 1, RoPE norm / identity / relative shift,
+    ring decode: a one-row ring returns the newest V, tokens older than the
+    window do not matter, a ring at least as long as the history is decode);
   * the pages' clamp cases and hand-computed window starts (tests/golden).
 """
 from __future__ import annotations
@@ -143,6 +145,31 @@ def decode_gqa(q, kc, vc, seq_len, scale=None, threads=0):
     o = np.empty_like(q)
     lib().oracle_decode_gqa(q, kc, vc, sl, o, B, Hq, Hkv, Lmax, D, _scale(scale, D), threads)
     return o
+
+
+def decode_ring(q, k_tokens, v_tokens, n_tokens, capacity, scale=None, threads=0):
+    """Decode over a ring KV cache of `capacity` rows, stated on the token
+    history: k_tokens / v_tokens [B, Hkv, T, D] hold every token appended to
+    each sequence in order, n_tokens [B] how many were appended (1 <= n <= T).
+    A ring of `capacity` rows keeps the most recent `capacity` of them, so
+    query b attends to tokens [max(0, n_b - capacity), n_b): a sliding window
+    (fak "GPU - the in-kernel forward pass", section 3b: a dynamic / ring
+    device KV as the follow-up to the fixed-capacity one).  The window is
+    gathered in time order into a cache and handed to the pinned decode."""
+    q, k_tokens, v_tokens = _c(q), _c(k_tokens), _c(v_tokens)
+    B, Hkv, T, D = k_tokens.shape
+    n = np.asarray(n_tokens, dtype=np.int64)
+    assert n.shape == (B,) and np.all((n >= 1) & (n <= T)) and capacity >= 1
+    L = int(min(capacity, n.max()))
+    kc = np.zeros((B, Hkv, L, D))
+    vc = np.zeros((B, Hkv, L, D))
+    lens = np.empty(B, dtype=np.int32)
+    for b in range(B):
+        lo = max(0, int(n[b]) - capacity)
+        lens[b] = int(n[b]) - lo
+        kc[b, :, :lens[b]] = k_tokens[b, :, lo:n[b]]
+        vc[b, :, :lens[b]] = v_tokens[b, :, lo:n[b]]
+    return decode_gqa(q, kc, vc, lens, scale=scale, threads=threads)
 
 
 def causal_gqa_fwd(q, k, v, scale=None, rows: Optional[Sequence[int]] = None, threads=0):

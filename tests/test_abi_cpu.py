@@ -80,6 +80,32 @@ def test_full_validation(L):
     assert _full(L, o=FAKE) == 1                         # output aliases an input
 
 
+def _strided(L, qs, os_, *, B=2, H=3, N=16, D=64, dt=1):
+    L.attn_full_fwd_strided.restype = ctypes.c_int
+    S = ctypes.c_int64 * 3
+    dense = S(H * N * D, N * D, D)
+    return L.attn_full_fwd_strided(FAKE, FAKE, FAKE, ctypes.c_void_p(0x20000), B, H, N, N, D,
+                                   S(*qs), dense, dense, S(*os_), dt, ctypes.c_float(0.0), None)
+
+
+def test_full_strided_validation(L):
+    """Only layouts that must be refused are passed: the pointers are fake."""
+    H, N, D = 3, 16, 64
+    dense = (H * N * D, N * D, D)
+    assert _strided(L, (H * N * D, N * D, D + 4), dense) == 1    # row stride 136 bytes in bf16
+    assert _strided(L, (H * N * D, 0, D), dense) == 1            # zero stride on an extent-3 axis
+    assert _strided(L, (-H * N * D, N * D, D), dense) == 1       # negative stride
+    assert _strided(L, dense, (H * N * D, N * D, D // 2)) == 1   # output rows overlap
+    assert _strided(L, dense, (H * N * D, D, D)) == 1            # two heads share output rows
+    assert _strided(L, dense, (N * D, N * D, D)) == 1            # batches share output heads
+    assert _strided(L, (H * N * D, N * D, 6), dense, dt=0) == 1  # fp32 row stride 24 bytes
+    L.attn_full_fwd_strided.restype = ctypes.c_int
+    S = ctypes.c_int64 * 3
+    assert L.attn_full_fwd_strided(FAKE, FAKE, FAKE, ctypes.c_void_p(0x20000), 1, 1, 8, 8, 64,
+                                   None, S(512, 512, 64), S(512, 512, 64), S(512, 512, 64), 1,
+                                   ctypes.c_float(0.0), None) == 1
+
+
 def test_na3d_validation(L):
     L.attn_na3d_fwd.restype = ctypes.c_int
     o = ctypes.c_void_p(0x20000)

@@ -70,6 +70,56 @@ def test_decode_ignores_cache_rows_past_seq_len():
         np.testing.assert_allclose(o[b], ref[:, 0], rtol=0, atol=1e-13)
 
 
+# Ring decode (a ring of `capacity` rows keeps the newest tokens; fak section
+# 3b names the dynamic / ring device KV as the follow-up to a fixed one).
+
+def _ring_case(seed, B=3, Hq=4, Hkv=2, T=40, D=8):
+    g = np.random.default_rng(seed)
+    return (g.standard_normal((B, Hq, D)), g.standard_normal((B, Hkv, T, D)),
+            g.standard_normal((B, Hkv, T, D)))
+
+
+def test_ring_decode_one_row_ring_returns_the_newest_value():
+    q, kt, vt = _ring_case(60)
+    n = [1, 23, 40]
+    o = oracle.decode_ring(q, kt, vt, n, capacity=1)
+    for b, nb in enumerate(n):
+        for h in range(4):
+            np.testing.assert_array_equal(o[b, h], vt[b, h // 2, nb - 1])
+
+
+def test_ring_decode_ignores_tokens_outside_the_window():
+    q, kt, vt = _ring_case(61)
+    n, cap = [5, 23, 40], 9
+    o = oracle.decode_ring(q, kt, vt, n, capacity=cap)
+    kt2, vt2 = kt.copy(), vt.copy()
+    for b, nb in enumerate(n):
+        kt2[b, :, :max(0, nb - cap)] = np.nan     # overwritten by the ring
+        vt2[b, :, :max(0, nb - cap)] = np.nan
+        kt2[b, :, nb:] = np.nan                   # not yet appended
+        vt2[b, :, nb:] = np.nan
+    np.testing.assert_array_equal(oracle.decode_ring(q, kt2, vt2, n, capacity=cap), o)
+
+
+def test_ring_decode_matches_brute_force_on_the_window():
+    q, kt, vt = _ring_case(62)
+    n, cap = [5, 23, 40], 9
+    o = oracle.decode_ring(q, kt, vt, n, capacity=cap)
+    for b, nb in enumerate(n):
+        lo = max(0, nb - cap)
+        kr = np.repeat(kt[b, :, lo:nb], 2, axis=0)    # query head h reads kv head h // 2
+        vr = np.repeat(vt[b, :, lo:nb], 2, axis=0)
+        ref, _ = dense_attention(q[b][:, None], kr, vr, 1 / math.sqrt(8))
+        np.testing.assert_allclose(o[b], ref[:, 0], rtol=0, atol=1e-13)
+
+
+def test_ring_at_least_as_long_as_the_history_is_plain_decode():
+    q, kt, vt = _ring_case(63)
+    n = [5, 23, 40]
+    np.testing.assert_array_equal(oracle.decode_ring(q, kt, vt, n, capacity=40),
+                                  oracle.decode_gqa(q, kt, vt, n))
+
+
 # ------------------------------------------------------------------ RoPE --
 
 def test_rope_golden_angles():

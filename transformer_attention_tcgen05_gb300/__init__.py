@@ -24,8 +24,8 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "AttnError", "lib", "full_fwd", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
-    "na3d_window_starts", "kv_append", "decode_workspace_bytes", "rope_joint_workspace_bytes",
+    "AttnError", "lib", "full_fwd", "full_fwd_strided", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
+    "na3d_window_starts", "kv_append", "kv_append_ring", "decode_gqa_ring", "decode_workspace_bytes", "rope_joint_workspace_bytes",
     "device_status", "launch_count", "version", "FAMILIES", "LIB_PATH",
 ]
 
@@ -71,7 +71,12 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(_i), _i, _f, _vp]
         L.attn_na3d_window_starts.argtypes = [_i, _i, _i, ctypes.POINTER(_i), _vp, _vp]
         L.attn_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
+        L.attn_kv_append_ring.argtypes = L.attn_kv_append.argtypes
+        L.attn_decode_gqa_ring.argtypes = L.attn_decode_gqa.argtypes
         L.attn_causal_gqa_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+        _st = ctypes.POINTER(ctypes.c_int64)
+        L.attn_full_fwd_strided.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                            _st, _st, _st, _st, _i, _f, _vp]
         L.attn_status_string.argtypes = [_i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_device_status.argtypes = [_vp]
@@ -80,7 +85,8 @@ def lib() -> ctypes.CDLL:
         L.attn_version.restype = ctypes.c_char_p
         for name in ("attn_full_fwd", "attn_rope_joint_fwd", "attn_decode_gqa", "attn_na3d_fwd",
                      "attn_na3d_window_starts", "attn_device_status", "attn_kv_append",
-                     "attn_causal_gqa_fwd"):
+                     "attn_causal_gqa_fwd", "attn_full_fwd_strided", "attn_kv_append_ring",
+                     "attn_decode_gqa_ring"):
             getattr(L, name).restype = _i
         _lib = L
     return _lib
@@ -101,14 +107,14 @@ def _dtype(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float16)")
 
 
-def _cuda(*ts: torch.Tensor):
+def _cuda(*ts: torch.Tensor, strided: bool = False):
     dev = ts[0].device
     for t in ts:
         if not t.is_cuda:
             raise ValueError("libattn tensors must be on a CUDA device")
         if t.device != dev:
             raise ValueError("all tensors must be on the same device")
-        if not t.is_contiguous():
+        if not strided and not t.is_contiguous():
             raise ValueError("libattn tensors must be contiguous")
     return dev
 
@@ -141,6 +147,34 @@ def full_fwd(q, k, v, o=None, scale=None):
         _check(lib().attn_full_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                    B, H, Nq, Nkv, D, _dtype(q), _scale(scale), _stream(dev)),
                "attn_full_fwd")
+    return o
+
+
+def _strides(t):
+    if t.stride(-1) != 1:
+        raise ValueError("the last (D) dimension must be contiguous")
+    return (ctypes.c_int64 * 3)(*t.stride()[:3])
+
+
+def full_fwd_strided(q, k, v, o=None, scale=None):
+    """Full attention on strided [B,H,N,D] views (D contiguous), read and
+    written in place: e.g. q.transpose(1, 2) of a [B,N,H,D] projection or
+    slices of a packed QKV tensor. o defaults to a new contiguous tensor."""
+    dev = _cuda(q, k, v, strided=True)
+    B, H, Nq, D = q.shape
+    Nkv = k.shape[2]
+    if k.shape != (B, H, Nkv, D) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k/v must be [B, H, Nkv, D] with q's dtype")
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if o is None else o
+    _cuda(q, o, strided=True)
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must be [B, H, Nq, D] with q's dtype")
+    with torch.cuda.device(dev):
+        _check(lib().attn_full_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           B, H, Nq, Nkv, D, _strides(q), _strides(k),
+                                           _strides(v), _strides(o), _dtype(q), _scale(scale),
+                                           _stream(dev)),
+               "attn_full_fwd_strided")
     return o
 
 
@@ -189,13 +223,14 @@ def decode_workspace_bytes(B, Hq, Hkv, Lmax, D) -> int:
     return int(lib().attn_decode_gqa_workspace_bytes(B, Hq, Hkv, Lmax, D))
 
 
-def decode_gqa(q, k_cache, v_cache, seq_len, o=None, scale=None, workspace=None):
+def decode_gqa(q, k_cache, v_cache, seq_len, o=None, scale=None, workspace=None, _ring=False):
     """GQA decode: q [B,Hq,D], caches [B,Hkv,Lmax,D], seq_len int32 [B] -> o [B,Hq,D].
 
     ``workspace`` (uint8, decode_workspace_bytes(...) bytes) must be zero-filled
     before its first use; calls leave it reusable.  If omitted a zeroed one is
     allocated for this call.
     """
+    entry = "attn_decode_gqa_ring" if _ring else "attn_decode_gqa"
     dev = _cuda(q, k_cache, v_cache, seq_len)
     B, Hq, D = q.shape
     _, Hkv, Lmax, _ = k_cache.shape
@@ -208,27 +243,40 @@ def decode_gqa(q, k_cache, v_cache, seq_len, o=None, scale=None, workspace=None)
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     _cuda(q, o, workspace)
     with torch.cuda.device(dev):
-        _check(lib().attn_decode_gqa(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        _check(getattr(lib(), entry)(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                      seq_len.data_ptr(), o.data_ptr(), B, Hq, Hkv, Lmax, D,
                                      _dtype(q), _scale(scale), workspace.data_ptr(),
                                      workspace.numel(), _stream(dev)),
-               "attn_decode_gqa")
+               entry)
     return o
 
 
-def kv_append(k_cache, v_cache, k_new, v_new, seq_len, advance=True):
+def decode_gqa_ring(q, k_cache, v_cache, seq_len, o=None, scale=None, workspace=None):
+    """GQA decode over a ring cache: seq_len[b] counts every token appended
+    (it may exceed Lmax); attends to the min(seq_len[b], Lmax) rows in use."""
+    return decode_gqa(q, k_cache, v_cache, seq_len, o, scale, workspace, _ring=True)
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, seq_len, advance=True, _ring=False):
     """Write k_new/v_new [B,Hkv,D] into row seq_len[b] of the caches [B,Hkv,Lmax,D]
     (device-side position); with advance, seq_len[b] += 1 on the device."""
+    entry = "attn_kv_append_ring" if _ring else "attn_kv_append"
     dev = _cuda(k_cache, v_cache, k_new, v_new, seq_len)
     B, Hkv, Lmax, D = k_cache.shape
     if v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape \
             or seq_len.shape != (B,) or seq_len.dtype != torch.int32:
         raise ValueError("caches [B,Hkv,Lmax,D], new rows [B,Hkv,D], seq_len int32 [B] required")
     with torch.cuda.device(dev):
-        _check(lib().attn_kv_append(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
-                                    v_new.data_ptr(), seq_len.data_ptr(), B, Hkv, Lmax, D,
-                                    _dtype(k_cache), 1 if advance else 0, _stream(dev)),
-               "attn_kv_append")
+        _check(getattr(lib(), entry)(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                                     v_new.data_ptr(), seq_len.data_ptr(), B, Hkv, Lmax, D,
+                                     _dtype(k_cache), 1 if advance else 0, _stream(dev)),
+               entry)
+
+
+def kv_append_ring(k_cache, v_cache, k_new, v_new, seq_len, advance=True):
+    """Ring-cache append: row seq_len[b] % Lmax (the oldest token's row once
+    the ring is full); with advance, seq_len[b] += 1 on the device."""
+    kv_append(k_cache, v_cache, k_new, v_new, seq_len, advance, _ring=True)
 
 
 def na3d_fwd(q, k, v, grid, kernel, o=None, scale=None):

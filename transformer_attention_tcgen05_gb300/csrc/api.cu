@@ -70,6 +70,13 @@ bool half_dtype(attn_dtype_t dt) { return dt == ATTN_BF16 || dt == ATTN_F16; }
 
 size_t elem_size(attn_dtype_t dt) { return dt == ATTN_F32 ? 4 : 2; }
 
+// A (batch, head or row) stride of a strided view: positive, a multiple of 16
+// bytes and below 2^40 bytes (the tensor-memory-access unit's stride limits).
+bool stride_ok(long long s, attn_dtype_t dt) {
+    const long long bytes = s * (long long)elem_size(dt);
+    return s >= 1 && s < (1ll << 38) && bytes % 16 == 0 && bytes < (1ll << 40);
+}
+
 // Extents whose element counts must stay below 2^31 per (batch, head) slice so
 // that 32-bit row indices inside the kernels cannot overflow.
 bool small_enough(long long rows, int D) { return rows > 0 && rows * D < (1ll << 31); }
@@ -171,6 +178,59 @@ attn_status_t attn_full_fwd(const void *q, const void *k, const void *v, void *o
     return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
 }
 
+attn_status_t attn_full_fwd_strided(const void *q, const void *k, const void *v, void *o,
+                                    int B, int H, int Nq, int Nkv, int D,
+                                    const int64_t q_strides[3], const int64_t k_strides[3],
+                                    const int64_t v_strides[3], const int64_t o_strides[3],
+                                    attn_dtype_t dtype, float scale, void *stream) {
+    if (!q || !k || !v || !o || !q_strides || !k_strides || !v_strides || !o_strides)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nkv < 1 || !valid_d(D) || !valid_dtype(dtype))
+        return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (o == q || o == k || o == v) return ATTN_ERR_INVALID_ARG;
+    const int64_t *in[4] = {q_strides, k_strides, v_strides, o_strides};
+    TensorStrides st[4];
+    for (int i = 0; i < 4; ++i) {
+        const long long ext[3] = {B, H, i == 0 || i == 3 ? Nq : Nkv};
+        long long s[3];
+        for (int a = 0; a < 3; ++a) {
+            // an extent-1 axis is never stepped along: any valid stride will do
+            s[a] = ext[a] == 1 ? D : (long long)in[i][a];
+            if (!stride_ok(s[a], dtype)) return ATTN_ERR_INVALID_ARG;
+        }
+        st[i] = TensorStrides{s[0], s[1], s[2]};
+    }
+    {
+        // o: the rows of D elements must be pairwise disjoint.  Sorted by
+        // stride, each axis' stride must be at least the span of the ones
+        // below it (the innermost span is the D-element row).
+        const long long ext[3] = {B, H, Nq};
+        const long long s[3] = {st[3].b, st[3].h, st[3].n};
+        int ord[3] = {0, 1, 2};
+        for (int a = 0; a < 3; ++a)
+            for (int b = a + 1; b < 3; ++b)
+                if (s[ord[b]] < s[ord[a]]) { const int t = ord[a]; ord[a] = ord[b]; ord[b] = t; }
+        long long span = D;
+        for (int a = 0; a < 3; ++a) {
+            if (ext[ord[a]] == 1) continue;
+            if (s[ord[a]] < span) return ATTN_ERR_INVALID_ARG;
+            span = s[ord[a]] * ext[ord[a]];
+        }
+    }
+    Ctx c;
+    attn_status_t status = get_ctx(stream, &c);
+    if (status != ATTN_OK) return status;
+    const float sc = resolve_scale(scale, D);
+    if (half_dtype(dtype) && tc_full_supported(B, H, Nq, Nkv, D)) {
+        status = tc_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc, st);
+        if (status != ATTN_ERR_UNSUPPORTED) return status;
+    }
+    return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc, st);
+}
+
 attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const void *v, void *o, int B,
                                   int Hq, int Hkv, int N, int D, attn_dtype_t dtype, float scale,
                                   void *stream) {
@@ -235,10 +295,11 @@ size_t attn_decode_gqa_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D) 
     return decode_workspace_bytes(B, Hq, Hkv, Lmax, D);
 }
 
-attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
-                              const int32_t *seq_len, void *o, int B, int Hq, int Hkv, int Lmax,
-                              int D, attn_dtype_t dtype, float scale, void *workspace,
-                              size_t workspace_bytes, void *stream) {
+static attn_status_t decode_entry(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *seq_len, void *o, int B, int Hq, int Hkv,
+                                  int Lmax, int D, attn_dtype_t dtype, float scale,
+                                  void *workspace, size_t workspace_bytes, void *stream,
+                                  bool ring) {
     if (!q || !k_cache || !v_cache || !seq_len || !o || !workspace) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -256,12 +317,28 @@ attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     return decode_gqa(c, dtype, q, k_cache, v_cache, seq_len, o, B, Hq, Hkv, Lmax, D,
-                      resolve_scale(scale, D), workspace, workspace_bytes);
+                      resolve_scale(scale, D), workspace, workspace_bytes, ring);
 }
 
-attn_status_t attn_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
-                             int32_t *seq_len, int B, int Hkv, int Lmax, int D, attn_dtype_t dtype,
-                             int advance, void *stream) {
+attn_status_t attn_decode_gqa(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *seq_len, void *o, int B, int Hq, int Hkv, int Lmax,
+                              int D, attn_dtype_t dtype, float scale, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    return decode_entry(q, k_cache, v_cache, seq_len, o, B, Hq, Hkv, Lmax, D, dtype, scale,
+                        workspace, workspace_bytes, stream, false);
+}
+
+attn_status_t attn_decode_gqa_ring(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *seq_len, void *o, int B, int Hq, int Hkv,
+                                   int Lmax, int D, attn_dtype_t dtype, float scale,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_entry(q, k_cache, v_cache, seq_len, o, B, Hq, Hkv, Lmax, D, dtype, scale,
+                        workspace, workspace_bytes, stream, true);
+}
+
+static attn_status_t append_entry(void *k_cache, void *v_cache, const void *k_new,
+                                  const void *v_new, int32_t *seq_len, int B, int Hkv, int Lmax,
+                                  int D, attn_dtype_t dtype, int advance, void *stream, bool ring) {
     if (!k_cache || !v_cache || !k_new || !v_new || !seq_len) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
         return ATTN_ERR_INVALID_ARG;
@@ -271,7 +348,22 @@ attn_status_t attn_kv_append(void *k_cache, void *v_cache, const void *k_new, co
     Ctx c;
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
-    return kv_append(c, dtype, k_cache, v_cache, k_new, v_new, seq_len, B, Hkv, Lmax, D, advance);
+    return kv_append(c, dtype, k_cache, v_cache, k_new, v_new, seq_len, B, Hkv, Lmax, D, advance,
+                     ring);
+}
+
+attn_status_t attn_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                             int32_t *seq_len, int B, int Hkv, int Lmax, int D, attn_dtype_t dtype,
+                             int advance, void *stream) {
+    return append_entry(k_cache, v_cache, k_new, v_new, seq_len, B, Hkv, Lmax, D, dtype, advance,
+                        stream, false);
+}
+
+attn_status_t attn_kv_append_ring(void *k_cache, void *v_cache, const void *k_new,
+                                  const void *v_new, int32_t *seq_len, int B, int Hkv, int Lmax,
+                                  int D, attn_dtype_t dtype, int advance, void *stream) {
+    return append_entry(k_cache, v_cache, k_new, v_new, seq_len, B, Hkv, Lmax, D, dtype, advance,
+                        stream, true);
 }
 
 static attn_status_t check_na(int T, int Hg, int W, const int kernel[3]) {

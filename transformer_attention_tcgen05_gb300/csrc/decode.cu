@@ -81,6 +81,7 @@ struct DecParams {
     void *o;
     int Hq, Hkv, Lmax, G;
     int splits, split_rows, ws_splits;
+    int ring;                // seq_len counts every token appended; the cache holds the last Lmax
     float qscale;
     float *part_o;           // [units][ws_splits][GP][D]
     float *part_ml;          // [units][ws_splits][GP][2]
@@ -121,11 +122,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int unit = b * p.Hkv + kvh;
 
-    const int L = p.seq_len[b];
-    if (L < 1 || L > p.Lmax) {          // invalid length: report, touch nothing
+    const int len = p.seq_len[b];
+    if (len < 1 || (!p.ring && len > p.Lmax)) {   // invalid length: report, touch nothing
         if (threadIdx.x == 0) raise_device_error(p.err, kDevCheck);
         return;
     }
+    // rows in use: every row once a ring cache has wrapped (attention over a
+    // set of keys does not depend on the order of the rows that hold them)
+    const int L = imin(len, p.Lmax);
     const int r0 = split * p.split_rows;
     const int r1 = imin(r0 + p.split_rows, L);
     const int nchunks = r1 > r0 ? cdiv(r1 - r0, kRowsPerChunk) : 0;
@@ -658,7 +662,7 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D) {
 
 attn_status_t decode_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                          const void *v, const int32_t *seq_len, void *o, int B, int Hq, int Hkv,
-                         int Lmax, int D, float scale, void *ws, size_t ws_bytes) {
+                         int Lmax, int D, float scale, void *ws, size_t ws_bytes, bool ring) {
     const bool f16 = dt == ATTN_F16;
     const int G = Hq / Hkv;
     const int GP = gp_for(G);
@@ -673,6 +677,7 @@ attn_status_t decode_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const voi
     p.seq_len = seq_len;
     p.o = o;
     p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
+    p.ring = ring;
     p.ws_splits = max_splits_for(Lmax);
     p.splits = splits_for(B, Hkv, Lmax, c.sm_count);
     p.split_rows = cdiv(cdiv(Lmax, p.splits), kRowsPerChunk) * kRowsPerChunk;

@@ -38,10 +38,15 @@ attn_status_t launch_status(int family);
 // Sets the dynamic shared-memory limit of `func` once per device.
 bool ensure_smem_attr(const void *func, size_t bytes, int device, int *done_mask);
 
+// Element strides of a [B, heads, N, D] tensor with D contiguous.
+struct TensorStrides {
+    long long b, h, n;
+};
+
 // fp32 / generic SIMT flash attention (exact FFMA for fp32 storage).
 attn_status_t simt_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                         const void *v, void *o, int B, int H, int Nq, int Nkv, int D,
-                        float scale);
+                        float scale, const TensorStrides *st = nullptr);
 attn_status_t simt_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                         const void *v, void *o, int B, int H, int T, int Hg, int W, int D,
                         const int kernel[3], float scale);
@@ -53,20 +58,24 @@ attn_status_t rope_rotate_qk(const Ctx &c, attn_dtype_t dt, const void *q, const
                              void *qr, void *kr, int BH, int N, int D, const int32_t *pos,
                              const int axes_dim[4], float theta);
 
-// KV-cache append at the device-side position seq_len[b] (optionally advancing it).
+// KV-cache append at the device-side position seq_len[b] (optionally advancing it);
+// ring: the cache keeps the last Lmax tokens, token t in row t % Lmax.
 attn_status_t kv_append(const Ctx &c, attn_dtype_t dt, void *kc, void *vc, const void *kn,
                         const void *vn, int32_t *seq_len, int B, int Hkv, int Lmax, int D,
-                        int advance);
+                        int advance, bool ring = false);
 
 // Split-KV GQA decode (bf16 or f16 cache).
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
 attn_status_t decode_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                          const void *v, const int32_t *seq_len, void *o, int B, int Hq, int Hkv,
-                         int Lmax, int D, float scale, void *ws, size_t ws_bytes);
+                         int Lmax, int D, float scale, void *ws, size_t ws_bytes,
+                         bool ring = false);
 
 // tcgen05 (tensor-core) flash attention, bf16 or f16: full and neighborhood.
+// st: strides of q, k, v, o (nullptr: contiguous).
 attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
-                      void *o, int B, int H, int Nq, int Nkv, int D, float scale);
+                      void *o, int B, int H, int Nq, int Nkv, int D, float scale,
+                      const TensorStrides *st = nullptr);
 bool tc_full_supported(int B, int H, int Nq, int Nkv, int D);
 attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                             const void *v, void *o, int B, int Hq, int Hkv, int N, int D,

@@ -23,19 +23,22 @@ namespace {
 template <typename T>
 __global__ void __launch_bounds__(128) kv_append_kernel(T *kc, T *vc, const T *kn, const T *vn,
                                                         int32_t *seq_len, int Hkv, int Lmax,
-                                                        int D, int advance, unsigned *err) {
+                                                        int D, int advance, int ring,
+                                                        unsigned *err) {
     const int b = blockIdx.x;
     const int pos = seq_len[b];
-    if (pos < 0 || pos >= Lmax) {            // cache full or corrupt length: write nothing
+    // linear cache: full or corrupt length; ring: a count that cannot advance
+    if (pos < 0 || (ring ? pos == 0x7fffffff : pos >= Lmax)) {   // write nothing
         if (threadIdx.x == 0) raise_device_error(err, kDevCheck);
         return;
     }
+    const int row = ring ? pos % Lmax : pos;
     constexpr int VEC = 16 / sizeof(T);
     const int per_head = D / VEC;
     for (int i = threadIdx.x; i < Hkv * per_head; i += blockDim.x) {
         const int h = i / per_head, c = i % per_head;
         const size_t src = (size_t(b) * Hkv + h) * D;
-        const size_t dst = ((size_t(b) * Hkv + h) * Lmax + pos) * D;
+        const size_t dst = ((size_t(b) * Hkv + h) * Lmax + row) * D;
         reinterpret_cast<uint4 *>(kc + dst)[c] = reinterpret_cast<const uint4 *>(kn + src)[c];
         reinterpret_cast<uint4 *>(vc + dst)[c] = reinterpret_cast<const uint4 *>(vn + src)[c];
     }
@@ -50,17 +53,17 @@ __global__ void __launch_bounds__(128) kv_append_kernel(T *kc, T *vc, const T *k
 // f16 rows are 2-byte elements like bf16: the same 16-byte copies serve both.
 attn_status_t kv_append(const Ctx &c, attn_dtype_t dt, void *kc, void *vc, const void *kn,
                         const void *vn, int32_t *seq_len, int B, int Hkv, int Lmax, int D,
-                        int advance) {
+                        int advance, bool ring) {
     if (B > 2147483647) return ATTN_ERR_UNSUPPORTED;
     if (dt == ATTN_F32)
         kv_append_kernel<float><<<B, 128, 0, c.stream>>>(
             static_cast<float *>(kc), static_cast<float *>(vc), static_cast<const float *>(kn),
-            static_cast<const float *>(vn), seq_len, Hkv, Lmax, D, advance, c.err);
+            static_cast<const float *>(vn), seq_len, Hkv, Lmax, D, advance, ring, c.err);
     else
         kv_append_kernel<__nv_bfloat16><<<B, 128, 0, c.stream>>>(
             static_cast<__nv_bfloat16 *>(kc), static_cast<__nv_bfloat16 *>(vc),
             static_cast<const __nv_bfloat16 *>(kn), static_cast<const __nv_bfloat16 *>(vn), seq_len,
-            Hkv, Lmax, D, advance, c.err);
+            Hkv, Lmax, D, advance, ring, c.err);
     return launch_status(kFamKvAppend);
 }
 

@@ -37,7 +37,11 @@ struct SimtParams {
     int bt, bh, bw;          // query box
     int nbh, nbw;            // boxes along h and w
     // causal grouped-query prefill (group > 1: KV head = query head / group)
-    int causal, Hq, Hkv, group;
+    int causal, group;
+    // H query heads: block row bh is batch bh / H, head bh % H; element
+    // strides (batch, head, row) of q, k, v, o with D contiguous
+    int H;
+    TensorStrides sq, sk, sv, so;
 };
 
 template <int D>
@@ -77,11 +81,11 @@ simt_flash_kernel(const SimtParams p) {
     const size_t bh = blockIdx.y;
     const int tile = blockIdx.x;
 
-    const size_t bkv = p.group > 1 ? (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group : bh;
-    const T *qg = static_cast<const T *>(p.q) + bh * size_t(p.Nq) * D;
-    const T *kg = static_cast<const T *>(p.k) + bkv * size_t(p.Nkv) * D;
-    const T *vg = static_cast<const T *>(p.v) + bkv * size_t(p.Nkv) * D;
-    T *og = static_cast<T *>(p.o) + bh * size_t(p.Nq) * D;
+    const long long b = bh / p.H, h = bh % p.H, hk = h / p.group;
+    const T *qg = static_cast<const T *>(p.q) + (b * p.sq.b + h * p.sq.h);
+    const T *kg = static_cast<const T *>(p.k) + (b * p.sk.b + hk * p.sk.h);
+    const T *vg = static_cast<const T *>(p.v) + (b * p.sv.b + hk * p.sv.h);
+    T *og = static_cast<T *>(p.o) + (b * p.so.b + h * p.so.h);
 
     int qi = 0;
     bool qvalid;
@@ -123,7 +127,7 @@ simt_flash_kernel(const SimtParams p) {
 #pragma unroll
     for (int d = 0; d < 32; d += 4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qvalid) x = load4<T>(qg + size_t(qi) * D + sl * 32 + d);
+        if (qvalid) x = load4<T>(qg + qi * p.sq.n + sl * 32 + d);
         qv[d] = x.x * p.qscale;
         qv[d + 1] = x.y * p.qscale;
         qv[d + 2] = x.z * p.qscale;
@@ -148,8 +152,8 @@ simt_flash_kernel(const SimtParams p) {
                 } else {
                     g = u;
                 }
-                kx = load4<T>(kg + size_t(g) * D + d0);
-                vx = load4<T>(vg + size_t(g) * D + d0);
+                kx = load4<T>(kg + g * p.sk.n + d0);
+                vx = load4<T>(vg + g * p.sv.n + d0);
             } else if (d0 == 0) {
                 kc[kk] = make_int4(0, 0, 0, 0);
             }
@@ -219,7 +223,7 @@ simt_flash_kernel(const SimtParams p) {
 
     if (qvalid) {
         const float inv = 1.f / l;
-        T *orow = og + size_t(qi) * D + sl * 32;
+        T *orow = og + qi * p.so.n + sl * 32;
 #pragma unroll
         for (int d = 0; d < 32; ++d) Elem<T>::store(orow + d, acc[d] * inv);
     }
@@ -300,13 +304,24 @@ attn_status_t dispatch(const Ctx &c, attn_dtype_t dt, int D, const SimtParams &p
 
 }  // namespace
 
+// Contiguous [B, heads, N, D] strides.
+static TensorStrides dense(int heads, int N, int D) {
+    return TensorStrides{(long long)heads * N * D, (long long)N * D, D};
+}
+
 attn_status_t simt_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                         const void *v, void *o, int B, int H, int Nq, int Nkv, int D,
-                        float scale) {
+                        float scale, const TensorStrides *st) {
     SimtParams p{};
     p.q = q; p.k = k; p.v = v; p.o = o;
     p.Nq = Nq; p.Nkv = Nkv;
     p.qscale = scale * kLog2e;
+    p.group = 1;
+    p.H = H;
+    p.sq = st ? st[0] : dense(H, Nq, D);
+    p.sk = st ? st[1] : dense(H, Nkv, D);
+    p.sv = st ? st[2] : dense(H, Nkv, D);
+    p.so = st ? st[3] : dense(H, Nq, D);
     return dispatch<false>(c, dt, D, p, cdiv(Nq, kRows), B * H);
 }
 
@@ -318,7 +333,10 @@ attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, cons
     p.Nq = p.Nkv = N;
     p.qscale = scale * kLog2e;
     p.causal = 1;
-    p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;   // group 1: every head reads its own K/V
+    p.group = Hq / Hkv;   // group 1: every head reads its own K/V
+    p.H = Hq;
+    p.sq = p.so = dense(Hq, N, D);
+    p.sk = p.sv = dense(Hkv, N, D);
     return dispatch<false>(c, dt, D, p, cdiv(N, kRows), B * Hq);
 }
 
@@ -329,6 +347,9 @@ attn_status_t simt_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void
     p.q = q; p.k = k; p.v = v; p.o = o;
     p.Nq = p.Nkv = T * Hg * W;
     p.qscale = scale * kLog2e;
+    p.group = 1;
+    p.H = H;
+    p.sq = p.sk = p.sv = p.so = dense(H, p.Nq, D);
     p.T = T; p.Hg = Hg; p.W = W;
     p.kt = kernel[0]; p.kh = kernel[1]; p.kw = kernel[2];
     p.et = imin(kernel[0], T); p.eh = imin(kernel[1], Hg); p.ew = imin(kernel[2], W);

@@ -131,6 +131,10 @@ struct TcParams {
     float penalty;           // bf16-exact power of two; penalty * c_log2 >= 300
     // causal grouped-query prefill
     int Hq, Hkv, group;
+    // full / causal: q, k, v are 4D tensor maps {D, N, heads, B}; o is written
+    // through element strides (batch, head, row), D contiguous
+    int H;                   // query heads (the batch of block row bh is bh / H)
+    long long o_sb, o_sh, o_sn;
 };
 
 // Barrier block at OFF_BAR.
@@ -220,9 +224,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
-    // K/V (batch, head) row of the tensor maps: the query head's KV head for
-    // grouped-query attention (contiguous groups of Hq / Hkv query heads)
-    const int bkv = CAUSAL ? (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group : bh;
+    // full attention: batch and head of this block row, and the K/V head (the
+    // query head's KV head for grouped-query attention: contiguous groups of
+    // Hq / Hkv query heads)
+    const int fb = NA ? 0 : bh / p.H, fh = NA ? 0 : bh % p.H;
+    const int fkh = CAUSAL ? fh / p.group : fh;
 
     // ---- per-CTA work description (identical in every role)
     int n_t[kNQ];
@@ -373,7 +379,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                                 ptx::tma_load_5d(dst, &tq, pn * 64, g[t].w0, g[t].h0, g[t].t0, bh,
                                                  &bars->q_full, pol_q);
                         } else {
-                            ptx::tma_load_3d(dst, &tq, pn * 64, q0 + t * kBM, bh, &bars->q_full,
+                            ptx::tma_load_4d(dst, &tq, pn * 64, q0 + t * kBM, fh, fb, &bars->q_full,
                                              pol_q);
                         }
                     }
@@ -404,7 +410,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                             na_key_box(g[u], BNt / kKW, j, kt_, kh_, kw_);
                             ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, &full[s], pol_kv);
                         } else {
-                            ptx::tma_load_3d(dst, tm, pn * 64, j * kBN, bkv, &full[s], pol_kv);
+                            ptx::tma_load_4d(dst, tm, pn * 64, j * kBN, fkh, fb, &full[s], pol_kv);
                         }
                     }
                 }
@@ -752,10 +758,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             if (qvalid) {
                 size_t idx;
                 if constexpr (NA)
-                    idx = (size_t(bh) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw;
+                    idx = ((size_t(bh) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw) * D;
                 else
-                    idx = size_t(bh) * p.Nq + q0 + t * kBM + row;
-                orow = static_cast<typename H16<F16>::T *>(p.o) + idx * D;
+                    idx = size_t(fb * p.o_sb + fh * p.o_sh + (long long)(q0 + t * kBM + row) * p.o_sn);
+                orow = static_cast<typename H16<F16>::T *>(p.o) + idx;
             }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -1050,26 +1056,48 @@ NaPlan cached_plan(int T, int Hg, int W, const int kern[3]) {
 
 }  // namespace
 
+// 4D map {D, N, heads, B} over a tensor with element strides (row, head,
+// batch) and D contiguous; 128-byte swizzle, box {64, 128, 1, 1}.
+bool make_tmap4(CUtensorMap *m, const void *base, int D, int N, int heads, int B,
+                const TensorStrides &st, bool f16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t gdim[4] = {cuuint64_t(D), cuuint64_t(N), cuuint64_t(heads), cuuint64_t(B)};
+    const cuuint64_t gstride[3] = {cuuint64_t(st.n) * 2, cuuint64_t(st.h) * 2, cuuint64_t(st.b) * 2};
+    const cuuint32_t box[4] = {64, kBM, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void *>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_full_supported(int B, int H, int Nq, int Nkv, int D) {
     return (D == 64 || D == 128) && B * H <= 65535 && Nq >= 1 && Nkv >= 1 && encode_fn() != nullptr;
 }
 
 attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
-                      void *o, int B, int H, int Nq, int Nkv, int D, float scale) {
+                      void *o, int B, int H, int Nq, int Nkv, int D, float scale,
+                      const TensorStrides *st) {
     const bool f16 = dt == ATTN_F16;
+    TensorStrides s4[4];                 // q, k, v, o
+    for (int i = 0; i < 4; ++i) {
+        const int n = i == 0 || i == 3 ? Nq : Nkv;
+        s4[i] = st ? st[i] : TensorStrides{(long long)H * n * D, (long long)n * D, D};
+    }
     CUtensorMap tq, tk, tv;
-    const uint64_t dq[3] = {uint64_t(D), uint64_t(Nq), uint64_t(B) * H};
-    const uint64_t dk[3] = {uint64_t(D), uint64_t(Nkv), uint64_t(B) * H};
-    const uint32_t box[3] = {64, kBM, 1};
-    if (!make_tmap(&tq, q, 3, dq, box, f16) || !make_tmap(&tk, k, 3, dk, box, f16) ||
-        !make_tmap(&tv, v, 3, dk, box, f16))
-        return ATTN_ERR_CUDA;
+    // a layout the tensor-map encoder refuses goes to the strided SIMT kernel
+    if (!make_tmap4(&tq, q, D, Nq, H, B, s4[0], f16) || !make_tmap4(&tk, k, D, Nkv, H, B, s4[1], f16) ||
+        !make_tmap4(&tv, v, D, Nkv, H, B, s4[2], f16))
+        return ATTN_ERR_UNSUPPORTED;
     TcParams p{};
     p.Nq = Nq;
     p.Nkv = Nkv;
     p.c_log2 = scale * kLog2e;
     p.o = o;
     p.err = c.err;
+    p.H = H;
+    p.o_sb = s4[3].b; p.o_sh = s4[3].h; p.o_sn = s4[3].n;
     const dim3 grid(cdiv(Nq, kNQ * kBM), B * H);
     if (f16)
         return D == 128 ? launch_tc<128, false, false, 0, true>(c, tq, tk, tv, p, grid)
@@ -1083,11 +1111,10 @@ attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const 
                             float scale) {
     const bool f16 = dt == ATTN_F16;
     CUtensorMap tq, tk, tv;
-    const uint64_t dq[3] = {uint64_t(D), uint64_t(N), uint64_t(B) * Hq};
-    const uint64_t dk[3] = {uint64_t(D), uint64_t(N), uint64_t(B) * Hkv};
-    const uint32_t box[3] = {64, kBM, 1};
-    if (!make_tmap(&tq, q, 3, dq, box, f16) || !make_tmap(&tk, k, 3, dk, box, f16) ||
-        !make_tmap(&tv, v, 3, dk, box, f16))
+    const TensorStrides sq{(long long)Hq * N * D, (long long)N * D, D};
+    const TensorStrides skv{(long long)Hkv * N * D, (long long)N * D, D};
+    if (!make_tmap4(&tq, q, D, N, Hq, B, sq, f16) || !make_tmap4(&tk, k, D, N, Hkv, B, skv, f16) ||
+        !make_tmap4(&tv, v, D, N, Hkv, B, skv, f16))
         return ATTN_ERR_CUDA;
     TcParams p{};
     p.Nq = N;
@@ -1098,6 +1125,8 @@ attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const 
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
+    p.H = Hq;
+    p.o_sb = sq.b; p.o_sh = sq.h; p.o_sn = sq.n;
     const dim3 grid(cdiv(N, kNQ * kBM), B * Hq);
     if (f16)
         return D == 128 ? launch_tc<128, false, true, 0, true>(c, tq, tk, tv, p, grid)

@@ -1,4 +1,4 @@
-// Tensor-core (tcgen05 + TMEM + TMA) flash attention for bf16, sm_103a.
+// Tensor-core (tcgen05 + TMEM + TMA) flash attention for bf16 and f16, sm_103a.
 //
 // S = Q K^T * scale, row softmax, O = P V, streamed over key tiles with an
 // online softmax (the attention of iris.c issue #15 "CUDA codepath !" and the
@@ -31,17 +31,24 @@
 //       S_t(j) into registers, then PV0(j), PV1(j) -- the next S is computed
 //       while the softmax of the current tile runs.
 //
-// Softmax (base 2): x = s * scale * log2(e); the running max m is only moved
-// when the tile max exceeds it by more than 8 (P stays <= 2^8); only then is
+// Softmax (base 2): x = s * scale * log2(e).  The first tile sets the running
+// max m; later tiles are exponentiated against m as it stands (no tile-max
+// pass) and only a tile whose row sum overflows a bound is redone with its own
+// max, which moves m if the tile max exceeds it by more than 8; only then is
 // O_t rescaled in TMEM, after waiting for the previous PV_t to complete.
 // Every branch that leads to a warp-collective tcgen05.ld / st is uniform
 // across the warp.
 //
-// Full attention: both query tiles share each K/V tile (one stream).
+// Full attention: both query tiles share each K/V tile (one stream).  Q, K
+// and V are 4D tensor maps {D, N, heads, B} built from each tensor's element
+// strides (contiguous for the plain entries), and the epilogue stores through
+// the output's strides, so strided views are read and written in place.
 // Neighborhood attention: the two query tiles are two 3D boxes adjacent in w;
 // each streams the union of its queries' clamped windows as (1, KH, 16)
-// (t, h, w) key sub-boxes loaded by 5D TMA, masked per element; a warp whose
-// 32 rows are all outside a key tile's window skips the exponentials.
+// (t, h, w) key sub-boxes loaded by 5D TMA.  The h and w window tests enter S
+// as a large negative penalty through one extra 16-channel MMA k-step (one-hot
+// query offsets against per-sub-box key penalty tiles); a key frame outside a
+// row's t window is dropped in the softmax (P = 0).
 //
 // All spin-waits are bounded (1 s); on a timeout the CTA raises the device
 // error word, drains what it issued, frees TMEM and exits.
@@ -631,98 +638,45 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 ptx::mbar_arrive(&bars->s_free[t]);
             }
 
-            // ---- mask and tile maximum
-            float mt;
-            {
-                if constexpr (NA) {
-                    // columns past this tile's keys (N = KH * 16 < 128) hold stale
-                    // values: whole 16-column groups, warp-uniform
+            // ---- mask: keys that do not exist in this tile
+            if constexpr (NA) {
+                // columns past this tile's keys (N = KH * 16 < 128) hold stale
+                // values: whole 16-column groups, warp-uniform
 #pragma unroll
-                    for (int gq = 0; gq < kBN / 16; ++gq)
-                        if (gq * 16 >= BNt) {
+                for (int gq = 0; gq < kBN / 16; ++gq)
+                    if (gq * 16 >= BNt) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) sv[gq * 16 + i] = -INFINITY;
-                        }
-                } else {
-                    int valid = p.Nkv - j * kBN;           // keys of this tile inside the sequence
-                    if constexpr (CAUSAL) {
-                        // the last tile is the diagonal one (query tile and key tile
-                        // start at the same position): key e is visible to row `row`
-                        // iff e <= row
-                        if (j == nt - 1) {
-#pragma unroll
-                            for (int e = 0; e < kBN; ++e)
-                                if (e > row || e >= valid) sv[e] = -INFINITY;
-                            valid = kBN;
-                        }
+                        for (int i = 0; i < 16; ++i) sv[gq * 16 + i] = -INFINITY;
                     }
-                    if (valid < kBN) {
+            } else {
+                int valid = p.Nkv - j * kBN;           // keys of this tile inside the sequence
+                if constexpr (CAUSAL) {
+                    // the last tile is the diagonal one (query tile and key tile
+                    // start at the same position): key e is visible to row `row`
+                    // iff e <= row
+                    if (j == nt - 1) {
 #pragma unroll
                         for (int e = 0; e < kBN; ++e)
-                            if (e >= valid) sv[e] = -INFINITY;
+                            if (e > row || e >= valid) sv[e] = -INFINITY;
+                        valid = kBN;
                     }
                 }
-                float mx[8];
+                if (valid < kBN) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
-#pragma unroll
-                for (int e = 16; e < kBN; e += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx[i] = ptx::fmax3(mx[i], sv[e + i], sv[e + 8 + i]);
-                const float tmax = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
-                                              ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-                mt = t_ok ? tmax * cl : -INFINITY;   // cl > 0: max commutes with the scaling
+                    for (int e = 0; e < kBN; ++e)
+                        if (e >= valid) sv[e] = -INFINITY;
+                }
             }
 
-            // ---- the previous P V must be done before O is rescaled or P_t rewritten
-            const bool want = j == 0 || mt > m + 8.f;   // this row moves its maximum
-            const bool any_want = __any_sync(0xffffffffu, want);
-            if (j > 0 && (C::SEP_P || any_want)) {
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
-                                                                     p.err, abort))) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-            }
-            // ---- running maximum (moved lazily) and O rescale in TMEM
-            if (j == 0) {
-                m = mt;
-            } else if (any_want) {
-                // rows that move m scale their O row; the others multiply by 1
-                const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
+            // P = 2^(x - m) in 16-bit into TMEM; returns the tile's row sum (fp32)
+            auto emit_p = [&](float nmu) -> float {
+                float acc[8];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    ptx::tmem_ld32(o_addr + c * 32, ov);
-                    ptx::tmem_wait_ld();
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float a0, a1;
-                        ptx::ffma2(a0, a1, __uint_as_float(ov[e]), __uint_as_float(ov[e + 1]), f, f,
-                                   0.f, 0.f);
-                        ov[e] = __float_as_uint(a0);
-                        ov[e + 1] = __float_as_uint(a1);
-                    }
-                    ptx::tmem_st32(o_addr + c * 32, ov);
-                }
-                if (want) {
-                    l *= f;
-                    m = mt;
-                }
-            }
-            // (a row whose t window misses this key sub-box gets P = 0)
-            const float nmu = !t_ok ? -INFINITY : (m == -INFINITY) ? 0.f : -m;
-
-            // ---- P = 2^(x - m) in bf16 into TMEM, row sum in fp32
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                if (c * 32 >= BNt) break;
-                uint32_t pk[16];
-                {
+                for (int c = 0; c < kBN / 32; ++c) {
+                    if (c * 32 >= BNt) break;
+                    uint32_t pk[16];
                     // the upper 16 keys of the last 32-key chunk may lie past the tile
                     const int ne = (c * 32 + 32 <= BNt) ? 16 : 8;
 #pragma unroll
@@ -739,10 +693,92 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                                    acc[(2 * e + 1) & 7], p0, p1);
                         pk[e] = H16<F16>::pack(p0, p1);
                     }
+                    ptx::tmem_st16(p_addr + c * 16, pk);
                 }
-                ptx::tmem_st16(p_addr + c * 16, pk);
+                return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            };
+
+            // ---- fast path: exponentiate against the running maximum m as it
+            //      stands, with no tile maximum.  P only has to stay finite in its
+            //      16-bit type, not below 1: a tile whose row sum exceeds 2^24 (2^15
+            //      for f16, whose largest finite value is 65504) or is not finite
+            //      (scores far above m, or m still the garbage of a row whose
+            //      first tiles were all outside its window) is redone below
+            //      against its own maximum.  After the first tiles m is close to
+            //      the row maximum and the redo almost never runs.
+            bool fast = j > 0 && __all_sync(0xffffffffu, !(t_ok && m == -INFINITY));
+            bool waited = false;                 // o_done of step j - 1 observed
+            if (fast) {
+                if constexpr (C::SEP_P) {
+                    // P_t has columns of its own: the previous P V must have read them
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
+                                                                         p.err, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    waited = true;
+                }
+                const float lt = emit_p(t_ok ? -m : -INFINITY);
+                if (__any_sync(0xffffffffu, !(lt <= (F16 ? 32768.f : 16777216.f))))
+                    fast = false;                 // redo the tile (P is rewritten below)
+                else
+                    l += lt;
             }
-            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+
+            if (!fast) {
+                // ---- tile maximum
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+                for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = ptx::fmax3(mx[i], sv[e + i], sv[e + 8 + i]);
+                const float tmax = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
+                                              ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                const float mt = t_ok ? tmax * cl : -INFINITY;   // cl > 0: max commutes with the scaling
+
+                // ---- the previous P V must be done before O is rescaled or P_t rewritten
+                const bool want = j == 0 || mt > m + 8.f;   // this row moves its maximum
+                const bool any_want = __any_sync(0xffffffffu, want);
+                if (j > 0 && !waited && (C::SEP_P || any_want)) {
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
+                                                                         p.err, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                // ---- running maximum (moved lazily) and O rescale in TMEM
+                if (j == 0) {
+                    m = mt;
+                } else if (any_want) {
+                    // rows that move m scale their O row; the others multiply by 1
+                    const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        ptx::tmem_ld32(o_addr + c * 32, ov);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float a0, a1;
+                            ptx::ffma2(a0, a1, __uint_as_float(ov[e]), __uint_as_float(ov[e + 1]), f,
+                                       f, 0.f, 0.f);
+                            ov[e] = __float_as_uint(a0);
+                            ov[e + 1] = __float_as_uint(a1);
+                        }
+                        ptx::tmem_st32(o_addr + c * 32, ov);
+                    }
+                    if (want) {
+                        l *= f;
+                        m = mt;
+                    }
+                }
+                // (a row whose t window misses this key sub-box gets P = 0)
+                l += emit_p(!t_ok ? -INFINITY : (m == -INFINITY) ? 0.f : -m);
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bars->p_ready[t]);

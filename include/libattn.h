@@ -142,6 +142,24 @@ ATTN_API attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const v
                                            attn_dtype_t dtype, float scale, void *stream);
 
 /*
+ * Causal grouped-query prefill on strided views: the operation of
+ * attn_causal_gqa_fwd with q, k, v and o addressed through element strides
+ * of (batch, head, row) as in attn_full_fwd_strided (D contiguous, every
+ * stride a multiple of 16 bytes, extent-1 axes' strides ignored, o's rows
+ * disjoint), so a Llama layer's [B, N, Hq, D] query projection and a packed
+ * [B, N, 2, Hkv, D] key/value projection are read in place.
+ * Passage: as attn_causal_gqa_fwd; the layout is an addressing choice with
+ * no counterpart in the pages.
+ */
+ATTN_API attn_status_t attn_causal_gqa_fwd_strided(const void *q, const void *k, const void *v,
+                                                  void *o, int B, int Hq, int Hkv, int N, int D,
+                                                  const int64_t q_strides[3],
+                                                  const int64_t k_strides[3],
+                                                  const int64_t v_strides[3],
+                                                  const int64_t o_strides[3],
+                                                  attn_dtype_t dtype, float scale, void *stream);
+
+/*
  * Single-token grouped-query decode attention over a KV cache.
  *   q [B, Hq, D], o [B, Hq, D]; k_cache, v_cache [B, Hkv, Lmax, D].
  *   seq_len: DEVICE int32 [B], 1 <= seq_len[b] <= Lmax (checked on the device;

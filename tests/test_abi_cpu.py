@@ -106,6 +106,24 @@ def test_full_strided_validation(L):
                                    ctypes.c_float(0.0), None) == 1
 
 
+def test_causal_strided_validation(L):
+    """Only layouts that must be refused are passed: the pointers are fake."""
+    L.attn_causal_gqa_fwd_strided.restype = ctypes.c_int
+    S = ctypes.c_int64 * 3
+    B, Hq, Hkv, N, D = 2, 4, 2, 16, 64
+    q = S(Hq * N * D, N * D, D)
+    kv = S(Hkv * N * D, N * D, D)
+
+    def call(qs=q, ks=kv, os_=q, hq=Hq, hkv=Hkv):
+        return L.attn_causal_gqa_fwd_strided(FAKE, FAKE, FAKE, ctypes.c_void_p(0x20000), B, hq,
+                                             hkv, N, D, qs, ks, kv, os_, 1, ctypes.c_float(0.0),
+                                             None)
+    assert call(hq=3, hkv=2) == 1                                # Hq not a multiple of Hkv
+    assert call(ks=S(Hkv * N * D, N * D, D + 2)) == 1            # K row stride 132 bytes
+    assert call(os_=S(Hq * N * D, D, D)) == 1                    # heads share output rows
+    assert call(qs=None) == 1
+
+
 def test_na3d_validation(L):
     L.attn_na3d_fwd.restype = ctypes.c_int
     o = ctypes.c_void_p(0x20000)

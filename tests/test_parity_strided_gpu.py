@@ -93,3 +93,26 @@ def test_broadcast_batch_of_one_ignores_its_stride(ta):
     k, v = base[1:2], base[2:3]
     o = torch.empty((1, H, N, D), dtype=torch.bfloat16, device="cuda")
     _check(ta, q, k, v, o, "bf16", "tc_flash", "batch of one")
+
+
+@pytest.mark.parametrize("dt,D,family", [("bf16", 128, "tc_flash"), ("f16", 64, "tc_flash"),
+                                         ("f32", 64, "simt")])
+def test_causal_gqa_llama_projection_layout(ta, dt, D, family):
+    """Causal GQA prefill reading q from a [B, N, Hq, D] projection and k, v
+    from one packed [B, N, 2, Hkv, D] projection, writing o into [B, N, Hq, D]."""
+    import torch
+    B, Hq, Hkv, N = 2, 4, 2, 300
+    g = np.random.default_rng(9950 + D)
+    qb = _dev(g.standard_normal((B, N, Hq, D), dtype=np.float32), dt)
+    kvb = _dev(g.standard_normal((B, N, 2, Hkv, D), dtype=np.float32), dt)
+    ob = torch.full_like(qb, 5.0)
+    q, o = qb.transpose(1, 2), ob.transpose(1, 2)
+    k, v = kvb[:, :, 0].transpose(1, 2), kvb[:, :, 1].transpose(1, 2)
+    n0 = ta.launch_count(family)
+    ta.causal_gqa_fwd_strided(q, k, v, o)
+    assert ta.launch_count(family) > n0, f"{family} did not launch"
+    assert ta.device_status() == 0
+    ref = oracle.causal_gqa_fwd(to_host64(q), to_host64(k), to_host64(v))
+    assert_close(to_host64(o), ref, dt, f"{dt} causal strided D={D}")
+    dense = ta.causal_gqa_fwd(q.contiguous(), k.contiguous(), v.contiguous())
+    assert torch.equal(dense, o), "strided causal result differs from the contiguous one"

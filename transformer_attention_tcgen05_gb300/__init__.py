@@ -24,7 +24,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "AttnError", "lib", "full_fwd", "full_fwd_strided", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
+    "AttnError", "lib", "full_fwd", "full_fwd_strided", "causal_gqa_fwd_strided", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
     "na3d_window_starts", "kv_append", "kv_append_ring", "decode_gqa_ring", "decode_workspace_bytes", "rope_joint_workspace_bytes",
     "device_status", "launch_count", "version", "FAMILIES", "LIB_PATH",
 ]
@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
         _st = ctypes.POINTER(ctypes.c_int64)
         L.attn_full_fwd_strided.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                             _st, _st, _st, _st, _i, _f, _vp]
+        L.attn_causal_gqa_fwd_strided.argtypes = L.attn_full_fwd_strided.argtypes
         L.attn_status_string.argtypes = [_i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_device_status.argtypes = [_vp]
@@ -86,6 +87,7 @@ def lib() -> ctypes.CDLL:
         for name in ("attn_full_fwd", "attn_rope_joint_fwd", "attn_decode_gqa", "attn_na3d_fwd",
                      "attn_na3d_window_starts", "attn_device_status", "attn_kv_append",
                      "attn_causal_gqa_fwd", "attn_full_fwd_strided", "attn_kv_append_ring",
+                     "attn_causal_gqa_fwd_strided",
                      "attn_decode_gqa_ring"):
             getattr(L, name).restype = _i
         _lib = L
@@ -191,6 +193,28 @@ def causal_gqa_fwd(q, k, v, o=None, scale=None):
         _check(lib().attn_causal_gqa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          B, Hq, Hkv, N, D, _dtype(q), _scale(scale), _stream(dev)),
                "attn_causal_gqa_fwd")
+    return o
+
+
+def causal_gqa_fwd_strided(q, k, v, o=None, scale=None):
+    """Causal GQA prefill on strided views q [B,Hq,N,D], k/v [B,Hkv,N,D] (D
+    contiguous), e.g. transposed projections or slices of a packed K/V tensor.
+    o defaults to a new contiguous tensor."""
+    dev = _cuda(q, k, v, strided=True)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, D) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k/v must be [B, Hkv, N, D] with q's dtype")
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if o is None else o
+    _cuda(q, o, strided=True)
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must be [B, Hq, N, D] with q's dtype")
+    with torch.cuda.device(dev):
+        _check(lib().attn_causal_gqa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                 o.data_ptr(), B, Hq, Hkv, N, D, _strides(q),
+                                                 _strides(k), _strides(v), _strides(o), _dtype(q),
+                                                 _scale(scale), _stream(dev)),
+               "attn_causal_gqa_fwd_strided")
     return o
 
 

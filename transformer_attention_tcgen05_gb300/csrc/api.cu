@@ -178,50 +178,57 @@ attn_status_t attn_full_fwd(const void *q, const void *k, const void *v, void *o
     return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
 }
 
+// Strides of the four tensors of a strided call: q (B, Hq, Nq), k and v
+// (B, Hkv, Nkv), o (B, Hq, Nq), each D-contiguous.  An extent-1 axis is never
+// stepped along, so its stride is replaced by a valid one; the output's rows
+// must be pairwise disjoint (sorted by stride, each axis' stride covers the
+// span of the axes below it, the innermost span being the D-element row).
+static attn_status_t parse_strides(const int64_t *const in[4], int B, int Hq, int Hkv, int Nq,
+                                   int Nkv, int D, attn_dtype_t dtype, TensorStrides st[4]) {
+    for (int i = 0; i < 4; ++i) {
+        if (!in[i]) return ATTN_ERR_INVALID_ARG;
+        const bool qo = i == 0 || i == 3;
+        const long long ext[3] = {B, qo ? Hq : Hkv, qo ? Nq : Nkv};
+        long long s[3];
+        for (int a = 0; a < 3; ++a) {
+            s[a] = ext[a] == 1 ? D : (long long)in[i][a];
+            if (!stride_ok(s[a], dtype)) return ATTN_ERR_INVALID_ARG;
+        }
+        st[i] = TensorStrides{s[0], s[1], s[2]};
+    }
+    const long long ext[3] = {B, Hq, Nq};
+    const long long s[3] = {st[3].b, st[3].h, st[3].n};
+    int ord[3] = {0, 1, 2};
+    for (int a = 0; a < 3; ++a)
+        for (int b = a + 1; b < 3; ++b)
+            if (s[ord[b]] < s[ord[a]]) { const int t = ord[a]; ord[a] = ord[b]; ord[b] = t; }
+    long long span = D;
+    for (int a = 0; a < 3; ++a) {
+        if (ext[ord[a]] == 1) continue;
+        if (s[ord[a]] < span) return ATTN_ERR_INVALID_ARG;
+        span = s[ord[a]] * ext[ord[a]];
+    }
+    return ATTN_OK;
+}
+
 attn_status_t attn_full_fwd_strided(const void *q, const void *k, const void *v, void *o,
                                     int B, int H, int Nq, int Nkv, int D,
                                     const int64_t q_strides[3], const int64_t k_strides[3],
                                     const int64_t v_strides[3], const int64_t o_strides[3],
                                     attn_dtype_t dtype, float scale, void *stream) {
-    if (!q || !k || !v || !o || !q_strides || !k_strides || !v_strides || !o_strides)
-        return ATTN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return ATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || Nq < 1 || Nkv < 1 || !valid_d(D) || !valid_dtype(dtype))
         return ATTN_ERR_INVALID_ARG;
     if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
     if (o == q || o == k || o == v) return ATTN_ERR_INVALID_ARG;
-    const int64_t *in[4] = {q_strides, k_strides, v_strides, o_strides};
+    const int64_t *const in[4] = {q_strides, k_strides, v_strides, o_strides};
     TensorStrides st[4];
-    for (int i = 0; i < 4; ++i) {
-        const long long ext[3] = {B, H, i == 0 || i == 3 ? Nq : Nkv};
-        long long s[3];
-        for (int a = 0; a < 3; ++a) {
-            // an extent-1 axis is never stepped along: any valid stride will do
-            s[a] = ext[a] == 1 ? D : (long long)in[i][a];
-            if (!stride_ok(s[a], dtype)) return ATTN_ERR_INVALID_ARG;
-        }
-        st[i] = TensorStrides{s[0], s[1], s[2]};
-    }
-    {
-        // o: the rows of D elements must be pairwise disjoint.  Sorted by
-        // stride, each axis' stride must be at least the span of the ones
-        // below it (the innermost span is the D-element row).
-        const long long ext[3] = {B, H, Nq};
-        const long long s[3] = {st[3].b, st[3].h, st[3].n};
-        int ord[3] = {0, 1, 2};
-        for (int a = 0; a < 3; ++a)
-            for (int b = a + 1; b < 3; ++b)
-                if (s[ord[b]] < s[ord[a]]) { const int t = ord[a]; ord[a] = ord[b]; ord[b] = t; }
-        long long span = D;
-        for (int a = 0; a < 3; ++a) {
-            if (ext[ord[a]] == 1) continue;
-            if (s[ord[a]] < span) return ATTN_ERR_INVALID_ARG;
-            span = s[ord[a]] * ext[ord[a]];
-        }
-    }
+    attn_status_t status = parse_strides(in, B, H, H, Nq, Nkv, D, dtype, st);
+    if (status != ATTN_OK) return status;
     Ctx c;
-    attn_status_t status = get_ctx(stream, &c);
+    status = get_ctx(stream, &c);
     if (status != ATTN_OK) return status;
     const float sc = resolve_scale(scale, D);
     if (half_dtype(dtype) && tc_full_supported(B, H, Nq, Nkv, D)) {
@@ -229,6 +236,33 @@ attn_status_t attn_full_fwd_strided(const void *q, const void *k, const void *v,
         if (status != ATTN_ERR_UNSUPPORTED) return status;
     }
     return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc, st);
+}
+
+attn_status_t attn_causal_gqa_fwd_strided(const void *q, const void *k, const void *v, void *o,
+                                          int B, int Hq, int Hkv, int N, int D,
+                                          const int64_t q_strides[3], const int64_t k_strides[3],
+                                          const int64_t v_strides[3], const int64_t o_strides[3],
+                                          attn_dtype_t dtype, float scale, void *stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0 || !valid_d(D) || !valid_dtype(dtype))
+        return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (o == q || o == k || o == v) return ATTN_ERR_INVALID_ARG;
+    const int64_t *const in[4] = {q_strides, k_strides, v_strides, o_strides};
+    TensorStrides st[4];
+    attn_status_t status = parse_strides(in, B, Hq, Hkv, N, N, D, dtype, st);
+    if (status != ATTN_OK) return status;
+    Ctx c;
+    status = get_ctx(stream, &c);
+    if (status != ATTN_OK) return status;
+    const float sc = resolve_scale(scale, D);
+    if (half_dtype(dtype) && tc_full_supported(B, Hq, N, N, D)) {
+        status = tc_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc, st);
+        if (status != ATTN_ERR_UNSUPPORTED) return status;
+    }
+    return simt_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc, st);
 }
 
 attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const void *v, void *o, int B,

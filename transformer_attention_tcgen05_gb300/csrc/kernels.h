@@ -79,10 +79,10 @@ attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *
 bool tc_full_supported(int B, int H, int Nq, int Nkv, int D);
 attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                             const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
-                            float scale);
+                            float scale, const TensorStrides *st = nullptr);
 attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                               const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
-                              float scale);
+                              float scale, const TensorStrides *st = nullptr);
 attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
                       void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
                       float scale);

@@ -327,7 +327,7 @@ attn_status_t simt_full(const Ctx &c, attn_dtype_t dt, const void *q, const void
 
 attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                               const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
-                              float scale) {
+                              float scale, const TensorStrides *st) {
     SimtParams p{};
     p.q = q; p.k = k; p.v = v; p.o = o;
     p.Nq = p.Nkv = N;
@@ -335,8 +335,10 @@ attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, cons
     p.causal = 1;
     p.group = Hq / Hkv;   // group 1: every head reads its own K/V
     p.H = Hq;
-    p.sq = p.so = dense(Hq, N, D);
-    p.sk = p.sv = dense(Hkv, N, D);
+    p.sq = st ? st[0] : dense(Hq, N, D);
+    p.sk = st ? st[1] : dense(Hkv, N, D);
+    p.sv = st ? st[2] : dense(Hkv, N, D);
+    p.so = st ? st[3] : dense(Hq, N, D);
     return dispatch<false>(c, dt, D, p, cdiv(N, kRows), B * Hq);
 }
 

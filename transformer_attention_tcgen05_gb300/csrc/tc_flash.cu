@@ -1144,14 +1144,17 @@ attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *
 
 attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                             const void *v, void *o, int B, int Hq, int Hkv, int N, int D,
-                            float scale) {
+                            float scale, const TensorStrides *st) {
     const bool f16 = dt == ATTN_F16;
     CUtensorMap tq, tk, tv;
-    const TensorStrides sq{(long long)Hq * N * D, (long long)N * D, D};
-    const TensorStrides skv{(long long)Hkv * N * D, (long long)N * D, D};
-    if (!make_tmap4(&tq, q, D, N, Hq, B, sq, f16) || !make_tmap4(&tk, k, D, N, Hkv, B, skv, f16) ||
-        !make_tmap4(&tv, v, D, N, Hkv, B, skv, f16))
-        return ATTN_ERR_CUDA;
+    const TensorStrides dq{(long long)Hq * N * D, (long long)N * D, D};
+    const TensorStrides dkv{(long long)Hkv * N * D, (long long)N * D, D};
+    const TensorStrides sq = st ? st[0] : dq, sk = st ? st[1] : dkv, sv = st ? st[2] : dkv,
+                        so = st ? st[3] : dq;
+    // a layout the tensor-map encoder refuses goes to the strided SIMT kernel
+    if (!make_tmap4(&tq, q, D, N, Hq, B, sq, f16) || !make_tmap4(&tk, k, D, N, Hkv, B, sk, f16) ||
+        !make_tmap4(&tv, v, D, N, Hkv, B, sv, f16))
+        return ATTN_ERR_UNSUPPORTED;
     TcParams p{};
     p.Nq = N;
     p.Nkv = N;
@@ -1162,7 +1165,7 @@ attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const 
     p.Hkv = Hkv;
     p.group = Hq / Hkv;
     p.H = Hq;
-    p.o_sb = sq.b; p.o_sh = sq.h; p.o_sn = sq.n;
+    p.o_sb = so.b; p.o_sh = so.h; p.o_sn = so.n;
     const dim3 grid(cdiv(N, kNQ * kBM), B * Hq);
     if (f16)
         return D == 128 ? launch_tc<128, false, true, 0, true>(c, tq, tk, tv, p, grid)

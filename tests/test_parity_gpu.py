@@ -329,6 +329,32 @@ def test_tc_full_sharp_rows_rescale(ta):
     assert_close(to_host64(o), ref, "bf16", "tc sharp")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("growth", [14.0, 40.0])
+@pytest.mark.parametrize("D", [64, 128])
+def test_tc_scores_growing_from_tile_to_tile(ta, dtype, growth, D):
+    """Each key tile's scores exceed the previous tile's by about `growth` (in
+    log2 units).  After the first tile the kernel exponentiates against the
+    running maximum as it stands: a growth of 40 overflows the tile's row sum
+    every time (the tile is redone with its own maximum and O rescaled); a
+    growth of 14 keeps P up to ~2^14 in bf16 but passes f16's bound (redo)."""
+    from workloads import bf16_round
+    rng = np.random.Generator(np.random.PCG64(7700 + D + int(growth)))
+    H, Nq, Nkv = 2, 256, 5 * 128
+    u = np.where(rng.random(D) < 0.5, -1.0, 1.0).astype(np.float32)
+    alpha = np.repeat(np.arange(5, dtype=np.float32), 128) * growth / (1.4426950408889634 * math.sqrt(D))
+    q = u + 0.25 * rng.standard_normal((1, H, Nq, D), dtype=np.float32)
+    k = alpha[None, None, :, None] * u + 0.5 * rng.standard_normal((1, H, Nkv, D), dtype=np.float32)
+    v = rng.standard_normal((1, H, Nkv, D), dtype=np.float32)
+    rnd = bf16_round if dtype == "bf16" else (lambda a: a.astype(np.float16))
+    q, k, v = rnd(q), rnd(k), rnd(v)
+    with launched(ta, "tc_flash"):
+        o = ta.full_fwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype))
+    ref = oracle.full_fwd(to_f64(q, dtype), to_f64(k, dtype), to_f64(v, dtype))
+    assert_close(to_host64(o), ref, dtype, f"growing scores {dtype} D={D} growth={growth}")
+    assert ta.device_status() == 0
+
+
 def test_flux_joint_full_size_sampled_rows(ta):
     import torch
     w = WORKLOADS["flux_joint"]

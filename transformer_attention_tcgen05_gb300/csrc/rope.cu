@@ -88,20 +88,33 @@ __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p, int heads
     const int h0 = blockIdx.y * heads_per_cta, h1 = imin(h0 + heads_per_cta, p.BH);
     const T *src[2] = {static_cast<const T *>(p.q), static_cast<const T *>(p.k)};
     T *dst[2] = {static_cast<T *>(p.qr), static_cast<T *>(p.kr)};
-    for (int h = h0; h < h1; ++h) {
-        const size_t off = (size_t(h) * p.N + t) * p.D + g * 8;
+    // kBatch heads at a time, every load of the batch issued before the first
+    // store, so 2 * kBatch 16-byte loads per thread are in flight at once
+    constexpr int kBatch = 4;
+    for (int hb = h0; hb < h1; hb += kBatch) {
+        Vec8<T> x[2][kBatch];
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-            Vec8<T> x;
-            x.load(src[w] + off);
-            Vec8<T> y = x;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x0 = x.get(2 * i), x1 = x.get(2 * i + 1);
-                y.set2(i, x0 * cs[i] - x1 * sn[i], x0 * sn[i] + x1 * cs[i]);
+        for (int b = 0; b < kBatch; ++b)
+            if (hb + b < h1) {
+                const size_t off = (size_t(hb + b) * p.N + t) * p.D + g * 8;
+                x[0][b].load(src[0] + off);
+                x[1][b].load(src[1] + off);
             }
-            y.store(dst[w] + off);
-        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+            if (hb + b < h1) {
+                const size_t off = (size_t(hb + b) * p.N + t) * p.D + g * 8;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    Vec8<T> y = x[w][b];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float x0 = x[w][b].get(2 * i), x1 = x[w][b].get(2 * i + 1);
+                        y.set2(i, x0 * cs[i] - x1 * sn[i], x0 * sn[i] + x1 * cs[i]);
+                    }
+                    y.store(dst[w] + off);
+                }
+            }
     }
 }
 

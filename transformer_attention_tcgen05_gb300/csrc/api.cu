@@ -173,8 +173,11 @@ attn_status_t attn_full_fwd(const void *q, const void *k, const void *v, void *o
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (half_dtype(dtype) && tc_full_supported(B, H, Nq, Nkv, D))
-        return tc_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
+    if (half_dtype(dtype) && tc_full_supported(B, H, Nq, Nkv, D)) {
+        // a layout the tensor-map encoder refuses falls through to the SIMT kernel
+        st = tc_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
+        if (st != ATTN_ERR_UNSUPPORTED) return st;
+    }
     return simt_full(c, dtype, q, k, v, o, B, H, Nq, Nkv, D, sc);
 }
 
@@ -279,8 +282,10 @@ attn_status_t attn_causal_gqa_fwd(const void *q, const void *k, const void *v, v
     attn_status_t st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (half_dtype(dtype) && tc_full_supported(B, Hq, N, N, D))
-        return tc_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc);
+    if (half_dtype(dtype) && tc_full_supported(B, Hq, N, N, D)) {
+        st = tc_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc);
+        if (st != ATTN_ERR_UNSUPPORTED) return st;
+    }
     return simt_causal_gqa(c, dtype, q, k, v, o, B, Hq, Hkv, N, D, sc);
 }
 
@@ -319,8 +324,10 @@ attn_status_t attn_rope_joint_fwd(const void *q, const void *k, const void *v, v
     st = rope_rotate_qk(c, dtype, q, k, qr, kr, B * H, N, D, pos, axes_dim, theta);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (half_dtype(dtype) && tc_full_supported(B, H, N, N, D))
-        return tc_full(c, dtype, qr, kr, v, o, B, H, N, N, D, sc);
+    if (half_dtype(dtype) && tc_full_supported(B, H, N, N, D)) {
+        st = tc_full(c, dtype, qr, kr, v, o, B, H, N, N, D, sc);
+        if (st != ATTN_ERR_UNSUPPORTED) return st;
+    }
     return simt_full(c, dtype, qr, kr, v, o, B, H, N, N, D, sc);
 }
 

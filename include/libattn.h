@@ -286,6 +286,26 @@ ATTN_API attn_status_t attn_na3d_fwd(const void *q, const void *k, const void *v
                             void *stream);
 
 /*
+ * 3D neighborhood attention on strided views: the operation of
+ * attn_na3d_fwd with q, k, v and o addressed through element strides of
+ * (batch, head, token) as in attn_full_fwd_strided (D contiguous, every
+ * stride a multiple of 16 bytes, extent-1 axes' strides ignored, o's rows
+ * disjoint); tokens keep their row-major (t, h, w) order at a uniform token
+ * stride, so a [B, T*Hg*W, heads, D] projection is read in place.  A
+ * non-contiguous layout runs on the exact SIMT kernel; contiguous strides
+ * take the tensor-core kernel of attn_na3d_fwd.
+ * Passage: as attn_na3d_fwd; the layout is an addressing choice with no
+ * counterpart in the pages.
+ */
+ATTN_API attn_status_t attn_na3d_fwd_strided(const void *q, const void *k, const void *v, void *o,
+                                            int B, int heads, int T, int Hg, int W, int D,
+                                            const int kernel[3], const int64_t q_strides[3],
+                                            const int64_t k_strides[3],
+                                            const int64_t v_strides[3],
+                                            const int64_t o_strides[3], attn_dtype_t dtype,
+                                            float scale, void *stream);
+
+/*
  * Window starts as the neighborhood kernels compute them (same device
  * function), for testing: starts = DEVICE int32 [T*Hg*W, 3], the (t, h, w)
  * start of each query's window.  Same validation as attn_na3d_fwd.

@@ -124,6 +124,23 @@ def test_causal_strided_validation(L):
     assert call(qs=None) == 1
 
 
+def test_na3d_strided_validation(L):
+    """Only layouts that must be refused are passed: the pointers are fake."""
+    L.attn_na3d_fwd_strided.restype = ctypes.c_int
+    S = ctypes.c_int64 * 3
+    B, H, T, Hg, W, D = 1, 2, 2, 4, 4, 64
+    N = T * Hg * W
+    ok = S(H * N * D, N * D, D)
+    kern = (ctypes.c_int * 3)(3, 3, 3)
+
+    def call(qs=ok, os_=ok, k=kern):
+        return L.attn_na3d_fwd_strided(FAKE, FAKE, FAKE, ctypes.c_void_p(0x20000), B, H, T, Hg, W,
+                                       D, k, qs, ok, ok, os_, 1, ctypes.c_float(0.0), None)
+    assert call(qs=S(H * N * D, N * D, D + 4)) == 1              # token stride 136 bytes
+    assert call(os_=S(H * N * D, D, H * D // 2)) == 1            # output tokens overlap
+    assert call(k=(ctypes.c_int * 3)(3, 4, 3)) == 1              # even window
+
+
 def test_na3d_validation(L):
     L.attn_na3d_fwd.restype = ctypes.c_int
     o = ctypes.c_void_p(0x20000)

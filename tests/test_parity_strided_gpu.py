@@ -116,3 +116,38 @@ def test_causal_gqa_llama_projection_layout(ta, dt, D, family):
     assert_close(to_host64(o), ref, dt, f"{dt} causal strided D={D}")
     dense = ta.causal_gqa_fwd(q.contiguous(), k.contiguous(), v.contiguous())
     assert torch.equal(dense, o), "strided causal result differs from the contiguous one"
+
+
+@pytest.mark.parametrize("dt,B", [("bf16", 1), ("f16", 1), ("bf16", 2)])
+def test_na3d_projection_layout(ta, dt, B):
+    """Neighborhood attention reading q, k, v from [B, T*Hg*W, heads, D]
+    projections and writing o into the same layout: a non-contiguous layout
+    runs on the exact SIMT kernel, which addresses every tensor through its
+    strides."""
+    import torch
+    grid, kernel, H, D = ((3, 20, 24), (3, 5, 7), 2, 64) if B == 1 else ((2, 8, 12), (3, 3, 5), 2, 64)
+    N = grid[0] * grid[1] * grid[2]
+    g = np.random.default_rng(9980 + B + len(dt))
+    qb, kb, vb = (_dev(g.standard_normal((B, N, H, D), dtype=np.float32), dt) for _ in range(3))
+    ob = torch.full_like(qb, 5.0)
+    q, k, v, o = (t.transpose(1, 2) for t in (qb, kb, vb, ob))
+    n0 = ta.launch_count("simt")
+    ta.na3d_fwd_strided(q, k, v, grid, kernel, o=o)
+    assert ta.launch_count("simt") > n0, "simt did not launch"
+    assert ta.device_status() == 0
+    ref = oracle.na3d_fwd(to_host64(q), to_host64(k), to_host64(v), grid, kernel)
+    assert_close(to_host64(o), ref, dt, f"{dt} na3d strided B={B}")
+
+
+def test_na3d_strided_entry_with_dense_strides_takes_the_tensor_cores(ta):
+    """Contiguous tensors passed through the strided entry run the tensor-core
+    kernel and give exactly the contiguous entry's result."""
+    import torch
+    grid, kernel, H, D = (3, 20, 24), (3, 5, 7), 2, 64
+    N = grid[0] * grid[1] * grid[2]
+    g = np.random.default_rng(9990)
+    q, k, v = (_dev(g.standard_normal((1, H, N, D), dtype=np.float32), "bf16") for _ in range(3))
+    n0 = ta.launch_count("tc_na")
+    o = ta.na3d_fwd_strided(q, k, v, grid, kernel)
+    assert ta.launch_count("tc_na") > n0, "tc_na did not launch"
+    assert torch.equal(o, ta.na3d_fwd(q, k, v, grid, kernel))

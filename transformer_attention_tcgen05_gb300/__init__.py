@@ -24,7 +24,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "AttnError", "lib", "full_fwd", "full_fwd_strided", "causal_gqa_fwd_strided", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
+    "AttnError", "lib", "full_fwd", "full_fwd_strided", "causal_gqa_fwd_strided", "na3d_fwd_strided", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
     "na3d_window_starts", "kv_append", "kv_append_ring", "decode_gqa_ring", "decode_workspace_bytes", "rope_joint_workspace_bytes",
     "device_status", "launch_count", "version", "FAMILIES", "LIB_PATH",
 ]
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.attn_full_fwd_strided.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                             _st, _st, _st, _st, _i, _f, _vp]
         L.attn_causal_gqa_fwd_strided.argtypes = L.attn_full_fwd_strided.argtypes
+        L.attn_na3d_fwd_strided.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                            ctypes.POINTER(_i), _st, _st, _st, _st, _i, _f, _vp]
         L.attn_status_string.argtypes = [_i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_device_status.argtypes = [_vp]
@@ -87,7 +89,7 @@ def lib() -> ctypes.CDLL:
         for name in ("attn_full_fwd", "attn_rope_joint_fwd", "attn_decode_gqa", "attn_na3d_fwd",
                      "attn_na3d_window_starts", "attn_device_status", "attn_kv_append",
                      "attn_causal_gqa_fwd", "attn_full_fwd_strided", "attn_kv_append_ring",
-                     "attn_causal_gqa_fwd_strided",
+                     "attn_causal_gqa_fwd_strided", "attn_na3d_fwd_strided",
                      "attn_decode_gqa_ring"):
             getattr(L, name).restype = _i
         _lib = L
@@ -317,6 +319,29 @@ def na3d_fwd(q, k, v, grid, kernel, o=None, scale=None):
                                    B, Hh, T, Hg, W, D, _ints(kernel, 3), _dtype(q),
                                    _scale(scale), _stream(dev)),
                "attn_na3d_fwd")
+    return o
+
+
+def na3d_fwd_strided(q, k, v, grid, kernel, o=None, scale=None):
+    """3D neighborhood attention on strided [B, heads, T*Hg*W, D] views (D
+    contiguous, tokens at a uniform stride), e.g. q.transpose(1, 2) of a
+    [B, T*Hg*W, heads, D] projection. o defaults to a new contiguous tensor."""
+    dev = _cuda(q, k, v, strided=True)
+    B, Hh, N, D = q.shape
+    T, Hg, W = (int(x) for x in grid)
+    if N != T * Hg * W or k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype \
+            or v.dtype != q.dtype:
+        raise ValueError("q/k/v must be [B, heads, T*Hg*W, D] with one dtype")
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if o is None else o
+    _cuda(q, o, strided=True)
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must be [B, heads, T*Hg*W, D] with q's dtype")
+    with torch.cuda.device(dev):
+        _check(lib().attn_na3d_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           B, Hh, T, Hg, W, D, _ints(kernel, 3), _strides(q),
+                                           _strides(k), _strides(v), _strides(o), _dtype(q),
+                                           _scale(scale), _stream(dev)),
+               "attn_na3d_fwd_strided")
     return o
 
 

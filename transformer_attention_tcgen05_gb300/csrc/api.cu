@@ -431,9 +431,50 @@ attn_status_t attn_na3d_fwd(const void *q, const void *k, const void *v, void *o
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
     if (half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel) &&
-        (dtype == ATTN_BF16 || tc_na3d_f16_scale_ok(sc)))
-        return tc_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
+        (dtype == ATTN_BF16 || tc_na3d_f16_scale_ok(sc))) {
+        st = tc_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
+        if (st != ATTN_ERR_UNSUPPORTED) return st;
+    }
     return simt_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
+}
+
+attn_status_t attn_na3d_fwd_strided(const void *q, const void *k, const void *v, void *o, int B,
+                                    int heads, int T, int Hg, int W, int D, const int kernel[3],
+                                    const int64_t q_strides[3], const int64_t k_strides[3],
+                                    const int64_t v_strides[3], const int64_t o_strides[3],
+                                    attn_dtype_t dtype, float scale, void *stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_na(T, Hg, W, kernel);
+    if (st != ATTN_OK) return st;
+    if (B < 1 || heads < 1 || !valid_d(D) || !valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * heads > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (o == q || o == k || o == v) return ATTN_ERR_INVALID_ARG;
+    const int N = T * Hg * W;
+    const int64_t *const in[4] = {q_strides, k_strides, v_strides, o_strides};
+    TensorStrides sts[4];
+    st = parse_strides(in, B, heads, heads, N, N, D, dtype, sts);
+    if (st != ATTN_OK) return st;
+    Ctx c;
+    st = get_ctx(stream, &c);
+    if (st != ATTN_OK) return st;
+    const float sc = resolve_scale(scale, D);
+    // The tensor-core kernel addresses the contiguous layout only (its output
+    // stores stay contiguous so that the dense path pays nothing for views);
+    // any other layout runs on the exact SIMT kernel, which takes the strides.
+    const long long n = N;
+    bool dense = true;
+    for (int i = 0; i < 4; ++i) {
+        const TensorStrides d{(B == 1 ? D : heads * n * D), (heads == 1 ? D : n * D), D};
+        dense = dense && sts[i].b == d.b && sts[i].h == d.h && sts[i].n == d.n;
+    }
+    if (dense && half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel) &&
+        (dtype == ATTN_BF16 || tc_na3d_f16_scale_ok(sc))) {
+        st = tc_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
+        if (st != ATTN_ERR_UNSUPPORTED) return st;
+    }
+    return simt_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc, sts);
 }
 
 attn_status_t attn_na3d_window_starts(int T, int Hg, int W, const int kernel[3], int32_t *starts,

@@ -49,7 +49,7 @@ attn_status_t simt_full(const Ctx &c, attn_dtype_t dt, const void *q, const void
                         float scale, const TensorStrides *st = nullptr);
 attn_status_t simt_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                         const void *v, void *o, int B, int H, int T, int Hg, int W, int D,
-                        const int kernel[3], float scale);
+                        const int kernel[3], float scale, const TensorStrides *st = nullptr);
 attn_status_t na_starts(const Ctx &c, int T, int Hg, int W, const int kernel[3],
                         int32_t *starts);
 

@@ -344,14 +344,17 @@ attn_status_t simt_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, cons
 
 attn_status_t simt_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
                         const void *v, void *o, int B, int H, int T, int Hg, int W, int D,
-                        const int kernel[3], float scale) {
+                        const int kernel[3], float scale, const TensorStrides *st) {
     SimtParams p{};
     p.q = q; p.k = k; p.v = v; p.o = o;
     p.Nq = p.Nkv = T * Hg * W;
     p.qscale = scale * kLog2e;
     p.group = 1;
     p.H = H;
-    p.sq = p.sk = p.sv = p.so = dense(H, p.Nq, D);
+    p.sq = st ? st[0] : dense(H, p.Nq, D);
+    p.sk = st ? st[1] : dense(H, p.Nq, D);
+    p.sv = st ? st[2] : dense(H, p.Nq, D);
+    p.so = st ? st[3] : dense(H, p.Nq, D);
     p.T = T; p.Hg = Hg; p.W = W;
     p.kt = kernel[0]; p.kh = kernel[1]; p.kw = kernel[2];
     p.et = imin(kernel[0], T); p.eh = imin(kernel[1], Hg); p.ew = imin(kernel[2], W);

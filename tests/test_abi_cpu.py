@@ -170,6 +170,29 @@ def test_decode_validation(L):
                              ctypes.c_void_p(0x40010), 1 << 20, None) == 1
 
 
+def test_ring_entries_validate_like_their_linear_forms(L):
+    """The ring decode and append entries share the linear ones' host checks
+    (only refusals are passed: the pointers are fake)."""
+    L.attn_decode_gqa_ring.restype = ctypes.c_int
+    L.attn_kv_append_ring.restype = ctypes.c_int
+    o = ctypes.c_void_p(0x20000)
+    ws = ctypes.c_void_p(0x40000)
+    f = ctypes.c_float(0.0)
+    assert L.attn_decode_gqa_ring(FAKE, FAKE, FAKE, FAKE, o, 1, 6, 4, 64, 128, 1, f, ws, 1 << 20,
+                                  None) == 1                      # Hq % Hkv != 0
+    assert L.attn_decode_gqa_ring(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 0, f, ws, 1 << 20,
+                                  None) == 2                      # fp32 cache
+    assert L.attn_decode_gqa_ring(FAKE, FAKE, FAKE, FAKE, o, 1, 8, 2, 64, 128, 1, f, ws, 16,
+                                  None) == 3                      # workspace too small
+    assert L.attn_decode_gqa_ring(FAKE, FAKE, FAKE, None, o, 1, 8, 2, 64, 128, 1, f, ws, 1 << 20,
+                                  None) == 1                      # no seq_len
+    kc, vc = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x30000)
+    new = ctypes.c_void_p(0x50000)
+    assert L.attn_kv_append_ring(kc, kc, new, new, FAKE, 1, 2, 64, 64, 1, 1, None) == 1  # k is v
+    assert L.attn_kv_append_ring(kc, vc, new, new, FAKE, 1, 2, 64, 48, 1, 1, None) == 1  # D = 48
+    assert L.attn_kv_append_ring(kc, vc, new, new, None, 1, 2, 64, 64, 1, 1, None) == 1  # no seq_len
+
+
 def test_rope_validation(L):
     L.attn_rope_joint_fwd.restype = ctypes.c_int
     o = ctypes.c_void_p(0x20000)

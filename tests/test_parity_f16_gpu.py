@@ -93,16 +93,17 @@ def test_f16_na3d(ta, grid, kernel, D, family):
     assert ta.device_status() == 0
 
 
-def test_f16_na3d_small_scale_takes_the_simt_kernel(ta):
-    """With a tiny scale the tensor-core kernel's window penalty would not be
-    representable in f16; the call must still be right (exact SIMT kernel)."""
+def test_f16_na3d_small_scale(ta):
+    """A tiny scale: the f16 neighborhood kernel tests h and w per key in the
+    softmax (no penalty that f16 would have to hold), so it stays on the
+    tensor cores and must still be right."""
     grid, kernel = (3, 20, 24), (3, 5, 7)
     w = WORKLOADS["na3d_9x64x64_k11_bf16"].with_(dtype="f16", grid=grid, kernel=kernel, D=64, H=1,
                                                  N=grid[0] * grid[1] * grid[2], seed=9450)
     x, dev, f64 = _io(w)
-    n0 = ta.launch_count("simt")
+    n0 = ta.launch_count("tc_na")
     o = ta.na3d_fwd(*dev, grid, kernel, scale=1e-4)
-    _ran(ta, "simt", n0)
+    _ran(ta, "tc_na", n0)
     ref = oracle.na3d_fwd(*f64, grid, kernel, scale=1e-4)
     assert_close(to_host64(o), ref, "f16", "f16 na3d tiny scale")
 

@@ -430,8 +430,7 @@ attn_status_t attn_na3d_fwd(const void *q, const void *k, const void *v, void *o
     st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     const float sc = resolve_scale(scale, D);
-    if (half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel) &&
-        (dtype == ATTN_BF16 || tc_na3d_f16_scale_ok(sc))) {
+    if (half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel)) {
         st = tc_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
         if (st != ATTN_ERR_UNSUPPORTED) return st;
     }
@@ -469,8 +468,7 @@ attn_status_t attn_na3d_fwd_strided(const void *q, const void *k, const void *v,
         const TensorStrides d{(B == 1 ? D : heads * n * D), (heads == 1 ? D : n * D), D};
         dense = dense && sts[i].b == d.b && sts[i].h == d.h && sts[i].n == d.n;
     }
-    if (dense && half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel) &&
-        (dtype == ATTN_BF16 || tc_na3d_f16_scale_ok(sc))) {
+    if (dense && half_dtype(dtype) && tc_na3d_supported(B, heads, T, Hg, W, D, kernel)) {
         st = tc_na3d(c, dtype, q, k, v, o, B, heads, T, Hg, W, D, kernel, sc);
         if (st != ATTN_ERR_UNSUPPORTED) return st;
     }

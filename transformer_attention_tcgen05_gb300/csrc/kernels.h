@@ -87,9 +87,6 @@ attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *
                       void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
                       float scale);
 bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]);
-// The f16 neighborhood kernel needs its window penalty (a power of two with
-// penalty * scale * log2(e) >= 300) to be representable in f16.
-bool tc_na3d_f16_scale_ok(float scale);
 // One 128 x 128 tile through both tcgen05 MMA forms (testing).
 attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,
                           const void *P, float *S, float *O, int D);

@@ -45,10 +45,13 @@
 // the output's strides, so strided views are read and written in place.
 // Neighborhood attention: the two query tiles are two 3D boxes adjacent in w;
 // each streams the union of its queries' clamped windows as (1, KH, 16)
-// (t, h, w) key sub-boxes loaded by 5D TMA.  The h and w window tests enter S
-// as a large negative penalty through one extra 16-channel MMA k-step (one-hot
-// query offsets against per-sub-box key penalty tiles); a key frame outside a
-// row's t window is dropped in the softmax (P = 0).
+// (t, h, w) key sub-boxes loaded by 5D TMA.  bf16: the h and w window tests
+// enter S as a penalty of -2^100 per violated axis through one extra
+// 16-channel MMA k-step (one-hot query offsets against per-sub-box key penalty
+// tiles), which drops every masked key exactly (P = 0) for any scores below
+// 2^98 in magnitude; f16, whose range cannot hold such a penalty, tests h and
+// w per key in the softmax instead.  A key frame outside a row's t window is
+// dropped in the softmax (P = 0).
 //
 // All spin-waits are bounded (1 s); on a timeout the CTA raises the device
 // error word, drains what it issued, frees TMEM and exits.
@@ -135,7 +138,7 @@ struct TcParams {
     int nbh, nbw2;           // boxes along h; box pairs along w
     int nbw;                 // boxes along w
     int KH;                  // key sub-box height (keys per tile = KH * 16)
-    float penalty;           // bf16-exact power of two; penalty * c_log2 >= 300
+    float penalty;           // bf16: power of two >= 2^100 with penalty * c_log2 >= 300
     // causal grouped-query prefill
     int Hq, Hkv, group;
     // full / causal: q, k, v are 4D tensor maps {D, N, heads, B}; o is written
@@ -294,6 +297,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     make_uint4(0, 0, 0, 0);
             }
         }
+    }
+    if constexpr (NA && !F16) {
+        const int rows = p.bt * p.bh * p.bw;
         // one-hot window-offset channels of every query row: channel dh, then
         // bh + dw (rows past the box: all zero)
         for (int i = threadIdx.x; i < kNQ * kBM * 2; i += C::NT) {
@@ -467,7 +473,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                     ptx::mma_ss(tmem + C::TM_S + t * kBN, ptx::desc_join(a0 + oa, HI128),
                                 ptx::desc_join(b0 + ob, HI128), id_qk, kk > 0);
                 }
-                if constexpr (NA) {
+                if constexpr (NA && !F16) {
                     // + window penalties: one more k-step over the 16 extra channels;
                     // QK_t(j) uses penalty tile j mod (h chunks x w chunks)
                     const uint32_t a = dqx0 + uint32_t((t * kBM * C::X_ROW) >> 4);
@@ -580,7 +586,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         const float cl = p.c_log2;
 
         // query of this row (neighborhood path) and its window
-        int qt = 0, qh = 0, qw = 0, wst = 0;
+        int qt = 0, qh = 0, qw = 0, wst = 0, wsh = 0, wsw = 0;
         bool qvalid;
         const NaTile gt = pick(g, t);           // this warp's tile, in registers
         const int nt = pick(n_t, t);
@@ -591,6 +597,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             qw = gt.w0 + dw;
             qvalid = nt > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
             wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
+            if constexpr (F16) {
+                wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
+                wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
+            }
         } else {
             qvalid = q0 + t * kBM + row < p.Nq;
         }
@@ -614,8 +624,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             //      computing them: the MMAs run anyway and the test costs issue
             //      slots on the critical path.)
             bool t_ok = true;
+            int kh0 = 0, kw0 = 0;                // key sub-box origin along h and w
             if constexpr (NA) {
                 const int kt_ = gt.u0t + tc;
+                kh0 = gt.u0h + hc * (BNt / kKW);
+                kw0 = gt.u0w + wc * kKW;
                 if (++wc == gt.nwc) {
                     wc = 0;
                     if (++hc == gt.nhc) {
@@ -648,6 +661,23 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 #pragma unroll
                         for (int i = 0; i < 16; ++i) sv[gq * 16 + i] = -INFINITY;
                     }
+                if constexpr (F16) {
+                    // f16: the h and w window tests per key.  Key e of the
+                    // (1, KH, 16) sub-box sits at h = kh0 + e / 16, w = kw0 + e % 16;
+                    // wm / hm hold the in-window w columns / h rows of this row.
+                    const int lw = wsw - kw0, lh = wsh - kh0;
+                    const int aw = imax(lw, 0), bw = imin(lw + p.ew, kKW);
+                    const int ah = imax(lh, 0), bh_ = imin(lh + p.eh, kBN / kKW);
+                    const uint32_t wm = aw < bw ? ((1u << bw) - 1u) & ~((1u << aw) - 1u) : 0u;
+                    const uint32_t hm = ah < bh_ ? ((1u << bh_) - 1u) & ~((1u << ah) - 1u) : 0u;
+#pragma unroll
+                    for (int gq = 0; gq < kBN / 16; ++gq) {
+                        const bool hin = (hm >> gq) & 1u;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (!hin || !((wm >> i) & 1u)) sv[gq * 16 + i] = -INFINITY;
+                    }
+                }
             } else {
                 int valid = p.Nkv - j * kBN;           // keys of this tile inside the sequence
                 if constexpr (CAUSAL) {
@@ -1179,10 +1209,6 @@ bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kern
            cached_plan(T, Hg, W, kernel).ok;
 }
 
-bool tc_na3d_f16_scale_ok(float scale) {
-    return exp2f(fminf(100.f, fmaxf(0.f, ceilf(log2f(300.f / (scale * kLog2e)))))) <= 32768.f;
-}
-
 attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
                       void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
                       float scale) {
@@ -1199,11 +1225,17 @@ attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *
         !make_tmap(&tv, v, 5, dims, kbox, f16))
         return ATTN_ERR_CUDA;
     p.c_log2 = scale * kLog2e;
-    // penalty per violated axis: a power of two (exact in bf16; in f16 up to
-    // 2^15) with penalty * scale * log2(e) >= 300, so 2^(x - m) underflows to
-    // exactly 0
-    p.penalty = exp2f(fminf(100.f, fmaxf(0.f, ceilf(log2f(300.f / p.c_log2)))));
-    if (f16 && p.penalty > 32768.f) return ATTN_ERR_UNSUPPORTED;   // scale too small for f16
+    // bf16 penalty per violated axis: a power of two (exact in bf16), at least
+    // 2^100 and with penalty * scale * log2(e) >= 300.  A masked key's score is
+    // then raw - penalty (or - 2 penalty) <= -2^99 whenever |raw| < 2^98, so
+    // 2^(x - m) underflows to exactly 0 however far its raw score lies above
+    // the row's in-window scores; up to 2^125 two penalties still fit fp32.
+    // (f16 masks in the softmax and does not use it.)
+    {
+        const int e = imax(100, int(ceilf(log2f(300.f / p.c_log2))));
+        if (!f16 && e > 125) return ATTN_ERR_UNSUPPORTED;   // scale below ~1e-28
+        p.penalty = ldexpf(1.f, imin(e, 125));
+    }
     p.o = o;
     p.err = c.err;
     p.T = T; p.Hg = Hg; p.W = W;

@@ -210,6 +210,9 @@ ATTN_API size_t attn_decode_gqa_workspace_bytes(int B, int Hq, int Hkv, int Lmax
  *     the GPU (other streams, other host threads) race: serialise them.
  *   - The first call on a device looks up the array's device address; make
  *     that first call outside any stream capture.
+ *   - `stream` must belong to the current device (the array used is the
+ *     current device's); a stream of another device returns
+ *     ATTN_ERR_INVALID_ARG and launches nothing.
  */
 ATTN_API attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_cache,
                                                const void *v_cache, const int32_t *seq_len,
@@ -328,6 +331,20 @@ ATTN_API attn_status_t attn_debug_tc_tile(const void *q, const void *k, const vo
                                           const void *P, float *S, float *O, int D,
                                           void *stream);
 
+/*
+ * Bounded-wait check (testing): launches one thread that waits on a
+ * shared-memory barrier nothing ever completes, with a wait limit of
+ * limit_ns nanoseconds (1000 .. 1000000000; outside that range
+ * ATTN_ERR_INVALID_ARG and nothing launches).  The wait runs out, sets the
+ * device error word to the timeout code and the thread returns, so the
+ * next attn_device_status() on this stream returns ATTN_ERR_TIMEOUT (and
+ * clears the word) with the context still usable.  Every spin-wait in the
+ * attention kernels is this same bounded wait with a limit of one second.
+ * No counterpart on the pages: it exercises the library's failure reporting
+ * without faulting or hanging a GPU.
+ */
+ATTN_API attn_status_t attn_debug_wait_test(uint64_t limit_ns, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 ATTN_API const char *attn_status_string(attn_status_t status);
 
@@ -343,7 +360,7 @@ ATTN_API attn_status_t attn_device_status(void *stream);
  * family, for tests that must prove the path under test really ran.
  * ids: 0 = fp32/SIMT flash, 1 = tcgen05 flash, 2 = decode split-KV,
  *      3 = RoPE prologue, 4 = window-start export, 5 = tcgen05 neighborhood,
- *      6 = KV-cache append.
+ *      6 = KV-cache append, 7 = bounded-wait check.
  * Returns 0 for an unknown id.
  */
 ATTN_API uint64_t attn_launch_count(int kernel_family);

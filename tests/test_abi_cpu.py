@@ -210,6 +210,13 @@ def test_rope_validation(L):
                                  ctypes.c_float(1e4), 1, f, ws, 64, None) == 3         # workspace
 
 
+def test_wait_test_limit_range_checked_on_the_host(L):
+    L.attn_debug_wait_test.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+    L.attn_debug_wait_test.restype = ctypes.c_int
+    assert L.attn_debug_wait_test(999, None) == 1              # below 1 us
+    assert L.attn_debug_wait_test(1_000_000_001, None) == 1    # above the 1 s wait limit
+
+
 def test_launch_counter_unknown_family(L):
     L.attn_launch_count.restype = ctypes.c_uint64
     assert L.attn_launch_count(99) == 0

@@ -5,8 +5,11 @@ workspace (a host whose allocator owns all device memory and passes plugins
 only tensors, or a decode loop that must not call cudaMalloc between tokens).
 It keeps its split partials in a fixed array inside the library, so this test
 calls it twice in a row through the C ABI -- the second call sees whatever the
-first left in that array -- and checks both outputs against attn_decode_gqa
-with a caller-owned workspace, within the bf16 tolerance of the parity tests.
+first left in that array -- and checks both outputs against the fp64 oracle
+and against attn_decode_gqa with a caller-owned workspace, within the bf16
+tolerance of the parity tests.  The cases cover the decode workload, ragged
+lengths, a single split per (batch, kv-head) and a problem whose partials fill
+the array to within 1% of its 4 MiB.
 The file sorts last so a failure here does not hide the other GPU tests.
 """
 import ctypes
@@ -14,8 +17,9 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from tests.util import assert_close, to_dev, to_host64
-from workloads import WORKLOADS, make_inputs
+from workloads import WORKLOADS, make_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -29,9 +33,16 @@ def _noalloc(ta):
     return fn
 
 
+_NEAR_LIMIT_LENS = tuple(int(x) for x in np.random.default_rng(7902).integers(1, 65, size=125))
+
+
 @pytest.mark.parametrize("name,overrides", [
     ("gqa_decode", {}),
     ("gqa_decode", dict(B=3, H=12, Hkv=4, D=64, Lmax=777, seq_len=(1, 777, 300), seed=7900)),
+    # Lmax below 512 rows: one split per (batch, kv-head)
+    ("gqa_decode", dict(B=2, H=8, Hkv=2, D=128, Lmax=200, seq_len=(200, 37), seed=7901)),
+    # 1000 (batch, kv-head) pairs x 8 heads x 128 channels: 4,164,000 of 4,194,304 bytes
+    ("gqa_decode", dict(B=125, H=64, Hkv=8, D=128, Lmax=64, seq_len=_NEAR_LIMIT_LENS, seed=7902)),
 ])
 def test_noalloc_decode_matches_workspace_decode_twice(name, overrides):
     import torch
@@ -44,6 +55,9 @@ def test_noalloc_decode_matches_workspace_decode_twice(name, overrides):
     q, k, v = (to_dev(x[n], "bf16") for n in "qkv")
     sl = torch.from_numpy(x["seq_len"]).cuda()
     ref = to_host64(ta.decode_gqa(q, k, v, sl))        # workspace path
+    exact = oracle.decode_gqa(to_f64(x["q"], "bf16"), to_f64(x["k"], "bf16"),
+                              to_f64(x["v"], "bf16"), x["seq_len"])
+    assert_close(ref, exact, "bf16", "workspace decode vs oracle")
     fn = _noalloc(ta)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     B, Hq, D = x["q"].shape
@@ -55,6 +69,7 @@ def test_noalloc_decode_matches_workspace_decode_twice(name, overrides):
         assert st == 0, f"call {call}: status {st}"
         torch.cuda.synchronize()
         assert ta.device_status() == 0
+        assert_close(to_host64(o), exact, "bf16", f"noalloc call {call} vs oracle")
         assert_close(to_host64(o), ref, "bf16", f"noalloc call {call} vs workspace decode")
 
 

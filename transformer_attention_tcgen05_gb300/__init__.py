@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "AttnError", "lib", "full_fwd", "full_fwd_strided", "causal_gqa_fwd_strided", "na3d_fwd_strided", "rope_joint_fwd", "decode_gqa", "na3d_fwd", "causal_gqa_fwd",
     "na3d_window_starts", "kv_append", "kv_append_ring", "decode_gqa_ring", "decode_workspace_bytes", "rope_joint_workspace_bytes",
-    "device_status", "launch_count", "version", "FAMILIES", "LIB_PATH",
+    "device_status", "debug_wait_test", "launch_count", "version", "FAMILIES", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libattn.so")
@@ -37,7 +37,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           6: "device-side check failed"}
 #: kernel families of attn_launch_count
 FAMILIES = {"simt": 0, "tc_flash": 1, "decode": 2, "rope": 3, "na_starts": 4, "tc_na": 5,
-            "kv_append": 6}
+            "kv_append": 6, "debug": 7}
 
 
 class AttnError(RuntimeError):
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         L.attn_status_string.argtypes = [_i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_device_status.argtypes = [_vp]
+        L.attn_debug_wait_test.argtypes = [_u64, _vp]
         L.attn_launch_count.argtypes = [_i]
         L.attn_launch_count.restype = _u64
         L.attn_version.restype = ctypes.c_char_p
@@ -362,6 +363,14 @@ def device_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(lib().attn_device_status(_stream(dev)))
+
+
+def debug_wait_test(limit_ns: int, device=None) -> None:
+    """One bounded device wait that is made to run out after limit_ns (testing
+    the failure path): the next device_status() reports the timeout."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib().attn_debug_wait_test(int(limit_ns), _stream(dev)), "debug_wait_test")
 
 
 def launch_count(family: str) -> int:

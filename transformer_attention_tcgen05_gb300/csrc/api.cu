@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace attn {
 
@@ -80,6 +81,15 @@ bool stride_ok(long long s, attn_dtype_t dt) {
 // Extents whose element counts must stay below 2^31 per (batch, head) slice so
 // that 32-bit row indices inside the kernels cannot overflow.
 bool small_enough(long long rows, int D) { return rows > 0 && rows * D < (1ll << 31); }
+
+// One thread waits on a shared-memory barrier that nothing ever completes:
+// the bounded wait runs out after limit_ns, raises kDevTimeout and returns.
+__global__ void wait_test_kernel(unsigned long long limit_ns, unsigned *err) {
+    __shared__ uint64_t bar;
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_barrier_init();
+    ptx::mbar_wait_limit(&bar, 0, err, limit_ns);
+}
 
 }  // namespace
 
@@ -484,6 +494,15 @@ attn_status_t attn_na3d_window_starts(int T, int Hg, int W, const int kernel[3],
     st = get_ctx(stream, &c);
     if (st != ATTN_OK) return st;
     return na_starts(c, T, Hg, W, kernel, starts);
+}
+
+attn_status_t attn_debug_wait_test(uint64_t limit_ns, void *stream) {
+    if (limit_ns < 1000 || limit_ns > kWaitLimitNs) return ATTN_ERR_INVALID_ARG;
+    Ctx c;
+    attn_status_t st = get_ctx(stream, &c);
+    if (st != ATTN_OK) return st;
+    wait_test_kernel<<<1, 1, 0, c.stream>>>(limit_ns, c.err);
+    return launch_status(kFamDebug);
 }
 
 attn_status_t attn_debug_tc_tile(const void *q, const void *k, const void *v, const void *P,

@@ -763,6 +763,16 @@ extern "C" attn_status_t attn_decode_gqa_noalloc(const void *q, const void *k_ca
     Ctx c;
     attn_status_t st = context_for(stream, &c);
     if (st != ATTN_OK) return st;
+    // the scratch address belongs to the current device: a stream of another
+    // device would run the kernel against the wrong memory
+    if (stream) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(c.stream, &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_INVALID_ARG;
+        }
+        if (sdev != c.device) return ATTN_ERR_INVALID_ARG;
+    }
     uint8_t *scratch = nullptr;
     st = scratch_address(c.device, &scratch);
     if (st != ATTN_OK) return st;

@@ -24,7 +24,8 @@ enum KernelFamily : int {
     kFamNaStarts = 4,
     kFamTcNa = 5,
     kFamKvAppend = 6,
-    kFamCount = 7,
+    kFamDebug = 7,
+    kFamCount = 8,
 };
 
 void count_launch(int family);

@@ -53,17 +53,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and raises kDevTimeout) if it does not within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+// false (and raises kDevTimeout) if it does not within limit_ns.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             raise_device_error(err, kDevTimeout);
             return false;
         }
     }
     return true;
+}
+
+// The same with the library's limit for every wait (kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+    return mbar_wait_limit(bar, parity, err, kWaitLimitNs);
 }
 
 // As mbar_wait, but also gives up (without raising) once *abort is set by

@@ -10,26 +10,37 @@
 //   warps 0-3   softmax warpgroup of Q0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax warpgroup of Q1
 //   warp  8     MMA issuer (one elected thread) and TMEM owner
-//   warp  9     TMA loader of Q and K (one elected thread)
-//   warp 10     TMA loader of V (one elected thread); warp 11 only donates
-//               registers: the third warpgroup drops to 72 registers per
-//               thread (setmaxnreg) so the softmax warpgroups can hold a whole
-//               128-column S row in registers (216 per thread).
-// Tensor memory (512 columns): S_t at [128 t, 128 t + 128), O_t at
-// [256 + D t, 256 + D (t + 1)).  With D = 128 the columns are full and P_t
-// (bf16, two per column) overwrites the first 64 columns of S_t once the
-// softmax has read S_t; with D = 64 P_t has columns of its own
-// ([384 + 64 t, 448 + 64 t)).  The P V MMA takes P straight from TMEM
-// (A operand) and V from shared memory (MN-major B operand).
+//   warp  9     TMA loader of Q and the K ring (one elected thread)
+//   warp 10     TMA loader of the V ring (one elected thread)
+//   warp 11     neighborhood attention: MMA issuer of Q1 (warp 8 then issues
+//               for Q0 only); full attention: idle.
+// The third warpgroup drops to 72 registers per thread (setmaxnreg) so the
+// softmax warpgroups can hold a whole S row in registers (216 per thread).
 //
-// Issue order of the MMA thread per key tile j:
+// Full attention (key tiles of 128): tensor memory holds S_t at [128 t,
+// 128 t + 128) and O_t at [256 + D t, 256 + D (t + 1)).  With D = 128 the
+// columns are full and P_t (16-bit, two per column) overwrites the first 64
+// columns of S_t once the softmax has read S_t; with D = 64 P_t has columns of
+// its own ([384 + 64 t, 448 + 64 t)).  One thread issues every MMA, per key
+// tile j:
 //   D = 128 (P over S):  PV0(j), QK0(j+1), PV1(j), QK1(j+1)   -- QK_t(j+1)
 //       overwrites S_t only after PV_t(j) has read P_t (MMAs of one thread
-//       execute in issue order), so each softmax warpgroup hides behind the
-//       other tile's PV and QK;
+//       execute in issue order);
 //   D = 64 (separate P): QK0(j+1), QK1(j+1) as soon as the softmax has read
-//       S_t(j) into registers, then PV0(j), PV1(j) -- the next S is computed
-//       while the softmax of the current tile runs.
+//       S_t(j) into registers, then PV0(j), PV1(j).
+//
+// Neighborhood attention (key tiles of 96): every query tile has two S
+// buffers and P is written over the S it came from: [S_t,0 | S_t,1 | O_t]
+// (96 + 96 + 64 columns) at 256 t.  Each query tile has an issuer of its own
+// that runs one key tile ahead: after PV_t(j) (which reads buffer j % 2) it
+// issues QK_t(j + 2) into that same buffer, so S(j + 1) is ready while the
+// softmax works on tile j.  Measured on the clock: a barrier hand-off between
+// warps costs ~200 cycles, a commit ~100 and each MMA ~46 cycles to issue, so
+// with one S buffer and one issuer the per-step chain of hand-offs, not the
+// tensor core or the softmax, set the pace.  The P V MMA takes P straight
+// from TMEM (A operand) and V from shared memory (MN-major B operand).  K and
+// V stream through rings of their own (K one stage deeper for neighborhood
+// attention, where the next Q K^T runs a key tile ahead).
 //
 // Softmax (base 2): x = s * scale * log2(e).  The first tile sets the running
 // max m; later tiles are exponentiated against m as it stands (no tile-max
@@ -69,14 +80,20 @@ namespace {
 
 constexpr int kBM = 128;      // query rows per tile (MMA M)
 constexpr int kNQ = 2;        // query tiles per CTA
-constexpr int kBN = 128;      // max keys per key tile (MMA N of S)
+constexpr int kBN = 128;      // keys per key tile of full attention (MMA N of S)
+constexpr int kBNA = 96;      // keys per neighborhood key tile (a (KT, KH, 16) sub-box)
 constexpr int kKW = 16;       // neighborhood key sub-box width along w
+constexpr int kMaxPenaltyTiles = 8;   // distinct key penalty tiles per query box
+// bf16 neighborhood attention applies the h and w window tests through the
+// tensor core (penalty channels) when true, in the softmax when false
+constexpr bool kNaPenalty = true;
 
-template <int D, bool NA>
+template <int D, bool NA, bool PEN>
 struct TcCfg {
+    static constexpr int BN = NA ? kBNA : kBN;             // keys per key tile
     static constexpr int PANELS = D / 64;                  // 128-byte swizzle panels
     static constexpr int PANEL_Q = kBM * 128;              // bytes per Q panel
-    static constexpr int PANEL_KV = kBN * 128;             // bytes per K/V panel
+    static constexpr int PANEL_KV = BN * 128;              // bytes per K/V panel
     static constexpr int Q_BYTES = PANELS * PANEL_Q;
     static constexpr int KV_BYTES = PANELS * PANEL_KV;
     static constexpr int STREAMS = NA ? kNQ : 1;           // K/V streams per stage
@@ -84,31 +101,60 @@ struct TcCfg {
     // The key-side penalties of a key sub-box depend only on its h and w chunk,
     // so each query box needs at most MAXV distinct penalty tiles, built once.
     static constexpr int X_ROW = 32;
-    static constexpr int MAXV = NA ? 6 : 0;
-    static constexpr int QX_BYTES = NA ? kNQ * kBM * X_ROW : 0;
-    static constexpr int KX_BYTES = kBN * X_ROW;              // one penalty tile
+    static constexpr int MAXV = PEN ? kMaxPenaltyTiles : 0;
+    static constexpr int QX_BYTES = PEN ? kNQ * kBM * X_ROW : 0;
+    static constexpr int KX_BYTES = BN * X_ROW;               // one penalty tile
     static constexpr int KXV_BYTES = STREAMS * MAXV * KX_BYTES;
-    static constexpr int STAGE_BYTES = 2 * STREAMS * KV_BYTES;
+    // K and V stream through rings of their own: a K stage is needed a
+    // whole step before the V stage of the same key tile, so K gets the
+    // deeper ring when shared memory allows only an odd number of stages
+    static constexpr int STAGE_BYTES = STREAMS * KV_BYTES;   // one K (or V) stage
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int NS_RAW = (BUDGET - kNQ * Q_BYTES - QX_BYTES - KXV_BYTES) / STAGE_BYTES;
-    static constexpr int NSTAGE = NS_RAW > 4 ? 4 : NS_RAW;
-    static_assert(NSTAGE >= 2, "at least two K/V stages");
+    static constexpr int NS_ALL = (BUDGET - kNQ * Q_BYTES - QX_BYTES - KXV_BYTES) / STAGE_BYTES;
+    // (full attention keeps equal rings: a third K stage at D = 128 measured slower)
+    static constexpr int KS_RAW = NA ? (NS_ALL + 1) / 2 : NS_ALL / 2;
+    static constexpr int KS = KS_RAW > 4 ? 4 : KS_RAW;                        // K stages
+    static constexpr int VS = NS_ALL - KS_RAW > 4 ? 4 : NS_ALL - KS_RAW;      // V stages
+    static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_QX = kNQ * Q_BYTES;
     static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
-    static constexpr int OFF_KV = OFF_KXV + KXV_BYTES;
-    static constexpr int OFF_BAR = OFF_KV + NSTAGE * STAGE_BYTES;
+    static constexpr int OFF_K = OFF_KXV + KXV_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + VS * STAGE_BYTES;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;      // barriers + 1024 B alignment slack
-    static constexpr uint32_t TM_S = 0;                    // S_t at TM_S + t * kBN
-    static constexpr uint32_t TM_O = kNQ * kBN;            // O_t at TM_O + t * D
-    static constexpr bool SEP_P = kNQ * (kBN + D + kBN / 2) <= 512;   // P_t has its own columns
-    static constexpr uint32_t TM_P = SEP_P ? TM_O + kNQ * D : TM_S;   // P_t at TM_P + t * PSTRIDE
-    static constexpr uint32_t PSTRIDE = SEP_P ? kBN / 2 : kBN;
+    // Tensor memory (512 columns).  P holds the 16-bit probabilities, two
+    // per column.
+    //  * full attention: S_t at t BN, O_t at kNQ BN + t D; P_t over the first
+    //    half of S_t (D = 128) or in columns of its own after the O's (D = 64).
+    //  * neighborhood attention: two S buffers per query tile (key tile j in
+    //    buffer j % 2) with P written over the S it came from, so the Q K^T of
+    //    tile j + 1 is already computed while the softmax works on tile j and
+    //    the MMA issuer runs a whole key tile ahead: per query tile
+    //    [S_t,0 | S_t,1 | O_t] (96 + 96 + 64 columns) at t 256.
+    static constexpr int SBUF = NA ? 2 : 1;
+    static constexpr bool SEP_P = !NA && kNQ * (BN + D + BN / 2) <= 512;
+    static constexpr uint32_t TBLK = NA ? 2 * BN + D : BN;
+    static constexpr uint32_t tm_s(int t, int b) { return t * TBLK + (NA ? b * BN : 0); }
+    static constexpr uint32_t tm_o(int t) { return NA ? t * TBLK + 2 * BN : kNQ * BN + t * D; }
+    static constexpr uint32_t tm_p(int t, int b) {
+        return NA ? tm_s(t, b) : (SEP_P ? kNQ * BN + kNQ * D + t * (BN / 2) : t * BN);
+    }
+    // S buffer of key tile j and the phase parity of its barriers
+    static constexpr int buf_of(int j) { return SBUF == 2 ? (j & 1) : 0; }
+    static constexpr uint32_t par_of(int j) { return SBUF == 2 ? ((j >> 1) & 1) : (j & 1); }
     static constexpr uint32_t TM_COLS = 512;
+    static_assert(tm_o(kNQ - 1) + D <= TM_COLS && (!SEP_P || tm_p(kNQ, 0) <= TM_COLS),
+                  "tensor-memory layout must fit 512 columns");
     static constexpr int NSOFT = 4 * kNQ;
-    static constexpr int W_MMA = NSOFT;
+    static constexpr int W_MMA = NSOFT;                   // MMA issuer of query tile 0, TMEM owner
     static constexpr int W_LOAD = NSOFT + 1;              // Q and K copies
     static constexpr int W_LOADV = NSOFT + 2;             // V copies
+    static constexpr int W_MMA1 = NSOFT + 3;              // MMA issuer of query tile 1
+    // MMA issuing threads: one per query tile for neighborhood attention (its
+    // per-tile barrier waits and MMAs kept one thread busy for the whole
+    // step), one for both tiles of full attention (two issuers measured slower)
+    static constexpr int ISSUERS = NA ? kNQ : 1;
     static constexpr int NT = (NSOFT + 4) * 32;            // 3 warpgroups
     // register split: launch 168 x 384 = 64512; 2 x 128 x 216 + 128 x 72 = 64512
     static constexpr int REGS_LAUNCH = 168;
@@ -117,10 +163,8 @@ struct TcCfg {
     static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= NT * REGS_LAUNCH,
                   "setmaxnreg split must fit the launch's register file share");
     // K (or V) tile of stream u in stage s
-    static constexpr int k_off(int s, int u) { return OFF_KV + s * STAGE_BYTES + u * KV_BYTES; }
-    static constexpr int v_off(int s, int u) {
-        return OFF_KV + s * STAGE_BYTES + (STREAMS + u) * KV_BYTES;
-    }
+    static constexpr int k_off(int s, int u) { return OFF_K + s * STAGE_BYTES + u * KV_BYTES; }
+    static constexpr int v_off(int s, int u) { return OFF_V + s * STAGE_BYTES + u * KV_BYTES; }
     // penalty tile v (= h chunk * w chunks + w chunk) of stream u
     static constexpr int kxv_off(int u, int v) { return OFF_KXV + (u * MAXV + v) * KX_BYTES; }
 };
@@ -137,7 +181,7 @@ struct TcParams {
     int bt, bh, bw;          // query box
     int nbh, nbw2;           // boxes along h; box pairs along w
     int nbw;                 // boxes along w
-    int KH;                  // key sub-box height (keys per tile = KH * 16)
+    int KT, KH;              // key sub-box frames and height (KT * KH * 16 = 96 keys)
     float penalty;           // bf16: power of two >= 2^100 with penalty * c_log2 >= 300
     // causal grouped-query prefill
     int Hq, Hkv, group;
@@ -148,13 +192,23 @@ struct TcParams {
 };
 
 // Barrier block at OFF_BAR.
-template <int NS>
+template <int KS, int VS>
 struct Bars {
     uint64_t q_full;
     // K and V rings are released separately: a K stage as soon as the Q K^T
     // products that read it have completed, a V stage after its P V
-    uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
-    uint64_t s_full[kNQ], s_free[kNQ], p_ready[kNQ], o_done[kNQ];
+    uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+    // per S buffer b of query tile t (one buffer, b = 0, outside
+    // neighborhood attention): s_full[2 t + b] its Q K^T has completed,
+    // p_ready[2 t + b] the softmax has written P there, o_done[2 t + b] the
+    // P V product that read that P has completed.  A parity wait is only
+    // valid while its barrier is at most one phase ahead of or behind the
+    // phase waited for; with two buffers one barrier per tile would break
+    // that (the issuer may complete the Q K^T of key tile j + 2, or the
+    // softmax finish tile j + 1, before the other side has waited for tile
+    // j), a barrier per buffer keeps it.
+    uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
+    uint64_t s_free[kNQ];      // separate P (D = 64): the softmax holds S_t in registers
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -164,8 +218,8 @@ struct Bars {
 struct NaTile {
     int t0, h0, w0;          // box origin
     int u0t, u0h, u0w;       // union origin
-    int ut, nhc, nwc;        // union t extent, h chunks, w chunks
-    int ntiles;              // key tiles = ut * nhc * nwc (0 if the box is empty)
+    int ntc, nhc, nwc;       // union t, h and w chunks (KT frames, KH rows, 16 columns)
+    int ntiles;              // key tiles = ntc * nhc * nwc (0 if the box is empty)
 };
 
 // a[t] for a per-query-tile array and a run-time t, by selects: indexing
@@ -179,7 +233,7 @@ __device__ __forceinline__ T pick(const T (&a)[kNQ], int t) {
     return r;
 }
 
-__device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t) {
+__device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t, int KT, int KH) {
     NaTile g;
     const int per_t = p.nbh * p.nbw2;
     const int bi_t = pair / per_t, bi_h = (pair / p.nbw2) % p.nbh, bi_w = (pair % p.nbw2) * 2 + t;
@@ -188,7 +242,7 @@ __device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t) {
     g.w0 = bi_w * p.bw;
     if (bi_w >= p.nbw) {
         g.ntiles = 0;
-        g.u0t = g.u0h = g.u0w = g.ut = g.nhc = g.nwc = 0;
+        g.u0t = g.u0h = g.u0w = g.ntc = g.nhc = g.nwc = 0;
         return g;
     }
     const int t1 = imin(g.t0 + p.bt, p.T) - 1, h1 = imin(g.h0 + p.bh, p.Hg) - 1,
@@ -196,40 +250,51 @@ __device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t) {
     g.u0t = na_window_start(g.t0, p.T, p.kt);
     g.u0h = na_window_start(g.h0, p.Hg, p.kh);
     g.u0w = na_window_start(g.w0, p.W, p.kw);
-    g.ut = na_window_start(t1, p.T, p.kt) + p.et - g.u0t;
+    const int ut = na_window_start(t1, p.T, p.kt) + p.et - g.u0t;
     const int uh = na_window_start(h1, p.Hg, p.kh) + p.eh - g.u0h;
     const int uw = na_window_start(w1, p.W, p.kw) + p.ew - g.u0w;
-    g.nhc = cdiv(uh, p.KH);
+    g.ntc = cdiv(ut, KT);
+    g.nhc = cdiv(uh, KH);
     g.nwc = cdiv(uw, kKW);
-    g.ntiles = g.ut * g.nhc * g.nwc;
+    g.ntiles = g.ntc * g.nhc * g.nwc;
     return g;
 }
 
-// Key sub-box of tile j: origin (t, h, w).
-__device__ __forceinline__ void na_key_box(const NaTile &g, int KH, int j, int &t, int &h, int &w) {
+// Key sub-box of tile j: origin (t, h, w); tiles run w chunk fastest, then
+// h chunk, then t chunk.
+__device__ __forceinline__ void na_key_box(const NaTile &g, int KT, int KH, int j, int &t, int &h,
+                                           int &w) {
     const int wc = j % g.nwc;
     const int hc = (j / g.nwc) % g.nhc;
     const int tc = j / (g.nwc * g.nhc);
-    t = g.u0t + tc;
+    t = g.u0t + tc * KT;
     h = g.u0h + hc * KH;
     w = g.u0w + wc * kKW;
 }
 
-// KHC > 0 fixes the neighborhood key sub-box height (keys per tile = 16 KHC)
-// at compile time, so the softmax's column loops and masks unroll without
-// run-time tests; KHC = 0 takes it from the parameters.  F16: inputs, P and
-// output in f16 instead of bf16 (same layouts; the MMA operand format flips).
-template <int D, bool NA, bool CAUSAL, int KHC, bool F16>
-__global__ void __launch_bounds__(TcCfg<D, NA>::NT, 1)
+// KSH = 10 KT + KH > 0 fixes the neighborhood key sub-box (KT frames x KH
+// rows x 16 columns = 96 keys) at compile time, so the softmax's masks
+// unroll without run-time tests; KSH = 0 takes KT and KH from the
+// parameters.  F16: inputs, P and output in f16 instead of bf16 (same
+// layouts; the MMA operand format flips).
+// Whether a kernel instance applies the neighborhood h / w window tests
+// through penalty channels (bf16 only: f16 cannot hold the penalty).
+template <bool NA, bool F16>
+constexpr bool na_penalty() { return NA && !F16 && kNaPenalty; }
+
+template <int D, bool NA, bool CAUSAL, int KSH, bool F16>
+__global__ void __launch_bounds__(TcCfg<D, NA, na_penalty<NA, F16>()>::NT, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams p) {
-    using C = TcCfg<D, NA>;
+    using C = TcCfg<D, NA, na_penalty<NA, F16>()>;
+    constexpr bool PEN = na_penalty<NA, F16>();
     static_assert(!(NA && CAUSAL), "causal prefill is a full-attention variant");
-    static_assert(sizeof(Bars<C::NSTAGE>) <= 512, "barrier block must fit its reserved bytes");
+    using BarsT = Bars<C::KS, C::VS>;
+    static_assert(sizeof(BarsT) <= 512, "barrier block must fit its reserved bytes");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
-    Bars<C::NSTAGE> *bars = reinterpret_cast<Bars<C::NSTAGE> *>(smem + C::OFF_BAR);
+    BarsT *bars = reinterpret_cast<BarsT *>(smem + C::OFF_BAR);
     volatile int *abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -245,14 +310,16 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     int steps;
     NaTile g[kNQ];
     int q0 = 0;
-    int BNt = kBN;                 // keys per tile
+    constexpr int BNt = C::BN;     // keys per tile
+    // neighborhood key sub-box: KT frames x KH rows x 16 columns
+    const int KT = NA ? (KSH > 0 ? KSH / 10 : p.KT) : 1;
+    const int KH = NA ? (KSH > 0 ? KSH % 10 : p.KH) : 1;
     if constexpr (NA) {
 #pragma unroll
         for (int t = 0; t < kNQ; ++t) {
-            g[t] = na_tile(p, blockIdx.x, t);
+            g[t] = na_tile(p, blockIdx.x, t, KT, KH);
             n_t[t] = g[t].ntiles;
         }
-        BNt = (KHC > 0 ? KHC : p.KH) * kKW;
         steps = imax(n_t[0], n_t[1]);
     } else if constexpr (CAUSAL) {
         // heaviest query blocks first; query tile t sees key tiles 0 .. its diagonal
@@ -270,19 +337,25 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bars->q_full, 1);
-        for (int s = 0; s < C::NSTAGE; ++s) {
+        // a stage is free once every MMA issuer has released it
+        for (int s = 0; s < C::KS; ++s) {
             ptx::mbar_init(&bars->k_full[s], 1);
+            ptx::mbar_init(&bars->k_empty[s], C::ISSUERS);
+        }
+        for (int s = 0; s < C::VS; ++s) {
             ptx::mbar_init(&bars->v_full[s], 1);
-            ptx::mbar_init(&bars->k_empty[s], 1);
-            ptx::mbar_init(&bars->v_empty[s], 1);
+            ptx::mbar_init(&bars->v_empty[s], C::ISSUERS);
         }
         for (int t = 0; t < kNQ; ++t) {
-            ptx::mbar_init(&bars->s_full[t], 1);
+            ptx::mbar_init(&bars->s_full[2 * t], 1);
+            ptx::mbar_init(&bars->s_full[2 * t + 1], 1);
+            ptx::mbar_init(&bars->p_ready[2 * t], 128);
+            ptx::mbar_init(&bars->p_ready[2 * t + 1], 128);
             ptx::mbar_init(&bars->s_free[t], 128);
-            ptx::mbar_init(&bars->p_ready[t], 128);
-            ptx::mbar_init(&bars->o_done[t], 1);
+            ptx::mbar_init(&bars->o_done[2 * t], 1);
+            ptx::mbar_init(&bars->o_done[2 * t + 1], 1);
         }
-        ptx::mbar_init(&bars->drain, 1);
+        ptx::mbar_init(&bars->drain, C::ISSUERS);
         bars->abort = 0;
         ptx::fence_barrier_init();
     }
@@ -298,7 +371,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             }
         }
     }
-    if constexpr (NA && !F16) {
+    if constexpr (PEN) {
         const int rows = p.bt * p.bh * p.bw;
         // one-hot window-offset channels of every query row: channel dh, then
         // bh + dw (rows past the box: all zero)
@@ -328,7 +401,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             const int nv = g[u].nhc * g[u].nwc;
             for (int i = threadIdx.x; i < nv * BNt * 2; i += C::NT) {
                 const int v = i / (BNt * 2), r = (i / 2) % BNt, half = i % 2;
-                const int kh = g[u].u0h + (v / g[u].nwc) * (BNt / kKW) + r / kKW;
+                // key r of the sub-box: w column r % 16, h row (r / 16) % KH
+                // (the same for each of its KT frames)
+                const int kh = g[u].u0h + (v / g[u].nwc) * KH + (r / kKW) % KH;
                 const int kw = g[u].u0w + (v % g[u].nwc) * kKW + r % kKW;
                 uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
@@ -397,11 +472,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         }
                     }
             }
+            const int NS = which == 0 ? C::KS : C::VS;   // depth of this ring
             int issued = 0;
             for (int j = 0; j < steps; ++j) {
-                const int s = j % C::NSTAGE;
-                if (j >= C::NSTAGE &&
-                    !ptx::mbar_wait_or_abort(&empty[s], ((j / C::NSTAGE) - 1) & 1, p.err, abort))
+                const int s = j % NS;
+                if (j >= NS && !ptx::mbar_wait_or_abort(&empty[s], ((j / NS) - 1) & 1, p.err, abort))
                     break;
                 issued = j + 1;
                 // a shared K/V stream (no neighborhood boxes) serves both query
@@ -420,7 +495,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                             smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) + pn * C::PANEL_KV;
                         if constexpr (NA) {
                             int kt_, kh_, kw_;
-                            na_key_box(g[u], BNt / kKW, j, kt_, kh_, kw_);
+                            na_key_box(g[u], KT, KH, j, kt_, kh_, kw_);
                             ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, &full[s], pol_kv);
                         } else {
                             ptx::tma_load_4d(dst, tm, pn * 64, j * kBN, fkh, fb, &full[s], pol_kv);
@@ -432,11 +507,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             // (bounded) before the CTA's shared memory is released
             if (*abort) {
                 if (which == 0) ptx::mbar_wait(&bars->q_full, 0, nullptr);
-                for (int j = imax(0, issued - C::NSTAGE); j < issued; ++j)
-                    ptx::mbar_wait(&full[j % C::NSTAGE], (j / C::NSTAGE) & 1, nullptr);
+                for (int j = imax(0, issued - NS); j < issued; ++j)
+                    ptx::mbar_wait(&full[j % NS], (j / NS) & 1, nullptr);
             }
-        } else if (warp == C::W_MMA && lane == 0) {
-            // ============================================= MMA issuer
+        } else if ((warp == C::W_MMA || (C::ISSUERS == kNQ && warp == C::W_MMA1)) && lane == 0) {
+            // ============================================= MMA issuers: one
+            // thread per query tile, in warps of different SM sub-partitions,
+            // so the issue of one tile's MMAs (and its barrier waits) does not
+            // wait behind the other's; both release the shared K/V stages
+            const int tt = warp == C::W_MMA ? 0 : 1;
             const uint32_t id_qk = ptx::idesc_16_f32(kBM, BNt, false, F16);
             const uint32_t id_pv = ptx::idesc_16_f32(kBM, D, true, F16);
             // Matrix descriptors are built once: a k-step, a stage or a tile only
@@ -460,9 +539,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 #pragma unroll
                 for (int t = 0; t < kNQ; ++t) nv[t] = imax(1, g[t].nhc * g[t].nwc);
             }
-            const int nkv = BNt / 16;            // k-steps of P V
+            constexpr int nkv = BNt / 16;        // k-steps of P V
             auto issue_qk = [&](int t, int j) {
-                const int s = j % C::NSTAGE;
+                const int s = j % C::KS;
                 const uint32_t a0 = dq0 + uint32_t((t * C::Q_BYTES) >> 4);
                 const uint32_t b0 =
                     dk0 + uint32_t((s * C::STAGE_BYTES + (C::STREAMS == 1 ? 0 : t) * C::KV_BYTES) >> 4);
@@ -470,107 +549,137 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = ((kk >> 2) * C::PANEL_Q + (kk & 3) * 32) >> 4;
                     const uint32_t ob = ((kk >> 2) * C::PANEL_KV + (kk & 3) * 32) >> 4;
-                    ptx::mma_ss(tmem + C::TM_S + t * kBN, ptx::desc_join(a0 + oa, HI128),
+                    ptx::mma_ss(tmem + C::tm_s(t, C::buf_of(j)), ptx::desc_join(a0 + oa, HI128),
                                 ptx::desc_join(b0 + ob, HI128), id_qk, kk > 0);
                 }
-                if constexpr (NA && !F16) {
+                if constexpr (PEN) {
                     // + window penalties: one more k-step over the 16 extra channels;
                     // QK_t(j) uses penalty tile j mod (h chunks x w chunks)
                     const uint32_t a = dqx0 + uint32_t((t * kBM * C::X_ROW) >> 4);
                     const uint32_t b = dkx0 + uint32_t(((t * C::MAXV + vq[t]) * C::KX_BYTES) >> 4);
                     if (++vq[t] == nv[t]) vq[t] = 0;
-                    ptx::mma_ss(tmem + C::TM_S + t * kBN, ptx::desc_join(a, HI32), ptx::desc_join(b, HI32),
+                    ptx::mma_ss(tmem + C::tm_s(t, C::buf_of(j)), ptx::desc_join(a, HI32), ptx::desc_join(b, HI32),
                                 id_qk, 1u);
                 }
-                ptx::tc_commit(&bars->s_full[t]);
+                ptx::tc_commit(&bars->s_full[2 * t + C::buf_of(j)]);
             };
             auto issue_pv = [&](int t, int j) {
-                const int s = j % C::NSTAGE;
+                const int s = j % C::VS;
                 const uint32_t b0 =
                     dv0 + uint32_t((s * C::STAGE_BYTES + (C::STREAMS == 1 ? 0 : t) * C::KV_BYTES) >> 4);
-                const uint32_t a0 = tmem + C::TM_P + t * C::PSTRIDE;
+                const uint32_t a0 = tmem + C::tm_p(t, C::buf_of(j));
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    if (kk >= nkv) break;
-                    ptx::mma_ts(tmem + C::TM_O + t * D, a0 + kk * 8,
+                for (int kk = 0; kk < nkv; ++kk)
+                    ptx::mma_ts(tmem + C::tm_o(t), a0 + kk * 8,
                                 ptx::desc_join(b0 + uint32_t(kk * (2048 >> 4)), HI128), id_pv,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                ptx::tc_commit(&bars->o_done[t]);
+                ptx::tc_commit(&bars->o_done[2 * t + C::buf_of(j)]);
             };
             bool ok = ptx::mbar_wait_or_abort(&bars->q_full, 0, p.err, abort) &&
                       (steps == 0 || ptx::mbar_wait_or_abort(&bars->k_full[0], 0, p.err, abort));
             ptx::tc_fence_after();
+            // query tiles of this issuer: its own one, or both with one issuer
+            const int t_lo = C::ISSUERS == kNQ ? tt : 0, t_hi = C::ISSUERS == kNQ ? tt + 1 : kNQ;
+            // every stage barrier counts one release per issuer and use
+            auto release = [&](uint64_t *bar) { ptx::tc_commit(bar); };
+            // Each stage barrier is waited on once per issuer and use (a completed
+            // wait still costs this thread a round trip to shared memory).
+            bool k_seen = false, v_seen = false;
+            auto wait_k = [&](int jn) {
+                if (!k_seen) {
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[jn % C::KS], (jn / C::KS) & 1,
+                                                       p.err, abort);
+                    k_seen = true;
+                }
+            };
+            auto wait_v = [&](int j) {
+                if (!v_seen) {
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[j % C::VS], (j / C::VS) & 1,
+                                                       p.err, abort);
+                    v_seen = true;
+                }
+            };
+            // Q K^T of key tile jn for tile t, once the softmax no longer needs
+            // the S buffer it overwrites; a K stage this tile does not read (its
+            // key tiles have run out) is still released only once it has been
+            // filled, so that an issuer running ahead cannot complete a stage
+            // phase in place of the other issuer
+            auto next_qk = [&](int t, int jn, int jprev) {
+                if (jn < pick(n_t, t)) {
+                    // separate P: as soon as the softmax holds S(jprev) in
+                    // registers; P over S: after P V (jprev), issued before
+                    if (C::SEP_P)
+                        ok = ok && ptx::mbar_wait_or_abort(&bars->s_free[t], jprev & 1, p.err, abort);
+                    wait_k(jn);
+                    if (!ok) return;
+                    ptx::tc_fence_after();
+                    issue_qk(t, jn);
+                } else {
+                    wait_k(jn);
+                }
+            };
+            // P V of key tile j for tile t
+            auto this_pv = [&](int t, int j) {
+                if (j < pick(n_t, t)) {
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->p_ready[2 * t + C::buf_of(j)],
+                                                       C::par_of(j), p.err, abort);
+                    wait_v(j);
+                    if (!ok) return;
+                    ptx::tc_fence_after();
+                    issue_pv(t, j);
+                } else {
+                    wait_v(j);
+                }
+            };
             if (ok) {
-#pragma unroll
-                for (int t = 0; t < kNQ; ++t)
-                    if (n_t[t] > 0) issue_qk(t, 0);
-                if (steps > 0) ptx::tc_commit(&bars->k_empty[0]);
+                for (int t = t_lo; t < t_hi; ++t)
+                    if (pick(n_t, t) > 0) issue_qk(t, 0);
+                if (steps > 0) release(&bars->k_empty[0]);
+            }
+            // two S buffers: the Q K^T of key tile 1 right away, so the issuer
+            // runs one key tile ahead of the softmax
+            constexpr int AHEAD = C::SBUF;       // QK(j + AHEAD) follows PV(j)
+            if (C::SBUF == 2 && ok && steps > 1) {
+                for (int t = t_lo; ok && t < t_hi; ++t) next_qk(t, 1, 0);
+                if (ok) release(&bars->k_empty[1 % C::KS]);
             }
             for (int j = 0; ok && j < steps; ++j) {
-                const int s = j % C::NSTAGE;
-                const uint32_t ph = (j / C::NSTAGE) & 1;
-                const int s1 = (j + 1) % C::NSTAGE;
-                const uint32_t ph1 = ((j + 1) / C::NSTAGE) & 1;
-                bool v_ready = false, k1_ready = false;
-                auto wait_k1 = [&]() {
-                    if (!k1_ready) {
-                        ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[s1], ph1, p.err, abort);
-                        k1_ready = true;
-                    }
-                };
-                auto wait_v = [&]() {
-                    if (!v_ready) {
-                        ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[s], ph, p.err, abort);
-                        v_ready = true;
-                    }
-                };
-                if constexpr (C::SEP_P) {
-                    // next S as soon as the softmax holds the current one in registers
+                const int jn = j + AHEAD;
+                k_seen = v_seen = false;
+                if constexpr (C::ISSUERS == 1) {
+                    // one issuer for both tiles (compile-time tile indices)
+                    if constexpr (C::SEP_P) {
+                        // separate P (one S buffer): the next S as soon as the
+                        // softmax holds the current one in registers, then P V
 #pragma unroll
-                    for (int t = 0; t < kNQ; ++t) {
-                        if (!ok) break;
-                        if (j + 1 >= n_t[t]) continue;
-                        ok = ptx::mbar_wait_or_abort(&bars->s_free[t], j & 1, p.err, abort);
-                        wait_k1();
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                        issue_qk(t, j + 1);
-                    }
+                        for (int t = 0; t < kNQ; ++t)
+                            if (ok && jn < steps) next_qk(t, jn, j);
 #pragma unroll
-                    for (int t = 0; t < kNQ; ++t) {
-                        if (!ok) break;
-                        if (j >= n_t[t]) continue;
-                        ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
-                        wait_v();
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                        issue_pv(t, j);
-                    }
-                } else {
+                        for (int t = 0; t < kNQ; ++t)
+                            if (ok) this_pv(t, j);
+                    } else {
+                        // P over S: the Q K^T that overwrites the S buffer of key
+                        // tile j follows the P V that reads P there (one thread's
+                        // MMAs execute in issue order)
 #pragma unroll
-                    for (int t = 0; t < kNQ; ++t) {
-                        if (!ok) break;
-                        if (j >= n_t[t]) continue;
-                        ok = ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
-                        wait_v();
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                        issue_pv(t, j);
-                        if (j + 1 < n_t[t]) {
-                            wait_k1();
-                            if (!ok) break;
-                            ptx::tc_fence_after();
-                            issue_qk(t, j + 1);
+                        for (int t = 0; t < kNQ; ++t) {
+                            if (ok) this_pv(t, j);
+                            if (ok && jn < steps) next_qk(t, jn, j);
                         }
                     }
+                } else {
+                    // one issuer per tile: P over S in two buffers
+                    static_assert(C::ISSUERS == 1 || !C::SEP_P, "per-tile issuers use P over S");
+                    this_pv(tt, j);
+                    if (ok && jn < steps) next_qk(tt, jn, j);
                 }
-                // every Q K^T of step j + 1 and every P V of step j is issued
-                if (j + 1 < steps) ptx::tc_commit(&bars->k_empty[s1]);
-                ptx::tc_commit(&bars->v_empty[s]);
+                if (!ok) break;
+                // Q K^T of key tile j + AHEAD and P V of key tile j are issued
+                if (jn < steps) release(&bars->k_empty[jn % C::KS]);
+                release(&bars->v_empty[j % C::VS]);
             }
-            // drain: every MMA this thread issued has completed before TMEM is freed
-            ptx::tc_commit(&bars->drain);
+            // drain: every MMA of every issuer has completed before TMEM is freed
+            release(&bars->drain);
             ptx::mbar_wait(&bars->drain, 0, p.err);
         }
     } else {
@@ -580,10 +689,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         const int quarter = warp & 3;            // TMEM lanes [32 quarter, 32 quarter + 32)
         const int row = quarter * 32 + lane;     // query row within the tile
         const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-        const uint32_t s_addr = lane_base + C::TM_S + t * kBN;
-        const uint32_t p_addr = lane_base + C::TM_P + t * C::PSTRIDE;
-        const uint32_t o_addr = lane_base + C::TM_O + t * D;
+        const uint32_t o_addr = lane_base + C::tm_o(t);
         const float cl = p.c_log2;
+        constexpr int NG = BNt / 16;             // 16-key groups per key tile
 
         // query of this row (neighborhood path) and its window
         int qt = 0, qh = 0, qw = 0, wst = 0, wsh = 0, wsw = 0;
@@ -597,7 +705,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             qw = gt.w0 + dw;
             qvalid = nt > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
             wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
-            if constexpr (F16) {
+            if constexpr (!PEN) {
                 wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
                 wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
             }
@@ -605,29 +713,43 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             qvalid = q0 + t * kBM + row < p.Nq;
         }
 
+        // waits for the P V product of key tile jj of this query tile (and so
+        // for every earlier one: one thread's MMAs complete in issue order).
+        // Valid while the P V of key tile jj - 2 is known complete: it is once
+        // the softmax holds S(jj), whose Q K^T was issued after it.
+        auto wait_pv = [&](int jj) -> bool {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[2 * t + C::buf_of(jj)],
+                                                                 C::par_of(jj), p.err, abort)))
+                return false;
+            ptx::tc_fence_after();
+            return true;
+        };
+
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // neighborhood: key sub-box counters (w fastest, then h, then t)
         int tc = 0, hc = 0, wc = 0;
         for (int j = 0; j < nt; ++j) {
-            if (!__all_sync(0xffffffffu,
-                            ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort))) {
+            const uint32_t s_addr = lane_base + C::tm_s(t, C::buf_of(j));
+            const uint32_t p_addr = lane_base + C::tm_p(t, C::buf_of(j));
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->s_full[2 * t + C::buf_of(j)],
+                                                                 C::par_of(j), p.err, abort))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
 
             // ---- neighborhood: the h and w window penalties are already in S
-            //      (extra MMA channels); a row whose t window misses this key
-            //      sub-box's frame gets P = 0 below.  (Skipping sub-boxes that
-            //      none of a warp's 32 windows reaches measured slower than
-            //      computing them: the MMAs run anyway and the test costs issue
-            //      slots on the critical path.)
-            bool t_ok = true;
+            //      (bf16: extra MMA channels); a row whose t window misses the
+            //      frame of a 16-key group gets P = 0 there (bit g of gmask
+            //      clear).  (Skipping sub-boxes that none of a warp's 32 windows
+            //      reaches measured slower than computing them: the MMAs run
+            //      anyway and the test costs issue slots on the critical path.)
+            uint32_t gmask = (1u << NG) - 1u;
             int kh0 = 0, kw0 = 0;                // key sub-box origin along h and w
             if constexpr (NA) {
-                const int kt_ = gt.u0t + tc;
-                kh0 = gt.u0h + hc * (BNt / kKW);
+                const int kt0 = gt.u0t + tc * KT;
+                kh0 = gt.u0h + hc * KH;
                 kw0 = gt.u0w + wc * kKW;
                 if (++wc == gt.nwc) {
                     wc = 0;
@@ -636,14 +758,18 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         ++tc;
                     }
                 }
-                t_ok = qvalid && unsigned(kt_ - wst) < unsigned(p.et);
+                gmask = 0u;
+                if (qvalid) {
+#pragma unroll
+                    for (int gq = 0; gq < NG; ++gq)   // group gq holds frame kt0 + gq / KH
+                        if (unsigned(kt0 + gq / KH - wst) < unsigned(p.et)) gmask |= 1u << gq;
+                }
             }
 
-            float sv[kBN];
+            float sv[BNt];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                if (c * 32 < BNt)
-                    ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+            for (int c = 0; c < BNt / 32; ++c)
+                ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
             ptx::tmem_wait_ld();
             if constexpr (C::SEP_P) {
                 // S_t is in registers: the next QK_t may overwrite it
@@ -651,73 +777,60 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 ptx::mbar_arrive(&bars->s_free[t]);
             }
 
-            // ---- mask: keys that do not exist in this tile
-            if constexpr (NA) {
-                // columns past this tile's keys (N = KH * 16 < 128) hold stale
-                // values: whole 16-column groups, warp-uniform
+            // ---- masks
+            if constexpr (NA && !PEN) {
+                // the h and w window tests per key (f16, whose range cannot hold
+                // a window penalty, and bf16 without penalty channels).  Key e of the (KT, KH, 16)
+                // sub-box sits at h = kh0 + (e / 16) % KH, w = kw0 + e % 16; wm / hm
+                // hold the in-window w columns / h rows of this row.
+                const int lw = wsw - kw0, lh = wsh - kh0;
+                const int aw = imax(lw, 0), bw = imin(lw + p.ew, kKW);
+                const int ah = imax(lh, 0), bh_ = imin(lh + p.eh, KH);
+                const uint32_t wm = aw < bw ? ((1u << bw) - 1u) & ~((1u << aw) - 1u) : 0u;
+                const uint32_t hm = ah < bh_ ? ((1u << bh_) - 1u) & ~((1u << ah) - 1u) : 0u;
 #pragma unroll
-                for (int gq = 0; gq < kBN / 16; ++gq)
-                    if (gq * 16 >= BNt) {
+                for (int gq = 0; gq < NG; ++gq) {
+                    const bool hin = (hm >> (gq % KH)) & 1u;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) sv[gq * 16 + i] = -INFINITY;
-                    }
-                if constexpr (F16) {
-                    // f16: the h and w window tests per key.  Key e of the
-                    // (1, KH, 16) sub-box sits at h = kh0 + e / 16, w = kw0 + e % 16;
-                    // wm / hm hold the in-window w columns / h rows of this row.
-                    const int lw = wsw - kw0, lh = wsh - kh0;
-                    const int aw = imax(lw, 0), bw = imin(lw + p.ew, kKW);
-                    const int ah = imax(lh, 0), bh_ = imin(lh + p.eh, kBN / kKW);
-                    const uint32_t wm = aw < bw ? ((1u << bw) - 1u) & ~((1u << aw) - 1u) : 0u;
-                    const uint32_t hm = ah < bh_ ? ((1u << bh_) - 1u) & ~((1u << ah) - 1u) : 0u;
-#pragma unroll
-                    for (int gq = 0; gq < kBN / 16; ++gq) {
-                        const bool hin = (hm >> gq) & 1u;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (!hin || !((wm >> i) & 1u)) sv[gq * 16 + i] = -INFINITY;
-                    }
+                    for (int i = 0; i < 16; ++i)
+                        if (!hin || !((wm >> i) & 1u)) sv[gq * 16 + i] = -INFINITY;
                 }
-            } else {
-                int valid = p.Nkv - j * kBN;           // keys of this tile inside the sequence
+            } else if constexpr (!NA) {
+                int valid = p.Nkv - j * BNt;           // keys of this tile inside the sequence
                 if constexpr (CAUSAL) {
                     // the last tile is the diagonal one (query tile and key tile
                     // start at the same position): key e is visible to row `row`
                     // iff e <= row
                     if (j == nt - 1) {
 #pragma unroll
-                        for (int e = 0; e < kBN; ++e)
+                        for (int e = 0; e < BNt; ++e)
                             if (e > row || e >= valid) sv[e] = -INFINITY;
-                        valid = kBN;
+                        valid = BNt;
                     }
                 }
-                if (valid < kBN) {
+                if (valid < BNt) {
 #pragma unroll
-                    for (int e = 0; e < kBN; ++e)
+                    for (int e = 0; e < BNt; ++e)
                         if (e >= valid) sv[e] = -INFINITY;
                 }
             }
 
-            // P = 2^(x - m) in 16-bit into TMEM; returns the tile's row sum (fp32)
-            auto emit_p = [&](float nmu) -> float {
+            // P = 2^(x - m) in 16-bit into TMEM (groups outside gm: P = 0);
+            // returns the tile's row sum (fp32)
+            auto emit_p = [&](float nmu, uint32_t gm) -> float {
                 float acc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    if (c * 32 >= BNt) break;
+                for (int c = 0; c < BNt / 32; ++c) {
+                    const float n0 = ((gm >> (2 * c)) & 1u) ? nmu : -INFINITY;
+                    const float n1 = ((gm >> (2 * c + 1)) & 1u) ? nmu : -INFINITY;
                     uint32_t pk[16];
-                    // the upper 16 keys of the last 32-key chunk may lie past the tile
-                    const int ne = (c * 32 + 32 <= BNt) ? 16 : 8;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        if (e >= 8 && ne == 8) {
-                            pk[e] = 0u;
-                            continue;
-                        }
+                        const float nm = e < 8 ? n0 : n1;
                         float x0, x1;
-                        ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nmu,
-                                   nmu);
+                        ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nm, nm);
                         const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                         ptx::fadd2(acc[(2 * e) & 7], acc[(2 * e + 1) & 7], acc[(2 * e) & 7],
                                    acc[(2 * e + 1) & 7], p0, p1);
@@ -728,6 +841,19 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             };
 
+            // ---- P in columns of its own (one buffer): the P V product that
+            //      last read them (key tile j - 1) must be done.  P over S needs no
+            //      wait: the Q K^T that wrote this S was issued after the P V that
+            //      read the P last held here, and MMAs complete in issue order.
+            bool prev_done = false;              // P V of tile j - 1 observed complete
+            if (C::SEP_P && j >= 1) {
+                if (!wait_pv(j - 1)) {
+                    ok = false;
+                    break;
+                }
+                prev_done = true;
+            }
+
             // ---- fast path: exponentiate against the running maximum m as it
             //      stands, with no tile maximum.  P only has to stay finite in its
             //      16-bit type, not below 1: a tile whose row sum exceeds 2^24 (2^15
@@ -736,20 +862,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             //      first tiles were all outside its window) is redone below
             //      against its own maximum.  After the first tiles m is close to
             //      the row maximum and the redo almost never runs.
-            bool fast = j > 0 && __all_sync(0xffffffffu, !(t_ok && m == -INFINITY));
-            bool waited = false;                 // o_done of step j - 1 observed
+            bool fast = j > 0 && __all_sync(0xffffffffu, !(gmask != 0u && m == -INFINITY));
             if (fast) {
-                if constexpr (C::SEP_P) {
-                    // P_t has columns of its own: the previous P V must have read them
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
-                                                                         p.err, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    waited = true;
-                }
-                const float lt = emit_p(t_ok ? -m : -INFINITY);
+                const float lt = emit_p(-m, gmask);
                 if (__any_sync(0xffffffffu, !(lt <= (F16 ? 32768.f : 16777216.f))))
                     fast = false;                 // redo the tile (P is rewritten below)
                 else
@@ -757,28 +872,27 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             }
 
             if (!fast) {
-                // ---- tile maximum
-                float mx[8];
+                // ---- tile maximum over the groups this row may see
+                float tmax = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
+                for (int gq = 0; gq < NG; ++gq) {
+                    float mx[8];
 #pragma unroll
-                for (int e = 16; e < kBN; e += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx[i] = ptx::fmax3(mx[i], sv[e + i], sv[e + 8 + i]);
-                const float tmax = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
-                                              ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-                const float mt = t_ok ? tmax * cl : -INFINITY;   // cl > 0: max commutes with the scaling
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[gq * 16 + i], sv[gq * 16 + 8 + i]);
+                    const float gmx = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
+                                                 ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                    if ((gmask >> gq) & 1u) tmax = fmaxf(tmax, gmx);
+                }
+                const float mt = tmax * cl;      // cl > 0: max commutes with the scaling
 
-                // ---- the previous P V must be done before O is rescaled or P_t rewritten
+                // ---- the previous P V must be done before O is rescaled
                 const bool want = j == 0 || mt > m + 8.f;   // this row moves its maximum
                 const bool any_want = __any_sync(0xffffffffu, want);
-                if (j > 0 && !waited && (C::SEP_P || any_want)) {
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], (j - 1) & 1,
-                                                                         p.err, abort))) {
+                if (j > 0 && any_want && !prev_done) {
+                    if (!wait_pv(j - 1)) {
                         ok = false;
                         break;
                     }
-                    ptx::tc_fence_after();
                 }
                 // ---- running maximum (moved lazily) and O rescale in TMEM
                 if (j == 0) {
@@ -806,19 +920,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         m = mt;
                     }
                 }
-                // (a row whose t window misses this key sub-box gets P = 0)
-                l += emit_p(!t_ok ? -INFINITY : (m == -INFINITY) ? 0.f : -m);
+                l += emit_p((m == -INFINITY) ? 0.f : -m, gmask);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bars->p_ready[t]);
+            ptx::mbar_arrive(&bars->p_ready[2 * t + C::buf_of(j)]);
         }
 
         // ---- epilogue: O / l -> bf16 -> global
-        if (ok && nt > 0 &&
-            __all_sync(0xffffffffu,
-                       ptx::mbar_wait_or_abort(&bars->o_done[t], (nt - 1) & 1, p.err, abort))) {
-            ptx::tc_fence_after();
+        if (ok && nt > 0 && wait_pv(nt - 1)) {
             const float inv = 1.f / l;
             typename H16<F16>::T *orow = nullptr;
             if (qvalid) {
@@ -1020,13 +1130,13 @@ bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool NA, bool CAUSAL = false, int KHC = 0, bool F16 = false>
+template <int D, bool NA, bool CAUSAL = false, int KSH = 0, bool F16 = false>
 attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
-    using C = TcCfg<D, NA>;
+    using C = TcCfg<D, NA, na_penalty<NA, F16>()>;
     static int done_mask = 0;
     static int regs = -1;
-    auto kern = tc_attn_kernel<D, NA, CAUSAL, KHC, F16>;
+    auto kern = tc_attn_kernel<D, NA, CAUSAL, KSH, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     // The warpgroups re-split the launch's register file with setmaxnreg; the
@@ -1044,26 +1154,27 @@ attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
     return launch_status(NA ? kFamTcNa : kFamTcFlash);
 }
 
-// Query box and key sub-box height for the neighborhood path: at most 128
-// queries per box, minimising the (query row, key) slots the MMAs compute over
-// all boxes (boxes x tiles x (KH*16 + per-tile overhead)).
-bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KH) {
+// Query box and key sub-box for the neighborhood path: at most 128 queries
+// per box and key tiles of KT frames x KH rows x 16 columns (KT KH = 6, 96
+// keys), minimising the key tiles -- i.e. the (query row, key) slots the MMAs
+// compute -- over all boxes.
+bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KT, int &KH) {
     const int ext[3] = {T, Hg, W};
+    constexpr int kShapes[4][2] = {{1, 6}, {2, 3}, {3, 2}, {6, 1}};
     double best = -1;
     for (int cbt = 1; cbt <= imin(T, 128); ++cbt)
         for (int cbh = 1; cbh <= imin(Hg, 128 / cbt); ++cbh)
             for (int cbw = 1; cbw <= imin(W, 128 / (cbt * cbh)); ++cbw) {
                 if (cbt * cbh * cbw < imin(64, T * Hg * W)) continue;   // keep MMA rows busy
                 if (cbh + cbw > 16) continue;                // h and w offsets fit 16 channels
-                // key tiles of 64..128 keys keep the MMAs large enough to amortise
-                // the per-tile barrier round trips
-                for (int ckh = imin(4, imin(kern[1], Hg) + cbh - 1); ckh <= 8; ++ckh) {
+                for (const auto &sh : kShapes) {
+                    const int ckt = sh[0], ckh = sh[1];
                     // distinct key penalty tiles of a box (h chunks x w chunks) must fit
                     const int nh_max = cdiv(imin(cbh + imin(kern[1], Hg) - 1, Hg), ckh);
                     const int nw_max = cdiv(imin(cbw + imin(kern[2], W) - 1, W), kKW);
-                    if (nh_max * nw_max > 6) continue;
-                    // total key slots over all boxes = sum_t(ut) * sum_h(nhc) * sum_w(nwc) * KH*16
-                    const int b[3] = {cbt, cbh, cbw};
+                    if (nh_max * nw_max > kMaxPenaltyTiles) continue;
+                    // key tiles over all boxes = sum_t(t chunks) * sum_h(h chunks) * sum_w(w chunks)
+                    const int b[3] = {cbt, cbh, cbw}, chunk[3] = {ckt, ckh, kKW};
                     double axis[3];
                     for (int a = 0; a < 3; ++a) {
                         const int keff = imin(kern[a], ext[a]);
@@ -1072,19 +1183,17 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
                             const int i1 = imin(i0 + b[a], ext[a]) - 1;
                             const int u = na_window_start(i1, ext[a], kern[a]) + keff -
                                           na_window_start(i0, ext[a], kern[a]);
-                            acc += a == 0 ? u : a == 1 ? cdiv(u, ckh) : cdiv(u, kKW);
+                            acc += cdiv(u, chunk[a]);
                         }
                         axis[a] = acc;
                     }
                     const int nbw = cdiv(W, cbw);
                     // odd box count along w leaves one query tile idle per (t, h) box row
                     const double w_pairs_waste = (nbw & 1) ? double(nbw + 1) / nbw : 1.0;
-                    // every box is one 128-row query tile: computed (row, key) slots
-                    // (a tile costs its key slots plus a fixed overhead of ~32 key slots)
-                    const double cost = axis[0] * axis[1] * axis[2] * (ckh * kKW + 32) * w_pairs_waste;
+                    const double cost = axis[0] * axis[1] * axis[2] * w_pairs_waste;
                     if (best < 0 || cost < best) {
                         best = cost;
-                        bt = cbt; bh = cbh; bw = cbw; KH = ckh;
+                        bt = cbt; bh = cbh; bw = cbw; KT = ckt; KH = ckh;
                     }
                 }
             }
@@ -1093,7 +1202,7 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
 
 // Plans are cached per (grid, kernel): the search is a few thousand candidates.
 struct NaPlan {
-    int bt, bh, bw, KH;
+    int bt, bh, bw, KT, KH;
     bool ok;
 };
 
@@ -1113,7 +1222,7 @@ NaPlan cached_plan(int T, int Hg, int W, const int kern[3]) {
         if (same) return cache[i].plan;
     }
     NaPlan pl{};
-    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KH);
+    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KT, pl.KH);
     Entry &e = cache[used < 64 ? used++ : 63];
     for (int a = 0; a < 6; ++a) e.key[a] = key[a];
     e.plan = pl;
@@ -1216,11 +1325,11 @@ attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *
     TcParams p{};
     const NaPlan pl = cached_plan(T, Hg, W, kernel);
     if (!pl.ok) return ATTN_ERR_UNSUPPORTED;
-    p.bt = pl.bt; p.bh = pl.bh; p.bw = pl.bw; p.KH = pl.KH;
+    p.bt = pl.bt; p.bh = pl.bh; p.bw = pl.bw; p.KT = pl.KT; p.KH = pl.KH;
     CUtensorMap tq, tk, tv;
     const uint64_t dims[5] = {uint64_t(D), uint64_t(W), uint64_t(Hg), uint64_t(T), uint64_t(B) * H};
     const uint32_t qbox[5] = {64, uint32_t(p.bw), uint32_t(p.bh), uint32_t(p.bt), 1};
-    const uint32_t kbox[5] = {64, uint32_t(kKW), uint32_t(p.KH), 1, 1};
+    const uint32_t kbox[5] = {64, uint32_t(kKW), uint32_t(p.KH), uint32_t(p.KT), 1};
     if (!make_tmap(&tq, q, 5, dims, qbox, f16) || !make_tmap(&tk, k, 5, dims, kbox, f16) ||
         !make_tmap(&tv, v, 5, dims, kbox, f16))
         return ATTN_ERR_CUDA;
@@ -1245,14 +1354,12 @@ attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *
     p.nbw = cdiv(W, p.bw);
     p.nbw2 = cdiv(p.nbw, 2);
     const dim3 grid(cdiv(T, p.bt) * p.nbh * p.nbw2, B * H);
-    // the planner's key sub-box heights (4..8) have compile-time kernels (bf16)
+    // the planner's key sub-box shapes have compile-time kernels (bf16)
     if (f16) return launch_tc<64, true, false, 0, true>(c, tq, tk, tv, p, grid);
-    switch (p.KH) {
-        case 4: return launch_tc<64, true, false, 4>(c, tq, tk, tv, p, grid);
-        case 5: return launch_tc<64, true, false, 5>(c, tq, tk, tv, p, grid);
-        case 6: return launch_tc<64, true, false, 6>(c, tq, tk, tv, p, grid);
-        case 7: return launch_tc<64, true, false, 7>(c, tq, tk, tv, p, grid);
-        case 8: return launch_tc<64, true, false, 8>(c, tq, tk, tv, p, grid);
+    switch (p.KT * 10 + p.KH) {
+        case 16: return launch_tc<64, true, false, 16>(c, tq, tk, tv, p, grid);
+        case 23: return launch_tc<64, true, false, 23>(c, tq, tk, tv, p, grid);
+        case 32: return launch_tc<64, true, false, 32>(c, tq, tk, tv, p, grid);
         default: return launch_tc<64, true>(c, tq, tk, tv, p, grid);
     }
 }

@@ -815,6 +815,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 }
             }
 
+            // neighborhood: 16-key groups that no row of this warp may see (a
+            // 32-key chunk whose frames lie outside all 32 rows' t windows)
+            // are written as P = 0 without exponentials
+            const uint32_t wlive = NA ? __reduce_or_sync(0xffffffffu, gmask) : ~0u;
+
             // P = 2^(x - m) in 16-bit into TMEM (groups outside gm: P = 0);
             // returns the tile's row sum (fp32)
             auto emit_p = [&](float nmu, uint32_t gm) -> float {
@@ -823,9 +828,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
                 for (int c = 0; c < BNt / 32; ++c) {
+                    uint32_t pk[16];
+                    if (((wlive >> (2 * c)) & 3u) == 0u) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                        ptx::tmem_st16(p_addr + c * 16, pk);
+                        continue;
+                    }
                     const float n0 = ((gm >> (2 * c)) & 1u) ? nmu : -INFINITY;
                     const float n1 = ((gm >> (2 * c + 1)) & 1u) ? nmu : -INFINITY;
-                    uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const float nm = e < 8 ? n0 : n1;

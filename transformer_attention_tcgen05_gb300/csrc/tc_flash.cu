@@ -335,7 +335,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         n_t[0] = n_t[1] = steps;
     }
 
-    if (threadIdx.x == 0) {
+    // Barrier set-up by the last warp, channel building by the others (the
+    // two run side by side; one thread's ~25 barrier inits take ~0.5 us).
+    constexpr int NBUILD = C::NT - 32;
+    if (threadIdx.x == C::NT - 32) {
         ptx::mbar_init(&bars->q_full, 1);
         // a stage is free once every MMA issuer has released it
         for (int s = 0; s < C::KS; ++s) {
@@ -362,8 +365,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     if constexpr (NA) {
         // query rows past the box (box smaller than 128 rows) hold zeros, not stale data
         const int rows = p.bt * p.bh * p.bw;
-        if (rows < kBM) {
-            for (int i = threadIdx.x; i < kNQ * C::PANELS * (kBM - rows) * 8; i += C::NT) {
+        if (rows < kBM && threadIdx.x < NBUILD) {
+            for (int i = threadIdx.x; i < kNQ * C::PANELS * (kBM - rows) * 8; i += NBUILD) {
                 const int chunk = i % 8, r = rows + (i / 8) % (kBM - rows);
                 const int pt = i / (8 * (kBM - rows));          // (tile, panel)
                 *reinterpret_cast<uint4 *>(smem + C::OFF_Q + pt * C::PANEL_Q + r * 128 + chunk * 16) =
@@ -373,54 +376,85 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     }
     if constexpr (PEN) {
         const int rows = p.bt * p.bh * p.bw;
-        // one-hot window-offset channels of every query row: channel dh, then
-        // bh + dw (rows past the box: all zero)
-        for (int i = threadIdx.x; i < kNQ * kBM * 2; i += C::NT) {
-            const int t = i / (kBM * 2), r = (i / 2) % kBM, half = i % 2;
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            if (r < rows) {
-                const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
-                const int ch[2] = {dh, p.bh + dw};
-#pragma unroll
-                for (int a = 0; a < 2; ++a) {
-                    const int c = ch[a] - half * 8;
-                    if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
+        // Window channels.  Query row r carries a one in channel dh (its h
+        // offset in the box) and in channel bh + dw; key (h, w) of a penalty
+        // tile carries -penalty in channel c < bh if h lies outside the h
+        // window of box row offset c, in channel bh + c' if w lies outside the
+        // w window of box column offset c'.  The violations depend on the key's
+        // h row or w column alone: they are tabulated first as 16-bit channel
+        // masks per union row / column of each stream (in the V ring, not yet
+        // in use), and every penalty row is then expanded from the OR of two
+        // table entries.
+        // table rows per stream and axis: a box has at most kMaxPenaltyTiles
+        // (h chunk, w chunk) pairs, so <= 8 chunks of <= 6 rows or 16 columns
+        constexpr int TAB = kMaxPenaltyTiles * kKW;
+        static_assert(kMaxPenaltyTiles * 6 <= TAB && 2 * C::STREAMS * TAB * 2 <= C::STAGE_BYTES,
+                      "window tables fit their rows and one V stage");
+        uint16_t *hmask = reinterpret_cast<uint16_t *>(smem + C::OFF_V);   // [STREAMS][TAB]
+        uint16_t *wmask = hmask + C::STREAMS * TAB;                         // [STREAMS][TAB]
+        if (threadIdx.x < NBUILD) {
+            for (int i = threadIdx.x; i < 2 * C::STREAMS * TAB; i += NBUILD) {
+                const int axis = i / (C::STREAMS * TAB), u = (i / TAB) % C::STREAMS, e = i % TAB;
+                const NaTile gu = pick(g, u);    // (selects: a run-time index would spill g)
+                if (gu.ntiles == 0) continue;
+                uint32_t m = 0u;
+                if (axis == 0 && e < gu.nhc * KH) {
+                    const int kh = gu.u0h + e;
+                    for (int c = 0; c < p.bh; ++c) {
+                        const int sh = na_window_start(imin(gu.h0 + c, p.Hg - 1), p.Hg, p.kh);
+                        if (unsigned(kh - sh) >= unsigned(p.eh)) m |= 1u << c;
+                    }
+                } else if (axis == 1 && e < gu.nwc * kKW) {
+                    const int kw = gu.u0w + e;
+                    for (int c = 0; c < p.bw; ++c) {
+                        const int sw = na_window_start(imin(gu.w0 + c, p.W - 1), p.W, p.kw);
+                        if (unsigned(kw - sw) >= unsigned(p.ew)) m |= 1u << (p.bh + c);
+                    }
                 }
+                (axis == 0 ? hmask : wmask)[u * TAB + e] = uint16_t(m);
             }
-            *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW + ptx::sw32_offset(r, half)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            // one-hot offset channels of every query row (rows past the box: zero)
+            for (int i = threadIdx.x; i < kNQ * kBM * 2; i += NBUILD) {
+                const int t = i / (kBM * 2), r = (i / 2) % kBM, half = i % 2;
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (r < rows) {
+                    const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
+                    const int ch[2] = {dh, p.bh + dw};
+#pragma unroll
+                    for (int a = 0; a < 2; ++a) {
+                        const int c = ch[a] - half * 8;
+                        if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
+                    }
+                }
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW + ptx::sw32_offset(r, half)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
-        // key-side penalty tiles: for key (h, w) of the sub-box of h chunk hc and
-        // w chunk wc, channel dh holds -penalty if h lies outside the h window of
-        // query offset dh, channel bh + dw likewise for w
+        __syncthreads();
         const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
         const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
+        if (threadIdx.x < NBUILD) {
 #pragma unroll
-        for (int u = 0; u < C::STREAMS; ++u) {
-            if (n_t[u] == 0) continue;
-            const int nv = g[u].nhc * g[u].nwc;
-            for (int i = threadIdx.x; i < nv * BNt * 2; i += C::NT) {
-                const int v = i / (BNt * 2), r = (i / 2) % BNt, half = i % 2;
-                // key r of the sub-box: w column r % 16, h row (r / 16) % KH
-                // (the same for each of its KT frames)
-                const int kh = g[u].u0h + (v / g[u].nwc) * KH + (r / kKW) % KH;
-                const int kw = g[u].u0w + (v % g[u].nwc) * kKW + r % kKW;
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int u = 0; u < C::STREAMS; ++u) {
+                if (n_t[u] == 0) continue;
+                const int nv = g[u].nhc * g[u].nwc;
+                for (int i = threadIdx.x; i < nv * BNt * 2; i += NBUILD) {
+                    const int half = i & 1, r = (i >> 1) % BNt, v = (i >> 1) / BNt;
+                    // key r of sub-box v: h row (v / nwc) KH + (r / 16) % KH, w
+                    // column (v % nwc) 16 + r % 16 of the union (the same for
+                    // each of its KT frames)
+                    const int hc = v / g[u].nwc, wc = v - hc * g[u].nwc;
+                    const uint32_t m = uint32_t(hmask[u * TAB + hc * KH + (r / kKW) % KH]) |
+                                       uint32_t(wmask[u * TAB + wc * kKW + r % kKW]);
+                    const uint32_t bits = (m >> (half * 8)) & 0xffu;
+                    uint32_t w[4];
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const int c = half * 8 + cc;
-                    bool viol = false;
-                    if (c < p.bh) {
-                        const int sh = na_window_start(imin(g[u].h0 + c, p.Hg - 1), p.Hg, p.kh);
-                        viol = unsigned(kh - sh) >= unsigned(p.eh);
-                    } else if (c < p.bh + p.bw) {
-                        const int sw = na_window_start(imin(g[u].w0 + c - p.bh, p.W - 1), p.W, p.kw);
-                        viol = unsigned(kw - sw) >= unsigned(p.ew);
-                    }
-                    if (viol) w[cc >> 1] |= neg << ((cc & 1) * 16);
+                    for (int cc = 0; cc < 4; ++cc)
+                        w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
+                                (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
+                    *reinterpret_cast<uint4 *>(smem + C::kxv_off(u, v) + ptx::sw32_offset(r, half)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *reinterpret_cast<uint4 *>(smem + C::kxv_off(u, v) + ptx::sw32_offset(r, half)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
         ptx::fence_proxy_async_smem();

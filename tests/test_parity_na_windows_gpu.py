@@ -72,7 +72,10 @@ def _dev(x: np.ndarray, dtype: str):
 
 
 # (grid, kernel, heads): the pages' two clamp shapes at D = 64, the large
-# workload's grid, and odd/even extents where windows clamp on some axes.
+# workload's grid, and odd/even extents where windows clamp on some axes.  The
+# kernel runs one CTA per SM over (box pair, head) items, so the many-head
+# cases give every CTA several items whose window geometry changes from one
+# to the next ((1, 4, 4) also leaves the second box of every pair empty).
 CASES = [
     ((9, 64, 64), (11, 11, 11), 1),
     ((21, 60, 104), (11, 11, 11), 1),
@@ -82,6 +85,8 @@ CASES = [
     ((7, 8, 9), (7, 9, 11), 2),
     ((3, 11, 50), (1, 3, 49), 1),
     ((5, 1, 30), (9, 5, 3), 1),
+    ((1, 4, 4), (3, 7, 7), 400),
+    ((4, 6, 33), (5, 7, 9), 64),
 ]
 
 

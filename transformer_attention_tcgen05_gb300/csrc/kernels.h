@@ -1,6 +1,7 @@
 // Host-side launchers of libattn's kernels (internal; the public ABI is include/libattn.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -38,6 +39,13 @@ attn_status_t launch_status(int family);
 
 // Sets the dynamic shared-memory limit of `func` once per device.
 bool ensure_smem_attr(const void *func, size_t bytes, int device, int *done_mask);
+
+// 16-bit (bf16 or f16) TMA tensor map with 128-byte swizzle; dims and box
+// innermost first (dims[0] = D), the tensor packed.  False if the driver's
+// encoder is unavailable or rejects the map.
+bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint32_t *box,
+               bool f16 = false);
+bool tma_encode_available();
 
 // Element strides of a [B, heads, N, D] tensor with D contiguous.
 struct TensorStrides {

@@ -1135,46 +1135,6 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
 }
 
-// ------------------------------------------------------------- host side
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
-// 16-bit (bf16 or f16) tensor map with 128-byte swizzle; dims/box innermost
-// first (dims[0] = D).
-bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-               const uint32_t *box, bool f16 = false) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gdim[5], gstride[4];
-    cuuint32_t bdim[5], estr[5];
-    uint64_t stride = 2;
-    for (int i = 0; i < rank; ++i) {
-        gdim[i] = dims[i];
-        bdim[i] = box[i];
-        estr[i] = 1;
-        if (i > 0) gstride[i - 1] = stride;
-        stride *= dims[i];
-    }
-    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-              const_cast<void *>(base), gdim, gstride,
-              bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, bool NA, bool CAUSAL = false, int KSH = 0, bool F16 = false>
 attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
@@ -1199,82 +1159,47 @@ attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
     return launch_status(NA ? kFamTcNa : kFamTcFlash);
 }
 
-// Query box and key sub-box for the neighborhood path: at most 128 queries
-// per box and key tiles of KT frames x KH rows x 16 columns (KT KH = 6, 96
-// keys), minimising the key tiles -- i.e. the (query row, key) slots the MMAs
-// compute -- over all boxes.
-bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KT, int &KH) {
-    const int ext[3] = {T, Hg, W};
-    constexpr int kShapes[4][2] = {{1, 6}, {2, 3}, {3, 2}, {6, 1}};
-    double best = -1;
-    for (int cbt = 1; cbt <= imin(T, 128); ++cbt)
-        for (int cbh = 1; cbh <= imin(Hg, 128 / cbt); ++cbh)
-            for (int cbw = 1; cbw <= imin(W, 128 / (cbt * cbh)); ++cbw) {
-                if (cbt * cbh * cbw < imin(64, T * Hg * W)) continue;   // keep MMA rows busy
-                if (cbh + cbw > 16) continue;                // h and w offsets fit 16 channels
-                for (const auto &sh : kShapes) {
-                    const int ckt = sh[0], ckh = sh[1];
-                    // distinct key penalty tiles of a box (h chunks x w chunks) must fit
-                    const int nh_max = cdiv(imin(cbh + imin(kern[1], Hg) - 1, Hg), ckh);
-                    const int nw_max = cdiv(imin(cbw + imin(kern[2], W) - 1, W), kKW);
-                    if (nh_max * nw_max > kMaxPenaltyTiles) continue;
-                    // key tiles over all boxes = sum_t(t chunks) * sum_h(h chunks) * sum_w(w chunks)
-                    const int b[3] = {cbt, cbh, cbw}, chunk[3] = {ckt, ckh, kKW};
-                    double axis[3];
-                    for (int a = 0; a < 3; ++a) {
-                        const int keff = imin(kern[a], ext[a]);
-                        double acc = 0;
-                        for (int i0 = 0; i0 < ext[a]; i0 += b[a]) {
-                            const int i1 = imin(i0 + b[a], ext[a]) - 1;
-                            const int u = na_window_start(i1, ext[a], kern[a]) + keff -
-                                          na_window_start(i0, ext[a], kern[a]);
-                            acc += cdiv(u, chunk[a]);
-                        }
-                        axis[a] = acc;
-                    }
-                    const int nbw = cdiv(W, cbw);
-                    // odd box count along w leaves one query tile idle per (t, h) box row
-                    const double w_pairs_waste = (nbw & 1) ? double(nbw + 1) / nbw : 1.0;
-                    const double cost = axis[0] * axis[1] * axis[2] * w_pairs_waste;
-                    if (best < 0 || cost < best) {
-                        best = cost;
-                        bt = cbt; bh = cbh; bw = cbw; KT = ckt; KH = ckh;
-                    }
-                }
-            }
-    return best > 0;
-}
-
-// Plans are cached per (grid, kernel): the search is a few thousand candidates.
-struct NaPlan {
-    int bt, bh, bw, KT, KH;
-    bool ok;
-};
-
-NaPlan cached_plan(int T, int Hg, int W, const int kern[3]) {
-    struct Entry {
-        int key[6];
-        NaPlan plan;
-    };
-    static std::mutex mu;
-    static Entry cache[64];
-    static int used = 0;
-    const int key[6] = {T, Hg, W, kern[0], kern[1], kern[2]};
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i) {
-        bool same = true;
-        for (int a = 0; a < 6; ++a) same = same && cache[i].key[a] == key[a];
-        if (same) return cache[i].plan;
-    }
-    NaPlan pl{};
-    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KT, pl.KH);
-    Entry &e = cache[used < 64 ? used++ : 63];
-    for (int a = 0; a < 6; ++a) e.key[a] = key[a];
-    e.plan = pl;
-    return pl;
-}
-
 }  // namespace
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool make_tmap(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+               const uint32_t *box, bool f16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t bdim[5], estr[5];
+    uint64_t stride = 2;
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) gstride[i - 1] = stride;
+        stride *= dims[i];
+    }
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+              const_cast<void *>(base), gdim, gstride,
+              bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tma_encode_available() { return encode_fn() != nullptr; }
 
 // 4D map {D, N, heads, B} over a tensor with element strides (row, head,
 // batch) and D contiguous; 128-byte swizzle, box {64, 128, 1, 1}.
@@ -1356,57 +1281,6 @@ attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const 
                         : launch_tc<64, false, true, 0, true>(c, tq, tk, tv, p, grid);
     return D == 128 ? launch_tc<128, false, true>(c, tq, tk, tv, p, grid)
                     : launch_tc<64, false, true>(c, tq, tk, tv, p, grid);
-}
-
-bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]) {
-    return D == 64 && B * H <= 65535 && encode_fn() != nullptr &&
-           cached_plan(T, Hg, W, kernel).ok;
-}
-
-attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
-                      void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
-                      float scale) {
-    const bool f16 = dt == ATTN_F16;
-    TcParams p{};
-    const NaPlan pl = cached_plan(T, Hg, W, kernel);
-    if (!pl.ok) return ATTN_ERR_UNSUPPORTED;
-    p.bt = pl.bt; p.bh = pl.bh; p.bw = pl.bw; p.KT = pl.KT; p.KH = pl.KH;
-    CUtensorMap tq, tk, tv;
-    const uint64_t dims[5] = {uint64_t(D), uint64_t(W), uint64_t(Hg), uint64_t(T), uint64_t(B) * H};
-    const uint32_t qbox[5] = {64, uint32_t(p.bw), uint32_t(p.bh), uint32_t(p.bt), 1};
-    const uint32_t kbox[5] = {64, uint32_t(kKW), uint32_t(p.KH), uint32_t(p.KT), 1};
-    if (!make_tmap(&tq, q, 5, dims, qbox, f16) || !make_tmap(&tk, k, 5, dims, kbox, f16) ||
-        !make_tmap(&tv, v, 5, dims, kbox, f16))
-        return ATTN_ERR_CUDA;
-    p.c_log2 = scale * kLog2e;
-    // bf16 penalty per violated axis: a power of two (exact in bf16), at least
-    // 2^100 and with penalty * scale * log2(e) >= 300.  A masked key's score is
-    // then raw - penalty (or - 2 penalty) <= -2^99 whenever |raw| < 2^98, so
-    // 2^(x - m) underflows to exactly 0 however far its raw score lies above
-    // the row's in-window scores; up to 2^125 two penalties still fit fp32.
-    // (f16 masks in the softmax and does not use it.)
-    {
-        const int e = imax(100, int(ceilf(log2f(300.f / p.c_log2))));
-        if (!f16 && e > 125) return ATTN_ERR_UNSUPPORTED;   // scale below ~1e-28
-        p.penalty = ldexpf(1.f, imin(e, 125));
-    }
-    p.o = o;
-    p.err = c.err;
-    p.T = T; p.Hg = Hg; p.W = W;
-    p.kt = kernel[0]; p.kh = kernel[1]; p.kw = kernel[2];
-    p.et = imin(kernel[0], T); p.eh = imin(kernel[1], Hg); p.ew = imin(kernel[2], W);
-    p.nbh = cdiv(Hg, p.bh);
-    p.nbw = cdiv(W, p.bw);
-    p.nbw2 = cdiv(p.nbw, 2);
-    const dim3 grid(cdiv(T, p.bt) * p.nbh * p.nbw2, B * H);
-    // the planner's key sub-box shapes have compile-time kernels (bf16)
-    if (f16) return launch_tc<64, true, false, 0, true>(c, tq, tk, tv, p, grid);
-    switch (p.KT * 10 + p.KH) {
-        case 16: return launch_tc<64, true, false, 16>(c, tq, tk, tv, p, grid);
-        case 23: return launch_tc<64, true, false, 23>(c, tq, tk, tv, p, grid);
-        case 32: return launch_tc<64, true, false, 32>(c, tq, tk, tv, p, grid);
-        default: return launch_tc<64, true>(c, tq, tk, tv, p, grid);
-    }
 }
 
 attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,

@@ -1,0 +1,1026 @@
+// Persistent tensor-core (tcgen05 + TMEM + TMA) 3D neighborhood attention for
+// bf16 and f16, sm_103a: the neighborhood attention of candle PR #11 ("3D
+// neighborhood attention", NATTEN boundary windows: window start
+// clamp(i - k/2, 0, n - k_eff) per axis), computed as a fused flash-style
+// kernel whose scores never leave the SM.
+//
+// Work item = two 3D query boxes adjacent in w (<= 128 queries each) of one
+// (batch, head).  One CTA per SM walks items blockIdx.x, + gridDim.x, ...,
+// so the CTAs in flight always hold neighbouring boxes of one head (their key
+// windows overlap in L2), and the set-up that a CTA per item paid every time
+// (barriers, tensor memory, the query-offset channels, the first copies and
+// the first Q K^T) is paid once or hidden behind the previous item: the K and
+// V loaders stream the next item's key tiles as soon as ring stages free up,
+// the next item's queries load once the last Q K^T of the current one has
+// completed, and its first two Q K^T are issued while the softmax warps are
+// still writing out the current item's outputs.
+//
+// Per item and query tile t the keys are the union of the box's clamped
+// windows (a 3D box again, the window start being monotone), streamed as
+// (KT, KH, 16) key sub-boxes of 96 keys by 5D TMA, K and V in rings of their
+// own.  bf16 applies the h and w window tests on the tensor core: every query
+// row carries 16 one-hot channels (its h and w offset inside the box) and
+// every key sub-box 16 matching channels holding -2^100 (at least; see the
+// host) where the key lies outside the window of that offset, so one extra
+// 16-deep MMA step adds -2^100 per violated axis to S and every masked key
+// gets P = 0 exactly whenever the raw scores are below 2^98 in magnitude.  f16
+// cannot hold such a penalty and tests h and w per key in the softmax.  The t
+// window is tested per 16-key group (one frame of the sub-box).
+//
+// The key-side penalty channels of a box depend only on the box's window
+// geometry relative to its union (chunk counts and where the clamped window
+// starts stop advancing), so a tile rebuilds them only when that changes from
+// its previous item: the interior boxes of a grid all share one set.
+//
+// Warps: 0-3 softmax of query tile 0 (thread = query row = TMEM lane), 4-7 of
+// tile 1, 8 MMA issuer of tile 0 and TMEM owner, 9 TMA loader of Q and the K
+// ring, 10 TMA loader of the V ring, 11 MMA issuer of tile 1 (and barrier
+// set-up).  The third warpgroup drops to 72 registers (setmaxnreg) so the
+// softmax warpgroups hold a whole score row in registers (216).
+//
+// Tensor memory per query tile t: [S_t,0 | S_t,1 | O_t] (96 + 96 + 64
+// columns) at 256 t.  Key tile g of the tile (counted over all items of the
+// CTA) has its scores in buffer g % 2, and its P is written over them; the
+// issuer of tile t issues P V (g) as soon as the softmax has written P(g) and
+// right behind it Q K^T (g + 2) into the same buffer (one thread's MMAs
+// execute in order), so the next scores are ready when the softmax finishes a
+// key tile.  Every barrier is waited for phase by phase, never skipping one,
+// and each is at most one phase ahead of any waiter (argued per barrier
+// below): a parity wait cannot tell phase k from phase k + 2.
+//
+// Softmax (base 2): x = s * scale * log2(e); the first key tile sets the
+// running max m, later tiles are exponentiated against m as it stands and a
+// tile whose row sum overflows a bound (or is not finite) is redone with its
+// own max, moving m (and rescaling O in TMEM after the previous P V) only
+// when the tile max exceeds it by more than 8.  32-key chunks outside the t
+// window of all 32 rows of a warp are written as P = 0 without exponentials.
+//
+// All spin-waits are bounded (1 s); on a timeout the CTA raises the device
+// error word, lets the copies it issued land, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;            // query rows per tile (MMA M)
+constexpr int kNQ = 2;              // query tiles (boxes) per item
+constexpr int kBN = 96;             // keys per key tile: a (KT, KH, 16) sub-box, KT KH = 6
+constexpr int kD = 64;              // head dimension
+constexpr int kKW = 16;             // key sub-box width along w
+constexpr int kMaxPenaltyTiles = 8; // distinct key penalty tiles per query box
+
+template <bool PEN>
+struct NaCfg {
+    static constexpr int PANEL = kBM * 128;              // one query tile (64 channels, 128 B rows)
+    static constexpr int KV_BYTES = kBN * 128;           // one K or V tile of one query tile
+    static constexpr int STAGE_BYTES = kNQ * KV_BYTES;   // both query tiles' key tiles
+    // window channels: 16 16-bit values per row, 32-byte swizzle
+    static constexpr int X_ROW = 32;
+    static constexpr int MAXV = PEN ? kMaxPenaltyTiles : 0;
+    static constexpr int QX_BYTES = PEN ? kNQ * kBM * X_ROW : 0;
+    static constexpr int KX_BYTES = kBN * X_ROW;         // one key penalty tile
+    static constexpr int KXV_BYTES = kNQ * MAXV * KX_BYTES;
+    // violation tables per query tile: 16-bit channel masks per union h row
+    // and w column; a box has <= 8 (h chunk, w chunk) pairs, so <= 8 chunks of
+    // <= 6 rows or 16 columns per axis
+    static constexpr int TAB = kMaxPenaltyTiles * kKW;
+    static constexpr int TAB_BYTES = PEN ? kNQ * 2 * TAB * 2 : 0;
+    static constexpr int BUDGET = 227 * 1024 - 2048;
+    static constexpr int NS_ALL =
+        (BUDGET - kNQ * PANEL - QX_BYTES - KXV_BYTES - TAB_BYTES) / STAGE_BYTES;
+    // a K stage is needed a whole key tile before the V stage of the same
+    // tile, so K gets the deeper ring when the stages come out odd
+    static constexpr int KS_RAW = (NS_ALL + 1) / 2;
+    static constexpr int KS = KS_RAW > 4 ? 4 : KS_RAW;
+    static constexpr int VS = NS_ALL - KS_RAW > 4 ? 4 : NS_ALL - KS_RAW;
+    static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_QX = OFF_Q + kNQ * PANEL;
+    static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
+    static constexpr int OFF_TAB = OFF_KXV + KXV_BYTES;
+    static constexpr int OFF_K = OFF_TAB + TAB_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + VS * STAGE_BYTES;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers + 1024 B alignment slack
+    static_assert(OFF_K % 1024 == 0, "128-byte swizzled stages start on 1024-byte boundaries");
+    // tensor memory
+    static constexpr uint32_t tm_s(int t, int b) { return t * 256 + b * kBN; }
+    static constexpr uint32_t tm_o(int t) { return t * 256 + 2 * kBN; }
+    static constexpr uint32_t TM_COLS = 512;
+    static_assert(tm_o(kNQ - 1) + kD <= TM_COLS, "tensor-memory layout must fit 512 columns");
+    // warps
+    static constexpr int NSOFT = 4 * kNQ;
+    static constexpr int W_MMA = NSOFT;       // issuer of tile 0, TMEM owner
+    static constexpr int W_LOAD = NSOFT + 1;  // Q and K copies
+    static constexpr int W_LOADV = NSOFT + 2; // V copies
+    static constexpr int W_MMA1 = NSOFT + 3;  // issuer of tile 1, barrier set-up
+    static constexpr int NT = (NSOFT + 4) * 32;
+    static constexpr int NBUILD = NT - 32;    // threads that build the query channels
+    // register split: launch 168 x 384 = 64512 = 2 x 128 x 216 + 128 x 72
+    static constexpr int REGS_LAUNCH = 168;
+    static constexpr int REGS_SOFTMAX = 216;
+    static constexpr int REGS_OTHER = 72;
+    static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= NT * REGS_LAUNCH,
+                  "setmaxnreg split must fit the launch's register file share");
+    static constexpr int k_off(int s, int u) { return OFF_K + s * STAGE_BYTES + u * KV_BYTES; }
+    static constexpr int v_off(int s, int u) { return OFF_V + s * STAGE_BYTES + u * KV_BYTES; }
+    static constexpr int kxv_off(int u, int v) { return OFF_KXV + (u * MAXV + v) * KX_BYTES; }
+};
+
+struct NaParams {
+    float c_log2;            // scale * log2(e)
+    float penalty;           // bf16: power of two >= 2^100 with penalty * c_log2 >= 300
+    void *o;                 // [B * heads, T * Hg * W, 64], like the inputs
+    unsigned *err;
+    int T, Hg, W;            // grid (row-major)
+    int kt, kh, kw;          // requested kernel
+    int et, eh, ew;          // effective kernel (min(k, extent))
+    int bt, bh, bw;          // query box
+    int nbt, nbh, nbw, nbw2; // boxes along t, h, w; box pairs along w
+    int KT, KH;              // key sub-box frames and rows (KT KH 16 = 96 keys)
+    int n_items;             // box pairs x (batch x heads)
+};
+
+// Barrier block at OFF_BAR.  Phases (k counts from 0):
+//   q_full   k: the queries of the CTA's item k have landed
+//   q_free   k: every Q K^T of item k has completed (one commit per issuer)
+//   k_full / v_full [s]: the K / V tile of CTA key step s + KS n has landed
+//   k_empty / v_empty [s]: both issuers are done with that stage
+//   s_full [2 t + b]: Q K^T of tile t's key tile g (g % 2 = b) has completed
+//   p_ready[2 t + b]: the softmax has written P(g) there (128 arrivals)
+//   o_done [2 t + b]: P V (g) has completed
+//   chan_ready[t]: tile t's key penalty channels are rebuilt (128 arrivals)
+//   tab_done[t] / tab_free[t]: tile t's violation tables of rebuild k are
+//                  written / no longer read (128 arrivals; bounded waits, so
+//                  a warp that gave up on a timeout cannot strand the others
+//                  the way a named barrier would)
+template <int KS, int VS>
+struct NaBars {
+    uint64_t q_full, q_free;
+    uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+    uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
+    uint64_t chan_ready[kNQ], tab_done[kNQ], tab_free[kNQ];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// One query box and the union of its windows.
+struct NaTile {
+    int t0, h0, w0;          // box origin
+    int u0t, u0h, u0w;       // union origin
+    int ntc, nhc, nwc;       // union chunks along t, h, w (KT frames, KH rows, 16 columns)
+    int ntiles;              // key tiles = ntc nhc nwc (0 for a box past the grid)
+};
+
+__host__ __device__ __forceinline__ NaTile na_tile(const NaParams &p, int bi_t, int bi_h, int bi_w,
+                                                   int KT, int KH) {
+    NaTile g;
+    g.t0 = bi_t * p.bt;
+    g.h0 = bi_h * p.bh;
+    g.w0 = bi_w * p.bw;
+    if (bi_w >= p.nbw) {
+        g.ntiles = 0;
+        g.u0t = g.u0h = g.u0w = g.ntc = g.nhc = g.nwc = 0;
+        return g;
+    }
+    const int t1 = imin(g.t0 + p.bt, p.T) - 1, h1 = imin(g.h0 + p.bh, p.Hg) - 1,
+              w1 = imin(g.w0 + p.bw, p.W) - 1;
+    g.u0t = na_window_start(g.t0, p.T, p.kt);
+    g.u0h = na_window_start(g.h0, p.Hg, p.kh);
+    g.u0w = na_window_start(g.w0, p.W, p.kw);
+    const int ut = na_window_start(t1, p.T, p.kt) + p.et - g.u0t;
+    const int uh = na_window_start(h1, p.Hg, p.kh) + p.eh - g.u0h;
+    const int uw = na_window_start(w1, p.W, p.kw) + p.ew - g.u0w;
+    g.ntc = cdiv(ut, KT);
+    g.nhc = cdiv(uh, KH);
+    g.nwc = cdiv(uw, kKW);
+    g.ntiles = g.ntc * g.nhc * g.nwc;
+    return g;
+}
+
+// Work item it: (batch x head) it / pairs, box pair it % pairs (w pairs
+// fastest, then h, then t) -- the order of the old one-CTA-per-item grid.
+struct NaItem {
+    NaTile g[kNQ];
+    int n[kNQ];              // key tiles of each query tile
+    int steps;               // key-tile steps of the item (the larger n)
+    int bhd;                 // batch x head
+};
+
+__device__ __forceinline__ NaItem na_item(const NaParams &p, int it, int KT, int KH) {
+    NaItem I;
+    const int pairs = p.nbt * p.nbh * p.nbw2;
+    I.bhd = it / pairs;
+    const int pr = it - I.bhd * pairs;
+    const int bi_t = pr / (p.nbh * p.nbw2), bi_h = (pr / p.nbw2) % p.nbh, bi_w2 = pr % p.nbw2;
+#pragma unroll
+    for (int t = 0; t < kNQ; ++t) {
+        I.g[t] = na_tile(p, bi_t, bi_h, 2 * bi_w2 + t, KT, KH);
+        I.n[t] = I.g[t].ntiles;
+    }
+    I.steps = imax(I.n[0], I.n[1]);
+    return I;
+}
+
+// Exact signature of a box's key penalty channels: they depend only on the
+// union's h and w chunk counts and on the window starts of the box's rows /
+// columns relative to the union origin, which advance by 0 or 1 per row
+// (a bit per row: did it advance).
+__device__ __forceinline__ unsigned long long na_sig(const NaParams &p, const NaTile &g) {
+    uint32_t ih = 0u, iw = 0u;
+    int prev = g.u0h;
+    for (int c = 1; c < p.bh; ++c) {
+        const int s = na_window_start(imin(g.h0 + c, p.Hg - 1), p.Hg, p.kh);
+        if (s != prev) ih |= 1u << c;
+        prev = s;
+    }
+    prev = g.u0w;
+    for (int c = 1; c < p.bw; ++c) {
+        const int s = na_window_start(imin(g.w0 + c, p.W - 1), p.W, p.kw);
+        if (s != prev) iw |= 1u << c;
+        prev = s;
+    }
+    return (static_cast<unsigned long long>(g.nhc) << 48) | (static_cast<unsigned long long>(g.nwc) << 40) |
+           (static_cast<unsigned long long>(ih) << 20) | iw;
+}
+
+// a[t] for a per-tile array and a run-time t, by selects (indexing the array
+// with a run-time value would place it in local memory)
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[kNQ], int t) {
+    T r = a[0];
+#pragma unroll
+    for (int i = 1; i < kNQ; ++i)
+        if (t == i) r = a[i];
+    return r;
+}
+
+// Origin (t, h, w) of key sub-box j of a tile: w chunk fastest, then h, then t.
+__device__ __forceinline__ void na_key_box(const NaTile &g, int KT, int KH, int j, int &t, int &h,
+                                           int &w) {
+    const int wc = j % g.nwc;
+    const int hc = (j / g.nwc) % g.nhc;
+    const int tc = j / (g.nwc * g.nhc);
+    t = g.u0t + tc * KT;
+    h = g.u0h + hc * KH;
+    w = g.u0w + wc * kKW;
+}
+
+// KSH = 10 KT + KH > 0 fixes the key sub-box at compile time (the softmax's
+// group masks unroll); 0 takes KT and KH from the parameters.  F16: inputs, P
+// and output in f16 (window tests in the softmax instead of penalty channels).
+template <int KSH, bool F16>
+__global__ void __launch_bounds__(NaCfg<!F16>::NT, 1)
+tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+             const __grid_constant__ CUtensorMap tv, const NaParams p) {
+    constexpr bool PEN = !F16;
+    using C = NaCfg<PEN>;
+    using BarsT = NaBars<C::KS, C::VS>;
+    static_assert(sizeof(BarsT) <= 512, "barrier block must fit its reserved bytes");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
+    BarsT *bars = reinterpret_cast<BarsT *>(smem + C::OFF_BAR);
+    volatile int *abort = &bars->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KT = KSH > 0 ? KSH / 10 : p.KT;
+    const int KH = KSH > 0 ? KSH % 10 : p.KH;
+    const int rows = p.bt * p.bh * p.bw;          // queries per box (<= 128)
+
+    // ---- set-up: barriers (one thread of the last warp) beside the query
+    //      channels, which are the same for every box
+    if (threadIdx.x == C::NT - 32) {
+        ptx::mbar_init(&bars->q_full, 1);
+        ptx::mbar_init(&bars->q_free, kNQ);
+        for (int s = 0; s < C::KS; ++s) {
+            ptx::mbar_init(&bars->k_full[s], 1);
+            ptx::mbar_init(&bars->k_empty[s], kNQ);
+        }
+        for (int s = 0; s < C::VS; ++s) {
+            ptx::mbar_init(&bars->v_full[s], 1);
+            ptx::mbar_init(&bars->v_empty[s], kNQ);
+        }
+        for (int b = 0; b < 2 * kNQ; ++b) {
+            ptx::mbar_init(&bars->s_full[b], 1);
+            ptx::mbar_init(&bars->p_ready[b], 128);
+            ptx::mbar_init(&bars->o_done[b], 1);
+        }
+        for (int t = 0; t < kNQ; ++t) {
+            ptx::mbar_init(&bars->chan_ready[t], 128);
+            ptx::mbar_init(&bars->tab_done[t], 128);
+            ptx::mbar_init(&bars->tab_free[t], 128);
+        }
+        ptx::mbar_init(&bars->drain, kNQ);
+        bars->abort = 0;
+        ptx::fence_barrier_init();
+    } else if (threadIdx.x < C::NBUILD) {
+        // query rows past the box hold zeros (TMA writes the box's rows only)
+        for (int i = threadIdx.x; i < kNQ * (kBM - rows) * 8; i += C::NBUILD) {
+            const int chunk = i % 8, r = rows + (i / 8) % (kBM - rows), t = i / (8 * (kBM - rows));
+            *reinterpret_cast<uint4 *>(smem + C::OFF_Q + t * C::PANEL + r * 128 + chunk * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+        if constexpr (PEN) {
+            // one-hot offset channels of every query row: channel dh, then
+            // bh + dw (rows past the box: zero)
+            for (int i = threadIdx.x; i < kNQ * kBM * 2; i += C::NBUILD) {
+                const int t = i / (kBM * 2), r = (i / 2) % kBM, half = i % 2;
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (r < rows) {
+                    const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
+                    const int ch[2] = {dh, p.bh + dw};
+#pragma unroll
+                    for (int a = 0; a < 2; ++a) {
+                        const int c = ch[a] - half * 8;
+                        if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
+                    }
+                }
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW +
+                                           ptx::sw32_offset(r, half)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == C::W_MMA) {
+        ptx::tmem_alloc(&bars->tmem_base, C::TM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp >= C::NSOFT) {
+        ptx::regs_decrease<C::REGS_OTHER>();
+        if ((warp == C::W_LOAD || warp == C::W_LOADV) && lane == 0) {
+            // ============================================= TMA loaders: the K
+            // (and Q) and V rings run on across items; stage s of CTA key step
+            // g = (steps of earlier items) + j is g % depth
+            const int which = warp == C::W_LOAD ? 0 : 1;
+            const CUtensorMap *tm = which == 0 ? &tk : &tv;
+            uint64_t *full = which == 0 ? bars->k_full : bars->v_full;
+            uint64_t *empty = which == 0 ? bars->k_empty : bars->v_empty;
+            const int NS = which == 0 ? C::KS : C::VS;
+            ptx::prefetch_tmap(tm);
+            if (which == 0) ptx::prefetch_tmap(&tq);
+            const uint64_t pol_kv = ptx::l2_policy_evict_last();
+            const uint64_t pol_q = ptx::l2_policy_evict_first();
+            int g0 = 0;                       // CTA key steps of earlier items
+            int issued = 0;                   // key steps whose copies were issued
+            int q_issued = 0;                 // query loads issued
+            bool ok = true;
+            int ci = 0;
+            for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++ci) {
+                const NaItem I = na_item(p, it, KT, KH);
+                if (which == 0) {
+                    // the queries of item ci overwrite those of item ci - 1 once
+                    // every Q K^T that read them has completed.  q_free is one
+                    // phase per item, and its phase ci needs the queries loaded
+                    // here, so it is never two phases ahead of this wait.
+                    if (ci > 0 && !ptx::mbar_wait_or_abort(&bars->q_free, (ci - 1) & 1, p.err, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t qbytes = 0;
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t)
+                        if (I.n[t] > 0) qbytes += rows * 128;
+                    ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t)
+                        if (I.n[t] > 0)
+                            ptx::tma_load_5d(smem + C::OFF_Q + t * C::PANEL, &tq, 0, I.g[t].w0, I.g[t].h0,
+                                             I.g[t].t0, I.bhd, &bars->q_full, pol_q);
+                    q_issued = ci + 1;
+                }
+                for (int j = 0; j < I.steps; ++j) {
+                    const int gs = g0 + j, s = gs % NS;
+                    if (gs >= NS && !ptx::mbar_wait_or_abort(&empty[s], ((gs / NS) - 1) & 1, p.err, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    issued = gs + 1;
+                    uint32_t bytes = 0;
+#pragma unroll
+                    for (int u = 0; u < kNQ; ++u)
+                        if (j < I.n[u]) bytes += kBN * 128;
+                    ptx::mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+                    for (int u = 0; u < kNQ; ++u) {
+                        if (j >= I.n[u]) continue;
+                        int kt_, kh_, kw_;
+                        na_key_box(I.g[u], KT, KH, j, kt_, kh_, kw_);
+                        ptx::tma_load_5d(smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)), tm, 0, kw_,
+                                         kh_, kt_, I.bhd, &full[s], pol_kv);
+                    }
+                }
+                g0 += I.steps;
+            }
+            // after a timeout elsewhere: let the copies this thread issued land
+            // (bounded) before the CTA's shared memory is released
+            if (*abort) {
+                if (which == 0 && q_issued > 0) ptx::mbar_wait(&bars->q_full, (q_issued - 1) & 1, nullptr);
+                for (int gs = imax(0, issued - NS); gs < issued; ++gs)
+                    ptx::mbar_wait(&full[gs % NS], (gs / NS) & 1, nullptr);
+            }
+        } else if ((warp == C::W_MMA || warp == C::W_MMA1) && lane == 0) {
+            // ============================================= MMA issuers: one
+            // thread per query tile (warps of different SM sub-partitions)
+            const int tt = warp == C::W_MMA ? 0 : 1;
+            const uint32_t id_qk = ptx::idesc_16_f32(kBM, kBN, false, F16);
+            const uint32_t id_pv = ptx::idesc_16_f32(kBM, kD, true, F16);
+            // descriptors are built once; a k-step, stage or tile only moves the
+            // start-address field (byte address >> 4, no carry below 256 KB)
+            constexpr uint32_t HI128 = ptx::desc_hi_sw128(1024), HI32 = ptx::desc_hi_sw32(256);
+            const uint32_t dq = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::OFF_Q + tt * C::PANEL), 16);
+            const uint32_t dk0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::k_off(0, tt)), 16);
+            const uint32_t dv0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::v_off(0, tt)), C::KV_BYTES);
+            uint32_t dqx = 0, dkx0 = 0;
+            if constexpr (PEN) {
+                dqx = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::OFF_QX + tt * kBM * C::X_ROW));
+                dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(tt, 0)));
+            }
+            int vq = 0, nv = 1;               // penalty tile of the next Q K^T
+            // S(g) of key tile j (CTA step gs) into buffer g % 2
+            auto issue_qk = [&](int g, int gs) {
+                const uint32_t b0 = dk0 + uint32_t(((gs % C::KS) * C::STAGE_BYTES) >> 4);
+                const uint32_t d = tmem + C::tm_s(tt, g & 1);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    ptx::mma_ss(d, ptx::desc_join(dq + uint32_t(kk * 2), HI128),
+                                ptx::desc_join(b0 + uint32_t(kk * 2), HI128), id_qk, kk > 0);
+                if constexpr (PEN) {
+                    // + window penalties: one more k-step over the 16 extra
+                    // channels; key tile j uses penalty tile j mod (h x w chunks)
+                    const uint32_t b = dkx0 + uint32_t((vq * C::KX_BYTES) >> 4);
+                    if (++vq == nv) vq = 0;
+                    ptx::mma_ss(d, ptx::desc_join(dqx, HI32), ptx::desc_join(b, HI32), id_qk, 1u);
+                }
+                ptx::tc_commit(&bars->s_full[2 * tt + (g & 1)]);
+            };
+            // O (+)= P(g) V of CTA step gs; the first key tile of an item overwrites O
+            auto issue_pv = [&](int g, int gs, bool first) {
+                const uint32_t b0 = dv0 + uint32_t(((gs % C::VS) * C::STAGE_BYTES) >> 4);
+                const uint32_t a0 = tmem + C::tm_s(tt, g & 1);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    ptx::mma_ts(tmem + C::tm_o(tt), a0 + kk * 8,
+                                ptx::desc_join(b0 + uint32_t(kk * (2048 >> 4)), HI128), id_pv,
+                                (!first || kk > 0) ? 1u : 0u);
+                ptx::tc_commit(&bars->o_done[2 * tt + (g & 1)]);
+            };
+            bool ok = true;
+            int G = 0;                        // key tiles of this tile in earlier items
+            int g0 = 0;                       // CTA key steps of earlier items
+            int rb = 0;                       // channel rebuilds waited for
+            unsigned long long last_sig = ~0ull;
+            int ci = 0;
+            for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++ci) {
+                const NaItem I = na_item(p, it, KT, KH);
+                const int nt = pick(I.n, tt), steps = I.steps;
+                // every phase of q_full is waited for (even by a tile without
+                // work in this item), so no wait can fall two phases behind
+                ok = ptx::mbar_wait_or_abort(&bars->q_full, ci & 1, p.err, abort);
+                if (!ok) break;
+                if constexpr (PEN) {
+                    if (nt > 0) {
+                        const NaTile gt = pick(I.g, tt);
+                        const unsigned long long sig = na_sig(p, gt);
+                        if (sig != last_sig) {
+                            // the softmax of this tile rebuilds the channels
+                            // after it has read every earlier S of the tile
+                            ok = ptx::mbar_wait_or_abort(&bars->chan_ready[tt], rb & 1, p.err, abort);
+                            ++rb;
+                            last_sig = sig;
+                            if (!ok) break;
+                        }
+                        nv = imax(1, gt.nhc * gt.nwc);
+                    }
+                    vq = 0;
+                }
+                // q_free: one commit per issuer and item, right after the last
+                // Q K^T of the tile (at once for a tile without work)
+                bool q_done = false;
+                auto release_q = [&]() {
+                    if (!q_done) ptx::tc_commit(&bars->q_free);
+                    q_done = true;
+                };
+                if (nt == 0) release_q();
+                ptx::tc_fence_after();
+                // Each stage is released once per issuer and use; a stage this
+                // tile does not read is released only once it has been filled,
+                // so that an issuer running ahead never completes a stage phase
+                // in place of the other one.
+                auto next_qk = [&](int j) {          // Q K^T of key tile j (CTA step g0 + j)
+                    const int gs = g0 + j;
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[gs % C::KS], (gs / C::KS) & 1, p.err, abort);
+                    if (!ok) return;
+                    if (j < nt) {
+                        ptx::tc_fence_after();
+                        issue_qk(G + j, gs);
+                        if (j == nt - 1) release_q();
+                    }
+                    ptx::tc_commit(&bars->k_empty[gs % C::KS]);
+                };
+                for (int j = 0; ok && j < 2 && j < steps; ++j) next_qk(j);
+                for (int j = 0; ok && j < steps; ++j) {
+                    const int gs = g0 + j;
+                    // P V (j) once the softmax has written P(j) and V(j) has landed
+                    if (j < nt)
+                        ok = ptx::mbar_wait_or_abort(&bars->p_ready[2 * tt + ((G + j) & 1)], ((G + j) >> 1) & 1,
+                                                     p.err, abort);
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[gs % C::VS], (gs / C::VS) & 1, p.err, abort);
+                    if (!ok) break;
+                    if (j < nt) {
+                        ptx::tc_fence_after();
+                        issue_pv(G + j, gs, j == 0);
+                    }
+                    // then Q K^T (j + 2) into the buffer P(j) came from
+                    if (j + 2 < steps) next_qk(j + 2);
+                    if (!ok) break;
+                    ptx::tc_commit(&bars->v_empty[gs % C::VS]);
+                }
+                if (ok) release_q();
+                G += nt;
+                g0 += steps;
+            }
+            // drain: every MMA of both issuers has completed before TMEM is freed
+            ptx::tc_commit(&bars->drain);
+            ptx::mbar_wait(&bars->drain, 0, p.err);
+        }
+    } else {
+        // ================================================= softmax warpgroups
+        ptx::regs_increase<C::REGS_SOFTMAX>();
+        const int t = warp >> 2;                 // query tile
+        const int quarter = warp & 3;            // TMEM lanes [32 quarter, 32 quarter + 32)
+        const int row = quarter * 32 + lane;     // query row within the box
+        const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+        const uint32_t o_addr = lane_base + C::tm_o(t);
+        const float cl = p.c_log2;
+        constexpr int NG = kBN / 16;             // 16-key groups per key tile
+        const int dt = row / (p.bh * p.bw), dh = (row / p.bw) % p.bh, dw = row % p.bw;
+        uint16_t *tab_h = reinterpret_cast<uint16_t *>(smem + C::OFF_TAB) + t * 2 * C::TAB;
+        uint16_t *tab_w = tab_h + C::TAB;
+
+        // waits for P V (gg) of this tile (and every earlier one: one thread's
+        // MMAs complete in issue order).  Valid once P V (gg - 2) is known
+        // complete: it is while the softmax holds S(gg), issued after it.
+        auto wait_pv = [&](int gg) -> bool {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[2 * t + (gg & 1)],
+                                                                 (gg >> 1) & 1, p.err, abort)))
+                return false;
+            ptx::tc_fence_after();
+            return true;
+        };
+
+        bool ok = true;
+        int G = 0;                               // key tiles of this tile in earlier items
+        unsigned long long last_sig = ~0ull;
+        int rbs = 0;                             // channel rebuilds done by this warpgroup
+        for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+            const NaItem I = na_item(p, it, KT, KH);
+            const int nt = pick(I.n, t);
+            if (nt == 0) continue;
+            const NaTile gt = pick(I.g, t);
+
+            if constexpr (PEN) {
+                const unsigned long long sig = na_sig(p, gt);
+                if (sig != last_sig) {
+                    // ---- rebuild this tile's key penalty channels.  Every Q K^T
+                    // of the tile so far has completed (this warpgroup has read
+                    // all their scores); the issuer waits for chan_ready before
+                    // the next one.  For key (h, w) of the sub-box of h chunk hc
+                    // and w chunk wc, channel c < bh holds -penalty if h lies
+                    // outside the h window of box row offset c, channel bh + c'
+                    // likewise for w: tabulated per union row / column first,
+                    // then each channel row is the OR of two entries.
+                    last_sig = sig;
+                    // every thread of the warpgroup is done reading the previous tables
+                    if (rbs > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_free[t],
+                                                                                     (rbs - 1) & 1, p.err, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    for (int i = row; i < 2 * C::TAB; i += 128) {
+                        const int axis = i / C::TAB, e = i % C::TAB;
+                        uint32_t m = 0u;
+                        if (axis == 0 && e < gt.nhc * KH) {
+                            const int kh = gt.u0h + e;
+                            for (int c = 0; c < p.bh; ++c) {
+                                const int sh = na_window_start(imin(gt.h0 + c, p.Hg - 1), p.Hg, p.kh);
+                                if (unsigned(kh - sh) >= unsigned(p.eh)) m |= 1u << c;
+                            }
+                        } else if (axis == 1 && e < gt.nwc * kKW) {
+                            const int kw = gt.u0w + e;
+                            for (int c = 0; c < p.bw; ++c) {
+                                const int sw = na_window_start(imin(gt.w0 + c, p.W - 1), p.W, p.kw);
+                                if (unsigned(kw - sw) >= unsigned(p.ew)) m |= 1u << (p.bh + c);
+                            }
+                        }
+                        (axis == 0 ? tab_h : tab_w)[e] = uint16_t(m);
+                    }
+                    ptx::mbar_arrive(&bars->tab_done[t]);
+                    if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_done[t], rbs & 1, p.err, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
+                    const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
+                    const int nvt = gt.nhc * gt.nwc;
+                    for (int i = row; i < nvt * kBN * 2; i += 128) {
+                        const int half = i & 1, r = (i >> 1) % kBN, v = (i >> 1) / kBN;
+                        // key r of sub-box v: union h row (v / nwc) KH + (r / 16) % KH,
+                        // w column (v % nwc) 16 + r % 16 (the same in each of its KT frames)
+                        const int hc = v / gt.nwc, wc = v - hc * gt.nwc;
+                        const uint32_t m = uint32_t(tab_h[hc * KH + (r / kKW) % KH]) |
+                                           uint32_t(tab_w[wc * kKW + r % kKW]);
+                        const uint32_t bits = (m >> (half * 8)) & 0xffu;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc)
+                            w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
+                                    (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
+                        *reinterpret_cast<uint4 *>(smem + C::kxv_off(t, v) + ptx::sw32_offset(r, half)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(&bars->chan_ready[t]);
+                    ptx::mbar_arrive(&bars->tab_free[t]);
+                    ++rbs;
+                }
+            }
+
+            // query of this row and its window
+            const int qt = gt.t0 + dt, qh = gt.h0 + dh, qw = gt.w0 + dw;
+            const bool qvalid = row < rows && qt < p.T && qh < p.Hg && qw < p.W;
+            const int wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
+            int wsh = 0, wsw = 0;
+            if constexpr (!PEN) {
+                wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
+                wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
+            }
+
+            float m = -INFINITY, l = 0.f;
+            int tc = 0, hc = 0, wc = 0;          // key sub-box counters (w fastest, then h, then t)
+            for (int j = 0; j < nt; ++j) {
+                const int gg = G + j;
+                const uint32_t s_addr = lane_base + C::tm_s(t, gg & 1);
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->s_full[2 * t + (gg & 1)],
+                                                                     (gg >> 1) & 1, p.err, abort))) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+
+                // ---- t window per 16-key group (group gq holds frame kt0 + gq / KH):
+                //      bit gq of gmask clear -> P = 0 there
+                const int kt0 = gt.u0t + tc * KT;
+                const int kh0 = gt.u0h + hc * KH, kw0 = gt.u0w + wc * kKW;
+                if (++wc == gt.nwc) {
+                    wc = 0;
+                    if (++hc == gt.nhc) {
+                        hc = 0;
+                        ++tc;
+                    }
+                }
+                uint32_t gmask = 0u;
+                if (qvalid) {
+#pragma unroll
+                    for (int gq = 0; gq < NG; ++gq)
+                        if (unsigned(kt0 + gq / KH - wst) < unsigned(p.et)) gmask |= 1u << gq;
+                }
+
+                float sv[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c)
+                    ptx::tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                ptx::tmem_wait_ld();
+
+                if constexpr (!PEN) {
+                    // f16: the h and w window tests per key.  Key e of the (KT, KH, 16)
+                    // sub-box sits at h = kh0 + (e / 16) % KH, w = kw0 + e % 16; wm / hm
+                    // hold the in-window w columns / h rows of this row.
+                    const int lw = wsw - kw0, lh = wsh - kh0;
+                    const int aw = imax(lw, 0), bw = imin(lw + p.ew, kKW);
+                    const int ah = imax(lh, 0), bh_ = imin(lh + p.eh, KH);
+                    const uint32_t wm = aw < bw ? ((1u << bw) - 1u) & ~((1u << aw) - 1u) : 0u;
+                    const uint32_t hm = ah < bh_ ? ((1u << bh_) - 1u) & ~((1u << ah) - 1u) : 0u;
+#pragma unroll
+                    for (int gq = 0; gq < NG; ++gq) {
+                        const bool hin = (hm >> (gq % KH)) & 1u;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (!hin || !((wm >> i) & 1u)) sv[gq * 16 + i] = -INFINITY;
+                    }
+                }
+
+                // 32-key chunks that no row of this warp may see: P = 0 without
+                // exponentials
+                const uint32_t wlive = __reduce_or_sync(0xffffffffu, gmask);
+
+                // P = 2^(x - m) in 16-bit over S (groups outside gm: P = 0);
+                // returns the tile's row sum (fp32)
+                auto emit_p = [&](float nmu, uint32_t gm) -> float {
+                    float acc[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t pk[16];
+                        if (((wlive >> (2 * c)) & 3u) == 0u) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                            ptx::tmem_st16(s_addr + c * 16, pk);
+                            continue;
+                        }
+                        const float n0 = ((gm >> (2 * c)) & 1u) ? nmu : -INFINITY;
+                        const float n1 = ((gm >> (2 * c + 1)) & 1u) ? nmu : -INFINITY;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float nm = e < 8 ? n0 : n1;
+                            float x0, x1;
+                            ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nm, nm);
+                            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                            ptx::fadd2(acc[(2 * e) & 7], acc[(2 * e + 1) & 7], acc[(2 * e) & 7],
+                                       acc[(2 * e + 1) & 7], p0, p1);
+                            pk[e] = H16<F16>::pack(p0, p1);
+                        }
+                        ptx::tmem_st16(s_addr + c * 16, pk);
+                    }
+                    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+                };
+
+                // ---- fast path: exponentiate against m as it stands.  P only
+                //      has to stay finite in its 16-bit type: a tile whose row sum
+                //      exceeds 2^24 (2^15 for f16, largest finite 65504) or is not
+                //      finite (scores far above m, or m still the garbage of a row
+                //      whose first tiles were all outside its window) is redone
+                //      against its own maximum.
+                bool fast = j > 0 && __all_sync(0xffffffffu, !(gmask != 0u && m == -INFINITY));
+                if (fast) {
+                    const float lt = emit_p(-m, gmask);
+                    if (__any_sync(0xffffffffu, !(lt <= (F16 ? 32768.f : 16777216.f))))
+                        fast = false;             // redo the tile (P is rewritten below)
+                    else
+                        l += lt;
+                }
+                if (!fast) {
+                    // ---- tile maximum over the groups this row may see
+                    float tmax = -INFINITY;
+#pragma unroll
+                    for (int gq = 0; gq < NG; ++gq) {
+                        float mx[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[gq * 16 + i], sv[gq * 16 + 8 + i]);
+                        const float gmx = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
+                                                     ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                        if ((gmask >> gq) & 1u) tmax = fmaxf(tmax, gmx);
+                    }
+                    const float mt = tmax * cl;  // cl > 0: max commutes with the scaling
+                    // ---- the previous P V must be done before O is rescaled
+                    const bool want = j == 0 || mt > m + 8.f;
+                    const bool any_want = __any_sync(0xffffffffu, want);
+                    if (j > 0 && any_want && !wait_pv(gg - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j == 0) {
+                        m = mt;
+                    } else if (any_want) {
+                        // rows that move m scale their O row; the others multiply by 1
+                        const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
+#pragma unroll
+                        for (int c = 0; c < kD / 32; ++c) {
+                            uint32_t ov[32];
+                            ptx::tmem_ld32(o_addr + c * 32, ov);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                float a0, a1;
+                                ptx::ffma2(a0, a1, __uint_as_float(ov[e]), __uint_as_float(ov[e + 1]), f, f,
+                                           0.f, 0.f);
+                                ov[e] = __float_as_uint(a0);
+                                ov[e + 1] = __float_as_uint(a1);
+                            }
+                            ptx::tmem_st32(o_addr + c * 32, ov);
+                        }
+                        if (want) {
+                            l *= f;
+                            m = mt;
+                        }
+                    }
+                    l += emit_p((m == -INFINITY) ? 0.f : -m, gmask);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bars->p_ready[2 * t + (gg & 1)]);
+            }
+            if (!ok) break;
+
+            // ---- epilogue: O / l -> 16-bit -> global.  The issuer overwrites O
+            //      with the next item's first P V only after this warpgroup has
+            //      written that item's P(0), i.e. after these reads.
+            if (!wait_pv(G + nt - 1)) {
+                ok = false;
+                break;
+            }
+            const float inv = 1.f / l;
+            typename H16<F16>::T *orow = nullptr;
+            if (qvalid)
+                orow = static_cast<typename H16<F16>::T *>(p.o) +
+                       ((size_t(I.bhd) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw) * kD;
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+                uint32_t ov[32];
+                ptx::tmem_ld32(o_addr + c * 32, ov);
+                ptx::tmem_wait_ld();
+                if (qvalid) {
+                    uint4 w4[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wp[e] = H16<F16>::pack(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = w4[e];
+                }
+            }
+            G += nt;
+        }
+    }
+
+    // ---- teardown: all TMEM traffic done before the owner warp frees it
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::W_MMA) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+// Query box and key sub-box: at most 128 queries per box and key tiles of KT
+// frames x KH rows x 16 columns (KT KH = 6, 96 keys), minimising the key tiles
+// -- i.e. the (query row, key) slots the MMAs compute -- over all boxes.
+bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KT, int &KH) {
+    const int ext[3] = {T, Hg, W};
+    constexpr int kShapes[4][2] = {{1, 6}, {2, 3}, {3, 2}, {6, 1}};
+    double best = -1;
+    for (int cbt = 1; cbt <= imin(T, 128); ++cbt)
+        for (int cbh = 1; cbh <= imin(Hg, 128 / cbt); ++cbh)
+            for (int cbw = 1; cbw <= imin(W, 128 / (cbt * cbh)); ++cbw) {
+                if (cbt * cbh * cbw < imin(64, T * Hg * W)) continue;   // keep MMA rows busy
+                if (cbh + cbw > 16) continue;                // h and w offsets fit 16 channels
+                for (const auto &sh : kShapes) {
+                    const int ckt = sh[0], ckh = sh[1];
+                    // distinct key penalty tiles of a box (h chunks x w chunks) must fit
+                    const int nh_max = cdiv(imin(cbh + imin(kern[1], Hg) - 1, Hg), ckh);
+                    const int nw_max = cdiv(imin(cbw + imin(kern[2], W) - 1, W), kKW);
+                    if (nh_max * nw_max > kMaxPenaltyTiles) continue;
+                    // key tiles over all boxes = sum_t(t chunks) * sum_h(h chunks) * sum_w(w chunks)
+                    const int b[3] = {cbt, cbh, cbw}, chunk[3] = {ckt, ckh, kKW};
+                    double axis[3];
+                    for (int a = 0; a < 3; ++a) {
+                        const int keff = imin(kern[a], ext[a]);
+                        double acc = 0;
+                        for (int i0 = 0; i0 < ext[a]; i0 += b[a]) {
+                            const int i1 = imin(i0 + b[a], ext[a]) - 1;
+                            const int u = na_window_start(i1, ext[a], kern[a]) + keff -
+                                          na_window_start(i0, ext[a], kern[a]);
+                            acc += cdiv(u, chunk[a]);
+                        }
+                        axis[a] = acc;
+                    }
+                    const int nbw = cdiv(W, cbw);
+                    // odd box count along w leaves one query tile idle per (t, h) box row
+                    const double w_pairs_waste = (nbw & 1) ? double(nbw + 1) / nbw : 1.0;
+                    const double cost = axis[0] * axis[1] * axis[2] * w_pairs_waste;
+                    if (best < 0 || cost < best) {
+                        best = cost;
+                        bt = cbt; bh = cbh; bw = cbw; KT = ckt; KH = ckh;
+                    }
+                }
+            }
+    return best > 0;
+}
+
+// Plans are cached per (grid, kernel): the search is a few thousand candidates.
+struct NaPlan {
+    int bt, bh, bw, KT, KH;
+    bool ok;
+};
+
+NaPlan cached_plan(int T, int Hg, int W, const int kern[3]) {
+    struct Entry {
+        int key[6];
+        NaPlan plan;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    const int key[6] = {T, Hg, W, kern[0], kern[1], kern[2]};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        bool same = true;
+        for (int a = 0; a < 6; ++a) same = same && cache[i].key[a] == key[a];
+        if (same) return cache[i].plan;
+    }
+    NaPlan pl{};
+    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KT, pl.KH);
+    Entry &e = cache[used < 64 ? used++ : 63];
+    for (int a = 0; a < 6; ++a) e.key[a] = key[a];
+    e.plan = pl;
+    return pl;
+}
+
+template <int KSH, bool F16 = false>
+attn_status_t launch_na(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const NaParams &p) {
+    using C = NaCfg<!F16>;
+    static int done_mask = 0;
+    static int regs = -1;
+    auto kern = tc_na_kernel<KSH, F16>;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
+        return ATTN_ERR_RESOURCE;
+    // the warpgroups re-split the launch's register file with setmaxnreg; the
+    // split is only valid for the per-thread count it was computed for
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kern)) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_CUDA;
+        }
+        regs = fa.numRegs;
+    }
+    if (regs != C::REGS_LAUNCH) return ATTN_ERR_UNSUPPORTED;
+    // one CTA per SM (the shared memory allows no second), each walking items
+    // blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int grid = imin(p.n_items, imax(1, c.sm_count));
+    kern<<<grid, C::NT, C::SMEM, c.stream>>>(tq, tk, tv, p);
+    return launch_status(kFamTcNa);
+}
+
+}  // namespace
+
+bool tc_na3d_supported(int B, int H, int T, int Hg, int W, int D, const int kernel[3]) {
+    return D == kD && tma_encode_available() && cached_plan(T, Hg, W, kernel).ok;
+}
+
+attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *k, const void *v,
+                      void *o, int B, int H, int T, int Hg, int W, int D, const int kernel[3],
+                      float scale) {
+    const bool f16 = dt == ATTN_F16;
+    const NaPlan pl = cached_plan(T, Hg, W, kernel);
+    if (!pl.ok || D != kD) return ATTN_ERR_UNSUPPORTED;
+    NaParams p{};
+    p.bt = pl.bt; p.bh = pl.bh; p.bw = pl.bw; p.KT = pl.KT; p.KH = pl.KH;
+    CUtensorMap tq, tk, tv;
+    const uint64_t dims[5] = {uint64_t(D), uint64_t(W), uint64_t(Hg), uint64_t(T), uint64_t(B) * H};
+    const uint32_t qbox[5] = {64, uint32_t(p.bw), uint32_t(p.bh), uint32_t(p.bt), 1};
+    const uint32_t kbox[5] = {64, uint32_t(kKW), uint32_t(p.KH), uint32_t(p.KT), 1};
+    if (!make_tmap(&tq, q, 5, dims, qbox, f16) || !make_tmap(&tk, k, 5, dims, kbox, f16) ||
+        !make_tmap(&tv, v, 5, dims, kbox, f16))
+        return ATTN_ERR_CUDA;
+    p.c_log2 = scale * kLog2e;
+    // bf16 penalty per violated axis: a power of two (exact in bf16), at least
+    // 2^100 and with penalty * scale * log2(e) >= 300.  A masked key's score is
+    // then raw - penalty (or - 2 penalty) <= -2^99 whenever |raw| < 2^98, so
+    // 2^(x - m) underflows to exactly 0 however far its raw score lies above
+    // the row's in-window scores; up to 2^125 two penalties still fit fp32.
+    // (f16 masks in the softmax and does not use it.)
+    {
+        const int e = imax(100, int(ceilf(log2f(300.f / p.c_log2))));
+        if (!f16 && e > 125) return ATTN_ERR_UNSUPPORTED;   // scale below ~1e-28
+        p.penalty = ldexpf(1.f, imin(e, 125));
+    }
+    p.o = o;
+    p.err = c.err;
+    p.T = T; p.Hg = Hg; p.W = W;
+    p.kt = kernel[0]; p.kh = kernel[1]; p.kw = kernel[2];
+    p.et = imin(kernel[0], T); p.eh = imin(kernel[1], Hg); p.ew = imin(kernel[2], W);
+    p.nbt = cdiv(T, p.bt);
+    p.nbh = cdiv(Hg, p.bh);
+    p.nbw = cdiv(W, p.bw);
+    p.nbw2 = cdiv(p.nbw, 2);
+    const long long items = (long long)p.nbt * p.nbh * p.nbw2 * B * H;
+    if (items > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    p.n_items = int(items);
+    // the planner's key sub-box shapes have compile-time kernels (bf16)
+    if (f16) return launch_na<0, true>(c, tq, tk, tv, p);
+    switch (p.KT * 10 + p.KH) {
+        case 16: return launch_na<16>(c, tq, tk, tv, p);
+        case 23: return launch_na<23>(c, tq, tk, tv, p);
+        case 32: return launch_na<32>(c, tq, tk, tv, p);
+        default: return launch_na<0>(c, tq, tk, tv, p);
+    }
+}
+
+}  // namespace attn

@@ -1,10 +1,12 @@
-// Tensor-core (tcgen05 + TMEM + TMA) flash attention for bf16 and f16, sm_103a.
+// Tensor-core (tcgen05 + TMEM + TMA) flash attention for bf16 and f16, sm_103a:
+// full attention (the joint text+image attention of FLUX) and causal
+// grouped-query prefill.  (3D neighborhood attention has a persistent kernel
+// of its own, tc_na.cu.)
 //
 // S = Q K^T * scale, row softmax, O = P V, streamed over key tiles with an
-// online softmax (the attention of iris.c issue #15 "CUDA codepath !" and the
-// neighborhood attention of candle PR #11).  The pages compute it as cuBLAS
-// GEMM -> softmax kernel -> GEMM with S in HBM, or as a one-block-per-query
-// SIMT kernel; here S and P never leave the SM.
+// online softmax (the attention of iris.c issue #15 "CUDA codepath !").  The
+// page computes it as cuBLAS GEMM -> softmax kernel -> GEMM with S in HBM;
+// here S and P never leave the SM.
 //
 // One CTA = two 128-row query tiles (Q0, Q1) of one (batch, head), 12 warps:
 //   warps 0-3   softmax warpgroup of Q0 (thread = query row = TMEM lane)
@@ -12,35 +14,22 @@
 //   warp  8     MMA issuer (one elected thread) and TMEM owner
 //   warp  9     TMA loader of Q and the K ring (one elected thread)
 //   warp 10     TMA loader of the V ring (one elected thread)
-//   warp 11     neighborhood attention: MMA issuer of Q1 (warp 8 then issues
-//               for Q0 only); full attention: idle.
+//   warp 11     barrier set-up, then idle
 // The third warpgroup drops to 72 registers per thread (setmaxnreg) so the
 // softmax warpgroups can hold a whole S row in registers (216 per thread).
 //
-// Full attention (key tiles of 128): tensor memory holds S_t at [128 t,
-// 128 t + 128) and O_t at [256 + D t, 256 + D (t + 1)).  With D = 128 the
-// columns are full and P_t (16-bit, two per column) overwrites the first 64
-// columns of S_t once the softmax has read S_t; with D = 64 P_t has columns of
-// its own ([384 + 64 t, 448 + 64 t)).  One thread issues every MMA, per key
-// tile j:
+// Key tiles of 128.  Tensor memory holds S_t at [128 t, 128 t + 128) and O_t
+// at [256 + D t, 256 + D (t + 1)).  With D = 128 the columns are full and P_t
+// (16-bit, two per column) overwrites the first 64 columns of S_t once the
+// softmax has read S_t; with D = 64 P_t has columns of its own
+// ([384 + 64 t, 448 + 64 t)).  One thread issues every MMA, per key tile j:
 //   D = 128 (P over S):  PV0(j), QK0(j+1), PV1(j), QK1(j+1)   -- QK_t(j+1)
 //       overwrites S_t only after PV_t(j) has read P_t (MMAs of one thread
 //       execute in issue order);
 //   D = 64 (separate P): QK0(j+1), QK1(j+1) as soon as the softmax has read
 //       S_t(j) into registers, then PV0(j), PV1(j).
-//
-// Neighborhood attention (key tiles of 96): every query tile has two S
-// buffers and P is written over the S it came from: [S_t,0 | S_t,1 | O_t]
-// (96 + 96 + 64 columns) at 256 t.  Each query tile has an issuer of its own
-// that runs one key tile ahead: after PV_t(j) (which reads buffer j % 2) it
-// issues QK_t(j + 2) into that same buffer, so S(j + 1) is ready while the
-// softmax works on tile j.  Measured on the clock: a barrier hand-off between
-// warps costs ~200 cycles, a commit ~100 and each MMA ~46 cycles to issue, so
-// with one S buffer and one issuer the per-step chain of hand-offs, not the
-// tensor core or the softmax, set the pace.  The P V MMA takes P straight
-// from TMEM (A operand) and V from shared memory (MN-major B operand).  K and
-// V stream through rings of their own (K one stage deeper for neighborhood
-// attention, where the next Q K^T runs a key tile ahead).
+// The P V MMA takes P straight from TMEM (A operand) and V from shared memory
+// (MN-major B operand).  K and V stream through rings of their own.
 //
 // Softmax (base 2): x = s * scale * log2(e).  The first tile sets the running
 // max m; later tiles are exponentiated against m as it stands (no tile-max
@@ -50,19 +39,10 @@
 // Every branch that leads to a warp-collective tcgen05.ld / st is uniform
 // across the warp.
 //
-// Full attention: both query tiles share each K/V tile (one stream).  Q, K
-// and V are 4D tensor maps {D, N, heads, B} built from each tensor's element
-// strides (contiguous for the plain entries), and the epilogue stores through
-// the output's strides, so strided views are read and written in place.
-// Neighborhood attention: the two query tiles are two 3D boxes adjacent in w;
-// each streams the union of its queries' clamped windows as (1, KH, 16)
-// (t, h, w) key sub-boxes loaded by 5D TMA.  bf16: the h and w window tests
-// enter S as a penalty of -2^100 per violated axis through one extra
-// 16-channel MMA k-step (one-hot query offsets against per-sub-box key penalty
-// tiles), which drops every masked key exactly (P = 0) for any scores below
-// 2^98 in magnitude; f16, whose range cannot hold such a penalty, tests h and
-// w per key in the softmax instead.  A key frame outside a row's t window is
-// dropped in the softmax (P = 0).
+// Both query tiles share each K/V tile.  Q, K and V are 4D tensor maps
+// {D, N, heads, B} built from each tensor's element strides (contiguous for
+// the plain entries), and the epilogue stores through the output's strides, so
+// strided views are read and written in place.
 //
 // All spin-waits are bounded (1 s); on a timeout the CTA raises the device
 // error word, drains what it issued, frees TMEM and exits.
@@ -80,81 +60,42 @@ namespace {
 
 constexpr int kBM = 128;      // query rows per tile (MMA M)
 constexpr int kNQ = 2;        // query tiles per CTA
-constexpr int kBN = 128;      // keys per key tile of full attention (MMA N of S)
-constexpr int kBNA = 96;      // keys per neighborhood key tile (a (KT, KH, 16) sub-box)
-constexpr int kKW = 16;       // neighborhood key sub-box width along w
-constexpr int kMaxPenaltyTiles = 8;   // distinct key penalty tiles per query box
-// bf16 neighborhood attention applies the h and w window tests through the
-// tensor core (penalty channels) when true, in the softmax when false
-constexpr bool kNaPenalty = true;
+constexpr int kBN = 128;      // keys per key tile (MMA N of S)
 
-template <int D, bool NA, bool PEN>
+template <int D>
 struct TcCfg {
-    static constexpr int BN = NA ? kBNA : kBN;             // keys per key tile
+    static constexpr int BN = kBN;                         // keys per key tile
     static constexpr int PANELS = D / 64;                  // 128-byte swizzle panels
     static constexpr int PANEL_Q = kBM * 128;              // bytes per Q panel
     static constexpr int PANEL_KV = BN * 128;              // bytes per K/V panel
     static constexpr int Q_BYTES = PANELS * PANEL_Q;
-    static constexpr int KV_BYTES = PANELS * PANEL_KV;
-    static constexpr int STREAMS = NA ? kNQ : 1;           // K/V streams per stage
-    // neighborhood window-penalty channels: 16 bf16 per row, 32-byte swizzle.
-    // The key-side penalties of a key sub-box depend only on its h and w chunk,
-    // so each query box needs at most MAXV distinct penalty tiles, built once.
-    static constexpr int X_ROW = 32;
-    static constexpr int MAXV = PEN ? kMaxPenaltyTiles : 0;
-    static constexpr int QX_BYTES = PEN ? kNQ * kBM * X_ROW : 0;
-    static constexpr int KX_BYTES = BN * X_ROW;               // one penalty tile
-    static constexpr int KXV_BYTES = STREAMS * MAXV * KX_BYTES;
-    // K and V stream through rings of their own: a K stage is needed a
-    // whole step before the V stage of the same key tile, so K gets the
-    // deeper ring when shared memory allows only an odd number of stages
-    static constexpr int STAGE_BYTES = STREAMS * KV_BYTES;   // one K (or V) stage
+    static constexpr int KV_BYTES = PANELS * PANEL_KV;     // one K (or V) stage
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int NS_ALL = (BUDGET - kNQ * Q_BYTES - QX_BYTES - KXV_BYTES) / STAGE_BYTES;
-    // (full attention keeps equal rings: a third K stage at D = 128 measured slower)
-    static constexpr int KS_RAW = NA ? (NS_ALL + 1) / 2 : NS_ALL / 2;
-    static constexpr int KS = KS_RAW > 4 ? 4 : KS_RAW;                        // K stages
-    static constexpr int VS = NS_ALL - KS_RAW > 4 ? 4 : NS_ALL - KS_RAW;      // V stages
+    static constexpr int NS_ALL = (BUDGET - kNQ * Q_BYTES) / KV_BYTES;
+    // K and V rings of equal depth (a third K stage at D = 128 measured slower)
+    static constexpr int KS = NS_ALL / 2 > 4 ? 4 : NS_ALL / 2;               // K stages
+    static constexpr int VS = NS_ALL - NS_ALL / 2 > 4 ? 4 : NS_ALL - NS_ALL / 2;  // V stages
     static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_QX = kNQ * Q_BYTES;
-    static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
-    static constexpr int OFF_K = OFF_KXV + KXV_BYTES;
-    static constexpr int OFF_V = OFF_K + KS * STAGE_BYTES;
-    static constexpr int OFF_BAR = OFF_V + VS * STAGE_BYTES;
+    static constexpr int OFF_K = kNQ * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + VS * KV_BYTES;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;      // barriers + 1024 B alignment slack
-    // Tensor memory (512 columns).  P holds the 16-bit probabilities, two
-    // per column.
-    //  * full attention: S_t at t BN, O_t at kNQ BN + t D; P_t over the first
-    //    half of S_t (D = 128) or in columns of its own after the O's (D = 64).
-    //  * neighborhood attention: two S buffers per query tile (key tile j in
-    //    buffer j % 2) with P written over the S it came from, so the Q K^T of
-    //    tile j + 1 is already computed while the softmax works on tile j and
-    //    the MMA issuer runs a whole key tile ahead: per query tile
-    //    [S_t,0 | S_t,1 | O_t] (96 + 96 + 64 columns) at t 256.
-    static constexpr int SBUF = NA ? 2 : 1;
-    static constexpr bool SEP_P = !NA && kNQ * (BN + D + BN / 2) <= 512;
-    static constexpr uint32_t TBLK = NA ? 2 * BN + D : BN;
-    static constexpr uint32_t tm_s(int t, int b) { return t * TBLK + (NA ? b * BN : 0); }
-    static constexpr uint32_t tm_o(int t) { return NA ? t * TBLK + 2 * BN : kNQ * BN + t * D; }
-    static constexpr uint32_t tm_p(int t, int b) {
-        return NA ? tm_s(t, b) : (SEP_P ? kNQ * BN + kNQ * D + t * (BN / 2) : t * BN);
-    }
-    // S buffer of key tile j and the phase parity of its barriers
-    static constexpr int buf_of(int j) { return SBUF == 2 ? (j & 1) : 0; }
-    static constexpr uint32_t par_of(int j) { return SBUF == 2 ? ((j >> 1) & 1) : (j & 1); }
+    // Tensor memory (512 columns): S_t at t BN, O_t at kNQ BN + t D; P (16-bit,
+    // two per column) over the first half of S_t (D = 128) or in columns of
+    // its own after the O's (D = 64).
+    static constexpr bool SEP_P = kNQ * (BN + D + BN / 2) <= 512;
+    static constexpr uint32_t tm_s(int t) { return t * BN; }
+    static constexpr uint32_t tm_o(int t) { return kNQ * BN + t * D; }
+    static constexpr uint32_t tm_p(int t) { return SEP_P ? kNQ * BN + kNQ * D + t * (BN / 2) : t * BN; }
     static constexpr uint32_t TM_COLS = 512;
-    static_assert(tm_o(kNQ - 1) + D <= TM_COLS && (!SEP_P || tm_p(kNQ, 0) <= TM_COLS),
+    static_assert(tm_o(kNQ - 1) + D <= TM_COLS && (!SEP_P || tm_p(kNQ) <= TM_COLS),
                   "tensor-memory layout must fit 512 columns");
     static constexpr int NSOFT = 4 * kNQ;
-    static constexpr int W_MMA = NSOFT;                   // MMA issuer of query tile 0, TMEM owner
+    static constexpr int W_MMA = NSOFT;                   // MMA issuer, TMEM owner
     static constexpr int W_LOAD = NSOFT + 1;              // Q and K copies
     static constexpr int W_LOADV = NSOFT + 2;             // V copies
-    static constexpr int W_MMA1 = NSOFT + 3;              // MMA issuer of query tile 1
-    // MMA issuing threads: one per query tile for neighborhood attention (its
-    // per-tile barrier waits and MMAs kept one thread busy for the whole
-    // step), one for both tiles of full attention (two issuers measured slower)
-    static constexpr int ISSUERS = NA ? kNQ : 1;
+    static constexpr int W_INIT = NSOFT + 3;              // barrier set-up
     static constexpr int NT = (NSOFT + 4) * 32;            // 3 warpgroups
     // register split: launch 168 x 384 = 64512; 2 x 128 x 216 + 128 x 72 = 64512
     static constexpr int REGS_LAUNCH = 168;
@@ -162,31 +103,19 @@ struct TcCfg {
     static constexpr int REGS_OTHER = 72;
     static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= NT * REGS_LAUNCH,
                   "setmaxnreg split must fit the launch's register file share");
-    // K (or V) tile of stream u in stage s
-    static constexpr int k_off(int s, int u) { return OFF_K + s * STAGE_BYTES + u * KV_BYTES; }
-    static constexpr int v_off(int s, int u) { return OFF_V + s * STAGE_BYTES + u * KV_BYTES; }
-    // penalty tile v (= h chunk * w chunks + w chunk) of stream u
-    static constexpr int kxv_off(int u, int v) { return OFF_KXV + (u * MAXV + v) * KX_BYTES; }
+    static constexpr int k_off(int s) { return OFF_K + s * KV_BYTES; }
+    static constexpr int v_off(int s) { return OFF_V + s * KV_BYTES; }
 };
 
 struct TcParams {
-    int Nq, Nkv;             // full attention: query / key tokens per (batch, head)
+    int Nq, Nkv;             // query / key tokens per (batch, head)
     float c_log2;            // scale * log2(e)
     void *o;                 // bf16 or f16, like the inputs
     unsigned *err;
-    // neighborhood attention (grid T x Hg x W, row-major)
-    int T, Hg, W;
-    int kt, kh, kw;          // requested kernel
-    int et, eh, ew;          // effective kernel
-    int bt, bh, bw;          // query box
-    int nbh, nbw2;           // boxes along h; box pairs along w
-    int nbw;                 // boxes along w
-    int KT, KH;              // key sub-box frames and height (KT * KH * 16 = 96 keys)
-    float penalty;           // bf16: power of two >= 2^100 with penalty * c_log2 >= 300
     // causal grouped-query prefill
     int Hq, Hkv, group;
-    // full / causal: q, k, v are 4D tensor maps {D, N, heads, B}; o is written
-    // through element strides (batch, head, row), D contiguous
+    // q, k, v are 4D tensor maps {D, N, heads, B}; o is written through
+    // element strides (batch, head, row), D contiguous
     int H;                   // query heads (the batch of block row bh is bh / H)
     long long o_sb, o_sh, o_sn;
 };
@@ -198,28 +127,13 @@ struct Bars {
     // K and V rings are released separately: a K stage as soon as the Q K^T
     // products that read it have completed, a V stage after its P V
     uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
-    // per S buffer b of query tile t (one buffer, b = 0, outside
-    // neighborhood attention): s_full[2 t + b] its Q K^T has completed,
-    // p_ready[2 t + b] the softmax has written P there, o_done[2 t + b] the
-    // P V product that read that P has completed.  A parity wait is only
-    // valid while its barrier is at most one phase ahead of or behind the
-    // phase waited for; with two buffers one barrier per tile would break
-    // that (the issuer may complete the Q K^T of key tile j + 2, or the
-    // softmax finish tile j + 1, before the other side has waited for tile
-    // j), a barrier per buffer keeps it.
-    uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
-    uint64_t s_free[kNQ];      // separate P (D = 64): the softmax holds S_t in registers
+    // per query tile t: s_full its Q K^T has completed, p_ready the softmax
+    // has written P, o_done the P V product that read P has completed,
+    // s_free (separate P, D = 64) the softmax holds S_t in registers
+    uint64_t s_full[kNQ], p_ready[kNQ], o_done[kNQ], s_free[kNQ];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-};
-
-// Per-query-tile geometry of the neighborhood path.
-struct NaTile {
-    int t0, h0, w0;          // box origin
-    int u0t, u0h, u0w;       // union origin
-    int ntc, nhc, nwc;       // union t, h and w chunks (KT frames, KH rows, 16 columns)
-    int ntiles;              // key tiles = ntc * nhc * nwc (0 if the box is empty)
 };
 
 // a[t] for a per-query-tile array and a run-time t, by selects: indexing
@@ -233,62 +147,14 @@ __device__ __forceinline__ T pick(const T (&a)[kNQ], int t) {
     return r;
 }
 
-__device__ __forceinline__ NaTile na_tile(const TcParams &p, int pair, int t, int KT, int KH) {
-    NaTile g;
-    const int per_t = p.nbh * p.nbw2;
-    const int bi_t = pair / per_t, bi_h = (pair / p.nbw2) % p.nbh, bi_w = (pair % p.nbw2) * 2 + t;
-    g.t0 = bi_t * p.bt;
-    g.h0 = bi_h * p.bh;
-    g.w0 = bi_w * p.bw;
-    if (bi_w >= p.nbw) {
-        g.ntiles = 0;
-        g.u0t = g.u0h = g.u0w = g.ntc = g.nhc = g.nwc = 0;
-        return g;
-    }
-    const int t1 = imin(g.t0 + p.bt, p.T) - 1, h1 = imin(g.h0 + p.bh, p.Hg) - 1,
-              w1 = imin(g.w0 + p.bw, p.W) - 1;
-    g.u0t = na_window_start(g.t0, p.T, p.kt);
-    g.u0h = na_window_start(g.h0, p.Hg, p.kh);
-    g.u0w = na_window_start(g.w0, p.W, p.kw);
-    const int ut = na_window_start(t1, p.T, p.kt) + p.et - g.u0t;
-    const int uh = na_window_start(h1, p.Hg, p.kh) + p.eh - g.u0h;
-    const int uw = na_window_start(w1, p.W, p.kw) + p.ew - g.u0w;
-    g.ntc = cdiv(ut, KT);
-    g.nhc = cdiv(uh, KH);
-    g.nwc = cdiv(uw, kKW);
-    g.ntiles = g.ntc * g.nhc * g.nwc;
-    return g;
-}
-
-// Key sub-box of tile j: origin (t, h, w); tiles run w chunk fastest, then
-// h chunk, then t chunk.
-__device__ __forceinline__ void na_key_box(const NaTile &g, int KT, int KH, int j, int &t, int &h,
-                                           int &w) {
-    const int wc = j % g.nwc;
-    const int hc = (j / g.nwc) % g.nhc;
-    const int tc = j / (g.nwc * g.nhc);
-    t = g.u0t + tc * KT;
-    h = g.u0h + hc * KH;
-    w = g.u0w + wc * kKW;
-}
-
-// KSH = 10 KT + KH > 0 fixes the neighborhood key sub-box (KT frames x KH
-// rows x 16 columns = 96 keys) at compile time, so the softmax's masks
-// unroll without run-time tests; KSH = 0 takes KT and KH from the
-// parameters.  F16: inputs, P and output in f16 instead of bf16 (same
-// layouts; the MMA operand format flips).
-// Whether a kernel instance applies the neighborhood h / w window tests
-// through penalty channels (bf16 only: f16 cannot hold the penalty).
-template <bool NA, bool F16>
-constexpr bool na_penalty() { return NA && !F16 && kNaPenalty; }
-
-template <int D, bool NA, bool CAUSAL, int KSH, bool F16>
-__global__ void __launch_bounds__(TcCfg<D, NA, na_penalty<NA, F16>()>::NT, 1)
+// CAUSAL: grouped-query causal prefill (query tile t sees key tiles up to its
+// diagonal).  F16: inputs, P and output in f16 instead of bf16 (same layouts;
+// the MMA operand format flips).
+template <int D, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(TcCfg<D>::NT, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams p) {
-    using C = TcCfg<D, NA, na_penalty<NA, F16>()>;
-    constexpr bool PEN = na_penalty<NA, F16>();
-    static_assert(!(NA && CAUSAL), "causal prefill is a full-attention variant");
+    using C = TcCfg<D>;
     using BarsT = Bars<C::KS, C::VS>;
     static_assert(sizeof(BarsT) <= 512, "barrier block must fit its reserved bytes");
     extern __shared__ uint8_t smem_raw[];
@@ -299,29 +165,17 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
-    // full attention: batch and head of this block row, and the K/V head (the
-    // query head's KV head for grouped-query attention: contiguous groups of
-    // Hq / Hkv query heads)
-    const int fb = NA ? 0 : bh / p.H, fh = NA ? 0 : bh % p.H;
+    // batch and head of this block row, and the K/V head (the query head's KV
+    // head for grouped-query attention: contiguous groups of Hq / Hkv heads)
+    const int fb = bh / p.H, fh = bh % p.H;
     const int fkh = CAUSAL ? fh / p.group : fh;
 
     // ---- per-CTA work description (identical in every role)
     int n_t[kNQ];
     int steps;
-    NaTile g[kNQ];
-    int q0 = 0;
+    int q0;
     constexpr int BNt = C::BN;     // keys per tile
-    // neighborhood key sub-box: KT frames x KH rows x 16 columns
-    const int KT = NA ? (KSH > 0 ? KSH / 10 : p.KT) : 1;
-    const int KH = NA ? (KSH > 0 ? KSH % 10 : p.KH) : 1;
-    if constexpr (NA) {
-#pragma unroll
-        for (int t = 0; t < kNQ; ++t) {
-            g[t] = na_tile(p, blockIdx.x, t, KT, KH);
-            n_t[t] = g[t].ntiles;
-        }
-        steps = imax(n_t[0], n_t[1]);
-    } else if constexpr (CAUSAL) {
+    if constexpr (CAUSAL) {
         // heaviest query blocks first; query tile t sees key tiles 0 .. its diagonal
         q0 = (gridDim.x - 1 - blockIdx.x) * (kNQ * kBM);
         const int all = cdiv(p.Nkv, kBN);
@@ -335,129 +189,25 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         n_t[0] = n_t[1] = steps;
     }
 
-    // Barrier set-up by the last warp, channel building by the others (the
-    // two run side by side; one thread's ~25 barrier inits take ~0.5 us).
-    constexpr int NBUILD = C::NT - 32;
-    if (threadIdx.x == C::NT - 32) {
+    if (warp == C::W_INIT && lane == 0) {
         ptx::mbar_init(&bars->q_full, 1);
-        // a stage is free once every MMA issuer has released it
         for (int s = 0; s < C::KS; ++s) {
             ptx::mbar_init(&bars->k_full[s], 1);
-            ptx::mbar_init(&bars->k_empty[s], C::ISSUERS);
+            ptx::mbar_init(&bars->k_empty[s], 1);
         }
         for (int s = 0; s < C::VS; ++s) {
             ptx::mbar_init(&bars->v_full[s], 1);
-            ptx::mbar_init(&bars->v_empty[s], C::ISSUERS);
+            ptx::mbar_init(&bars->v_empty[s], 1);
         }
         for (int t = 0; t < kNQ; ++t) {
-            ptx::mbar_init(&bars->s_full[2 * t], 1);
-            ptx::mbar_init(&bars->s_full[2 * t + 1], 1);
-            ptx::mbar_init(&bars->p_ready[2 * t], 128);
-            ptx::mbar_init(&bars->p_ready[2 * t + 1], 128);
+            ptx::mbar_init(&bars->s_full[t], 1);
+            ptx::mbar_init(&bars->p_ready[t], 128);
+            ptx::mbar_init(&bars->o_done[t], 1);
             ptx::mbar_init(&bars->s_free[t], 128);
-            ptx::mbar_init(&bars->o_done[2 * t], 1);
-            ptx::mbar_init(&bars->o_done[2 * t + 1], 1);
         }
-        ptx::mbar_init(&bars->drain, C::ISSUERS);
+        ptx::mbar_init(&bars->drain, 1);
         bars->abort = 0;
         ptx::fence_barrier_init();
-    }
-    if constexpr (NA) {
-        // query rows past the box (box smaller than 128 rows) hold zeros, not stale data
-        const int rows = p.bt * p.bh * p.bw;
-        if (rows < kBM && threadIdx.x < NBUILD) {
-            for (int i = threadIdx.x; i < kNQ * C::PANELS * (kBM - rows) * 8; i += NBUILD) {
-                const int chunk = i % 8, r = rows + (i / 8) % (kBM - rows);
-                const int pt = i / (8 * (kBM - rows));          // (tile, panel)
-                *reinterpret_cast<uint4 *>(smem + C::OFF_Q + pt * C::PANEL_Q + r * 128 + chunk * 16) =
-                    make_uint4(0, 0, 0, 0);
-            }
-        }
-    }
-    if constexpr (PEN) {
-        const int rows = p.bt * p.bh * p.bw;
-        // Window channels.  Query row r carries a one in channel dh (its h
-        // offset in the box) and in channel bh + dw; key (h, w) of a penalty
-        // tile carries -penalty in channel c < bh if h lies outside the h
-        // window of box row offset c, in channel bh + c' if w lies outside the
-        // w window of box column offset c'.  The violations depend on the key's
-        // h row or w column alone: they are tabulated first as 16-bit channel
-        // masks per union row / column of each stream (in the V ring, not yet
-        // in use), and every penalty row is then expanded from the OR of two
-        // table entries.
-        // table rows per stream and axis: a box has at most kMaxPenaltyTiles
-        // (h chunk, w chunk) pairs, so <= 8 chunks of <= 6 rows or 16 columns
-        constexpr int TAB = kMaxPenaltyTiles * kKW;
-        static_assert(kMaxPenaltyTiles * 6 <= TAB && 2 * C::STREAMS * TAB * 2 <= C::STAGE_BYTES,
-                      "window tables fit their rows and one V stage");
-        uint16_t *hmask = reinterpret_cast<uint16_t *>(smem + C::OFF_V);   // [STREAMS][TAB]
-        uint16_t *wmask = hmask + C::STREAMS * TAB;                         // [STREAMS][TAB]
-        if (threadIdx.x < NBUILD) {
-            for (int i = threadIdx.x; i < 2 * C::STREAMS * TAB; i += NBUILD) {
-                const int axis = i / (C::STREAMS * TAB), u = (i / TAB) % C::STREAMS, e = i % TAB;
-                const NaTile gu = pick(g, u);    // (selects: a run-time index would spill g)
-                if (gu.ntiles == 0) continue;
-                uint32_t m = 0u;
-                if (axis == 0 && e < gu.nhc * KH) {
-                    const int kh = gu.u0h + e;
-                    for (int c = 0; c < p.bh; ++c) {
-                        const int sh = na_window_start(imin(gu.h0 + c, p.Hg - 1), p.Hg, p.kh);
-                        if (unsigned(kh - sh) >= unsigned(p.eh)) m |= 1u << c;
-                    }
-                } else if (axis == 1 && e < gu.nwc * kKW) {
-                    const int kw = gu.u0w + e;
-                    for (int c = 0; c < p.bw; ++c) {
-                        const int sw = na_window_start(imin(gu.w0 + c, p.W - 1), p.W, p.kw);
-                        if (unsigned(kw - sw) >= unsigned(p.ew)) m |= 1u << (p.bh + c);
-                    }
-                }
-                (axis == 0 ? hmask : wmask)[u * TAB + e] = uint16_t(m);
-            }
-            // one-hot offset channels of every query row (rows past the box: zero)
-            for (int i = threadIdx.x; i < kNQ * kBM * 2; i += NBUILD) {
-                const int t = i / (kBM * 2), r = (i / 2) % kBM, half = i % 2;
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
-                if (r < rows) {
-                    const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
-                    const int ch[2] = {dh, p.bh + dw};
-#pragma unroll
-                    for (int a = 0; a < 2; ++a) {
-                        const int c = ch[a] - half * 8;
-                        if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
-                    }
-                }
-                *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW + ptx::sw32_offset(r, half)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        __syncthreads();
-        const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
-        const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
-        if (threadIdx.x < NBUILD) {
-#pragma unroll
-            for (int u = 0; u < C::STREAMS; ++u) {
-                if (n_t[u] == 0) continue;
-                const int nv = g[u].nhc * g[u].nwc;
-                for (int i = threadIdx.x; i < nv * BNt * 2; i += NBUILD) {
-                    const int half = i & 1, r = (i >> 1) % BNt, v = (i >> 1) / BNt;
-                    // key r of sub-box v: h row (v / nwc) KH + (r / 16) % KH, w
-                    // column (v % nwc) 16 + r % 16 of the union (the same for
-                    // each of its KT frames)
-                    const int hc = v / g[u].nwc, wc = v - hc * g[u].nwc;
-                    const uint32_t m = uint32_t(hmask[u * TAB + hc * KH + (r / kKW) % KH]) |
-                                       uint32_t(wmask[u * TAB + wc * kKW + r % kKW]);
-                    const uint32_t bits = (m >> (half * 8)) & 0xffu;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
-                                (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
-                    *reinterpret_cast<uint4 *>(smem + C::kxv_off(u, v) + ptx::sw32_offset(r, half)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-        ptx::fence_proxy_async_smem();
     }
     if (warp == C::W_MMA) {
         ptx::tmem_alloc(&bars->tmem_base, C::TM_COLS);
@@ -483,28 +233,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             if (which == 0) {
                 ptx::prefetch_tmap(&tq);
                 const uint64_t pol_q = ptx::l2_policy_evict_first();
-                uint32_t qbytes = 0;
-                if constexpr (NA) {
-#pragma unroll
-                    for (int t = 0; t < kNQ; ++t)
-                        if (n_t[t] > 0) qbytes += C::PANELS * p.bt * p.bh * p.bw * 128;
-                } else {
-                    qbytes = kNQ * C::Q_BYTES;
-                }
-                ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+                ptx::mbar_arrive_expect_tx(&bars->q_full, kNQ * C::Q_BYTES);
 #pragma unroll
                 for (int t = 0; t < kNQ; ++t)
-                    for (int pn = 0; pn < C::PANELS; ++pn) {
-                        uint8_t *dst = smem + C::OFF_Q + t * C::Q_BYTES + pn * C::PANEL_Q;
-                        if constexpr (NA) {
-                            if (n_t[t] > 0)
-                                ptx::tma_load_5d(dst, &tq, pn * 64, g[t].w0, g[t].h0, g[t].t0, bh,
-                                                 &bars->q_full, pol_q);
-                        } else {
-                            ptx::tma_load_4d(dst, &tq, pn * 64, q0 + t * kBM, fh, fb, &bars->q_full,
-                                             pol_q);
-                        }
-                    }
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        ptx::tma_load_4d(smem + C::OFF_Q + t * C::Q_BYTES + pn * C::PANEL_Q, &tq, pn * 64,
+                                         q0 + t * kBM, fh, fb, &bars->q_full, pol_q);
             }
             const int NS = which == 0 ? C::KS : C::VS;   // depth of this ring
             int issued = 0;
@@ -513,29 +247,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 if (j >= NS && !ptx::mbar_wait_or_abort(&empty[s], ((j / NS) - 1) & 1, p.err, abort))
                     break;
                 issued = j + 1;
-                // a shared K/V stream (no neighborhood boxes) serves both query
-                // tiles, so it runs for the longer of the two tile counts
-                auto stream_has = [&](int u) { return NA ? j < n_t[u] : j < steps; };
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int u = 0; u < C::STREAMS; ++u)
-                    if (stream_has(u)) bytes += C::PANELS * BNt * 128;
-                ptx::mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-                for (int u = 0; u < C::STREAMS; ++u) {
-                    if (!stream_has(u)) continue;
-                    for (int pn = 0; pn < C::PANELS; ++pn) {
-                        uint8_t *dst =
-                            smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)) + pn * C::PANEL_KV;
-                        if constexpr (NA) {
-                            int kt_, kh_, kw_;
-                            na_key_box(g[u], KT, KH, j, kt_, kh_, kw_);
-                            ptx::tma_load_5d(dst, tm, pn * 64, kw_, kh_, kt_, bh, &full[s], pol_kv);
-                        } else {
-                            ptx::tma_load_4d(dst, tm, pn * 64, j * kBN, fkh, fb, &full[s], pol_kv);
-                        }
-                    }
-                }
+                // the K/V stream serves both query tiles, so it runs for the
+                // longer of the two tile counts
+                ptx::mbar_arrive_expect_tx(&full[s], C::KV_BYTES);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    ptx::tma_load_4d(smem + (which == 0 ? C::k_off(s) : C::v_off(s)) + pn * C::PANEL_KV, tm,
+                                     pn * 64, j * kBN, fkh, fb, &full[s], pol_kv);
             }
             // after a timeout elsewhere: let the copies this thread issued land
             // (bounded) before the CTA's shared memory is released
@@ -544,104 +261,64 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 for (int j = imax(0, issued - NS); j < issued; ++j)
                     ptx::mbar_wait(&full[j % NS], (j / NS) & 1, nullptr);
             }
-        } else if ((warp == C::W_MMA || (C::ISSUERS == kNQ && warp == C::W_MMA1)) && lane == 0) {
-            // ============================================= MMA issuers: one
-            // thread per query tile, in warps of different SM sub-partitions,
-            // so the issue of one tile's MMAs (and its barrier waits) does not
-            // wait behind the other's; both release the shared K/V stages
-            const int tt = warp == C::W_MMA ? 0 : 1;
+        } else if (warp == C::W_MMA && lane == 0) {
+            // ============================================= MMA issuer
             const uint32_t id_qk = ptx::idesc_16_f32(kBM, BNt, false, F16);
             const uint32_t id_pv = ptx::idesc_16_f32(kBM, D, true, F16);
             // Matrix descriptors are built once: a k-step, a stage or a tile only
             // moves the start-address field (bits 0-13, byte address >> 4, no
             // carry out of it below 256 KB), so each MMA costs one add here
             // instead of a rebuilt 64-bit descriptor on this single thread.
-            constexpr uint32_t HI128 = ptx::desc_hi_sw128(1024), HI32 = ptx::desc_hi_sw32(256);
+            constexpr uint32_t HI128 = ptx::desc_hi_sw128(1024);
             const uint32_t dq0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::OFF_Q), 16);
-            const uint32_t dk0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::k_off(0, 0)), 16);
-            const uint32_t dv0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::v_off(0, 0)), C::PANEL_KV);
-            uint32_t dqx0 = 0, dkx0 = 0;
-            int vq[kNQ], nv[kNQ];                // penalty tile of each tile's next Q K^T
-#pragma unroll
-            for (int t = 0; t < kNQ; ++t) {
-                vq[t] = 0;
-                nv[t] = 1;
-            }
-            if constexpr (NA) {
-                dqx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::OFF_QX));
-                dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(0, 0)));
-#pragma unroll
-                for (int t = 0; t < kNQ; ++t) nv[t] = imax(1, g[t].nhc * g[t].nwc);
-            }
+            const uint32_t dk0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::k_off(0)), 16);
+            const uint32_t dv0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::v_off(0)), C::PANEL_KV);
             constexpr int nkv = BNt / 16;        // k-steps of P V
             auto issue_qk = [&](int t, int j) {
-                const int s = j % C::KS;
                 const uint32_t a0 = dq0 + uint32_t((t * C::Q_BYTES) >> 4);
-                const uint32_t b0 =
-                    dk0 + uint32_t((s * C::STAGE_BYTES + (C::STREAMS == 1 ? 0 : t) * C::KV_BYTES) >> 4);
+                const uint32_t b0 = dk0 + uint32_t(((j % C::KS) * C::KV_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = ((kk >> 2) * C::PANEL_Q + (kk & 3) * 32) >> 4;
                     const uint32_t ob = ((kk >> 2) * C::PANEL_KV + (kk & 3) * 32) >> 4;
-                    ptx::mma_ss(tmem + C::tm_s(t, C::buf_of(j)), ptx::desc_join(a0 + oa, HI128),
+                    ptx::mma_ss(tmem + C::tm_s(t), ptx::desc_join(a0 + oa, HI128),
                                 ptx::desc_join(b0 + ob, HI128), id_qk, kk > 0);
                 }
-                if constexpr (PEN) {
-                    // + window penalties: one more k-step over the 16 extra channels;
-                    // QK_t(j) uses penalty tile j mod (h chunks x w chunks)
-                    const uint32_t a = dqx0 + uint32_t((t * kBM * C::X_ROW) >> 4);
-                    const uint32_t b = dkx0 + uint32_t(((t * C::MAXV + vq[t]) * C::KX_BYTES) >> 4);
-                    if (++vq[t] == nv[t]) vq[t] = 0;
-                    ptx::mma_ss(tmem + C::tm_s(t, C::buf_of(j)), ptx::desc_join(a, HI32), ptx::desc_join(b, HI32),
-                                id_qk, 1u);
-                }
-                ptx::tc_commit(&bars->s_full[2 * t + C::buf_of(j)]);
+                ptx::tc_commit(&bars->s_full[t]);
             };
             auto issue_pv = [&](int t, int j) {
-                const int s = j % C::VS;
-                const uint32_t b0 =
-                    dv0 + uint32_t((s * C::STAGE_BYTES + (C::STREAMS == 1 ? 0 : t) * C::KV_BYTES) >> 4);
-                const uint32_t a0 = tmem + C::tm_p(t, C::buf_of(j));
+                const uint32_t b0 = dv0 + uint32_t(((j % C::VS) * C::KV_BYTES) >> 4);
+                const uint32_t a0 = tmem + C::tm_p(t);
 #pragma unroll
                 for (int kk = 0; kk < nkv; ++kk)
                     ptx::mma_ts(tmem + C::tm_o(t), a0 + kk * 8,
                                 ptx::desc_join(b0 + uint32_t(kk * (2048 >> 4)), HI128), id_pv,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                ptx::tc_commit(&bars->o_done[2 * t + C::buf_of(j)]);
+                ptx::tc_commit(&bars->o_done[t]);
             };
             bool ok = ptx::mbar_wait_or_abort(&bars->q_full, 0, p.err, abort) &&
                       (steps == 0 || ptx::mbar_wait_or_abort(&bars->k_full[0], 0, p.err, abort));
             ptx::tc_fence_after();
-            // query tiles of this issuer: its own one, or both with one issuer
-            const int t_lo = C::ISSUERS == kNQ ? tt : 0, t_hi = C::ISSUERS == kNQ ? tt + 1 : kNQ;
-            // every stage barrier counts one release per issuer and use
-            auto release = [&](uint64_t *bar) { ptx::tc_commit(bar); };
-            // Each stage barrier is waited on once per issuer and use (a completed
-            // wait still costs this thread a round trip to shared memory).
+            // Each stage barrier is waited on once per use (a completed wait
+            // still costs this thread a round trip to shared memory).
             bool k_seen = false, v_seen = false;
             auto wait_k = [&](int jn) {
                 if (!k_seen) {
-                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[jn % C::KS], (jn / C::KS) & 1,
-                                                       p.err, abort);
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[jn % C::KS], (jn / C::KS) & 1, p.err, abort);
                     k_seen = true;
                 }
             };
             auto wait_v = [&](int j) {
                 if (!v_seen) {
-                    ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[j % C::VS], (j / C::VS) & 1,
-                                                       p.err, abort);
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[j % C::VS], (j / C::VS) & 1, p.err, abort);
                     v_seen = true;
                 }
             };
             // Q K^T of key tile jn for tile t, once the softmax no longer needs
-            // the S buffer it overwrites; a K stage this tile does not read (its
-            // key tiles have run out) is still released only once it has been
-            // filled, so that an issuer running ahead cannot complete a stage
-            // phase in place of the other issuer
+            // the S it overwrites (separate P: as soon as the softmax holds
+            // S(jprev) in registers; P over S: after P V (jprev), issued before)
             auto next_qk = [&](int t, int jn, int jprev) {
                 if (jn < pick(n_t, t)) {
-                    // separate P: as soon as the softmax holds S(jprev) in
-                    // registers; P over S: after P V (jprev), issued before
                     if (C::SEP_P)
                         ok = ok && ptx::mbar_wait_or_abort(&bars->s_free[t], jprev & 1, p.err, abort);
                     wait_k(jn);
@@ -655,8 +332,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             // P V of key tile j for tile t
             auto this_pv = [&](int t, int j) {
                 if (j < pick(n_t, t)) {
-                    ok = ok && ptx::mbar_wait_or_abort(&bars->p_ready[2 * t + C::buf_of(j)],
-                                                       C::par_of(j), p.err, abort);
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->p_ready[t], j & 1, p.err, abort);
                     wait_v(j);
                     if (!ok) return;
                     ptx::tc_fence_after();
@@ -666,54 +342,39 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 }
             };
             if (ok) {
-                for (int t = t_lo; t < t_hi; ++t)
-                    if (pick(n_t, t) > 0) issue_qk(t, 0);
-                if (steps > 0) release(&bars->k_empty[0]);
-            }
-            // two S buffers: the Q K^T of key tile 1 right away, so the issuer
-            // runs one key tile ahead of the softmax
-            constexpr int AHEAD = C::SBUF;       // QK(j + AHEAD) follows PV(j)
-            if (C::SBUF == 2 && ok && steps > 1) {
-                for (int t = t_lo; ok && t < t_hi; ++t) next_qk(t, 1, 0);
-                if (ok) release(&bars->k_empty[1 % C::KS]);
+#pragma unroll
+                for (int t = 0; t < kNQ; ++t)
+                    if (n_t[t] > 0) issue_qk(t, 0);
+                if (steps > 0) ptx::tc_commit(&bars->k_empty[0]);
             }
             for (int j = 0; ok && j < steps; ++j) {
-                const int jn = j + AHEAD;
+                const int jn = j + 1;
                 k_seen = v_seen = false;
-                if constexpr (C::ISSUERS == 1) {
-                    // one issuer for both tiles (compile-time tile indices)
-                    if constexpr (C::SEP_P) {
-                        // separate P (one S buffer): the next S as soon as the
-                        // softmax holds the current one in registers, then P V
+                if constexpr (C::SEP_P) {
+                    // separate P: the next S as soon as the softmax holds the
+                    // current one in registers, then P V
 #pragma unroll
-                        for (int t = 0; t < kNQ; ++t)
-                            if (ok && jn < steps) next_qk(t, jn, j);
+                    for (int t = 0; t < kNQ; ++t)
+                        if (ok && jn < steps) next_qk(t, jn, j);
 #pragma unroll
-                        for (int t = 0; t < kNQ; ++t)
-                            if (ok) this_pv(t, j);
-                    } else {
-                        // P over S: the Q K^T that overwrites the S buffer of key
-                        // tile j follows the P V that reads P there (one thread's
-                        // MMAs execute in issue order)
-#pragma unroll
-                        for (int t = 0; t < kNQ; ++t) {
-                            if (ok) this_pv(t, j);
-                            if (ok && jn < steps) next_qk(t, jn, j);
-                        }
-                    }
+                    for (int t = 0; t < kNQ; ++t)
+                        if (ok) this_pv(t, j);
                 } else {
-                    // one issuer per tile: P over S in two buffers
-                    static_assert(C::ISSUERS == 1 || !C::SEP_P, "per-tile issuers use P over S");
-                    this_pv(tt, j);
-                    if (ok && jn < steps) next_qk(tt, jn, j);
+                    // P over S: the Q K^T that overwrites S_t follows the P V that
+                    // reads P there (one thread's MMAs execute in issue order)
+#pragma unroll
+                    for (int t = 0; t < kNQ; ++t) {
+                        if (ok) this_pv(t, j);
+                        if (ok && jn < steps) next_qk(t, jn, j);
+                    }
                 }
                 if (!ok) break;
-                // Q K^T of key tile j + AHEAD and P V of key tile j are issued
-                if (jn < steps) release(&bars->k_empty[jn % C::KS]);
-                release(&bars->v_empty[j % C::VS]);
+                // Q K^T of key tile j + 1 and P V of key tile j are issued
+                if (jn < steps) ptx::tc_commit(&bars->k_empty[jn % C::KS]);
+                ptx::tc_commit(&bars->v_empty[j % C::VS]);
             }
-            // drain: every MMA of every issuer has completed before TMEM is freed
-            release(&bars->drain);
+            // drain: every MMA has completed before TMEM is freed
+            ptx::tc_commit(&bars->drain);
             ptx::mbar_wait(&bars->drain, 0, p.err);
         }
     } else {
@@ -724,36 +385,16 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         const int row = quarter * 32 + lane;     // query row within the tile
         const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
         const uint32_t o_addr = lane_base + C::tm_o(t);
+        const uint32_t s_addr = lane_base + C::tm_s(t);
+        const uint32_t p_addr = lane_base + C::tm_p(t);
         const float cl = p.c_log2;
-        constexpr int NG = BNt / 16;             // 16-key groups per key tile
-
-        // query of this row (neighborhood path) and its window
-        int qt = 0, qh = 0, qw = 0, wst = 0, wsh = 0, wsw = 0;
-        bool qvalid;
-        const NaTile gt = pick(g, t);           // this warp's tile, in registers
         const int nt = pick(n_t, t);
-        if constexpr (NA) {
-            const int dt = row / (p.bh * p.bw), dh = (row / p.bw) % p.bh, dw = row % p.bw;
-            qt = gt.t0 + dt;
-            qh = gt.h0 + dh;
-            qw = gt.w0 + dw;
-            qvalid = nt > 0 && row < p.bt * p.bh * p.bw && qt < p.T && qh < p.Hg && qw < p.W;
-            wst = na_window_start(imin(qt, p.T - 1), p.T, p.kt);
-            if constexpr (!PEN) {
-                wsh = na_window_start(imin(qh, p.Hg - 1), p.Hg, p.kh);
-                wsw = na_window_start(imin(qw, p.W - 1), p.W, p.kw);
-            }
-        } else {
-            qvalid = q0 + t * kBM + row < p.Nq;
-        }
+        const bool qvalid = q0 + t * kBM + row < p.Nq;
 
         // waits for the P V product of key tile jj of this query tile (and so
-        // for every earlier one: one thread's MMAs complete in issue order).
-        // Valid while the P V of key tile jj - 2 is known complete: it is once
-        // the softmax holds S(jj), whose Q K^T was issued after it.
+        // for every earlier one: one thread's MMAs complete in issue order)
         auto wait_pv = [&](int jj) -> bool {
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[2 * t + C::buf_of(jj)],
-                                                                 C::par_of(jj), p.err, abort)))
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[t], jj & 1, p.err, abort)))
                 return false;
             ptx::tc_fence_after();
             return true;
@@ -761,44 +402,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        // neighborhood: key sub-box counters (w fastest, then h, then t)
-        int tc = 0, hc = 0, wc = 0;
         for (int j = 0; j < nt; ++j) {
-            const uint32_t s_addr = lane_base + C::tm_s(t, C::buf_of(j));
-            const uint32_t p_addr = lane_base + C::tm_p(t, C::buf_of(j));
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->s_full[2 * t + C::buf_of(j)],
-                                                                 C::par_of(j), p.err, abort))) {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->s_full[t], j & 1, p.err, abort))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-
-            // ---- neighborhood: the h and w window penalties are already in S
-            //      (bf16: extra MMA channels); a row whose t window misses the
-            //      frame of a 16-key group gets P = 0 there (bit g of gmask
-            //      clear).  (Skipping sub-boxes that none of a warp's 32 windows
-            //      reaches measured slower than computing them: the MMAs run
-            //      anyway and the test costs issue slots on the critical path.)
-            uint32_t gmask = (1u << NG) - 1u;
-            int kh0 = 0, kw0 = 0;                // key sub-box origin along h and w
-            if constexpr (NA) {
-                const int kt0 = gt.u0t + tc * KT;
-                kh0 = gt.u0h + hc * KH;
-                kw0 = gt.u0w + wc * kKW;
-                if (++wc == gt.nwc) {
-                    wc = 0;
-                    if (++hc == gt.nhc) {
-                        hc = 0;
-                        ++tc;
-                    }
-                }
-                gmask = 0u;
-                if (qvalid) {
-#pragma unroll
-                    for (int gq = 0; gq < NG; ++gq)   // group gq holds frame kt0 + gq / KH
-                        if (unsigned(kt0 + gq / KH - wst) < unsigned(p.et)) gmask |= 1u << gq;
-                }
-            }
 
             float sv[BNt];
 #pragma unroll
@@ -811,30 +420,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 ptx::mbar_arrive(&bars->s_free[t]);
             }
 
-            // ---- masks
-            if constexpr (NA && !PEN) {
-                // the h and w window tests per key (f16, whose range cannot hold
-                // a window penalty, and bf16 without penalty channels).  Key e of the (KT, KH, 16)
-                // sub-box sits at h = kh0 + (e / 16) % KH, w = kw0 + e % 16; wm / hm
-                // hold the in-window w columns / h rows of this row.
-                const int lw = wsw - kw0, lh = wsh - kh0;
-                const int aw = imax(lw, 0), bw = imin(lw + p.ew, kKW);
-                const int ah = imax(lh, 0), bh_ = imin(lh + p.eh, KH);
-                const uint32_t wm = aw < bw ? ((1u << bw) - 1u) & ~((1u << aw) - 1u) : 0u;
-                const uint32_t hm = ah < bh_ ? ((1u << bh_) - 1u) & ~((1u << ah) - 1u) : 0u;
-#pragma unroll
-                for (int gq = 0; gq < NG; ++gq) {
-                    const bool hin = (hm >> (gq % KH)) & 1u;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (!hin || !((wm >> i) & 1u)) sv[gq * 16 + i] = -INFINITY;
-                }
-            } else if constexpr (!NA) {
-                int valid = p.Nkv - j * BNt;           // keys of this tile inside the sequence
+            // ---- masks: keys past the sequence; causal: the last tile is the
+            //      diagonal one (query tile and key tile start at the same
+            //      position), key e is visible to row `row` iff e <= row
+            {
+                int valid = p.Nkv - j * BNt;
                 if constexpr (CAUSAL) {
-                    // the last tile is the diagonal one (query tile and key tile
-                    // start at the same position): key e is visible to row `row`
-                    // iff e <= row
                     if (j == nt - 1) {
 #pragma unroll
                         for (int e = 0; e < BNt; ++e)
@@ -849,33 +440,18 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 }
             }
 
-            // neighborhood: 16-key groups that no row of this warp may see (a
-            // 32-key chunk whose frames lie outside all 32 rows' t windows)
-            // are written as P = 0 without exponentials
-            const uint32_t wlive = NA ? __reduce_or_sync(0xffffffffu, gmask) : ~0u;
-
-            // P = 2^(x - m) in 16-bit into TMEM (groups outside gm: P = 0);
-            // returns the tile's row sum (fp32)
-            auto emit_p = [&](float nmu, uint32_t gm) -> float {
+            // P = 2^(x - m) in 16-bit into TMEM; returns the tile's row sum (fp32)
+            auto emit_p = [&](float nmu) -> float {
                 float acc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
                 for (int c = 0; c < BNt / 32; ++c) {
                     uint32_t pk[16];
-                    if (((wlive >> (2 * c)) & 3u) == 0u) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
-                        ptx::tmem_st16(p_addr + c * 16, pk);
-                        continue;
-                    }
-                    const float n0 = ((gm >> (2 * c)) & 1u) ? nmu : -INFINITY;
-                    const float n1 = ((gm >> (2 * c + 1)) & 1u) ? nmu : -INFINITY;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float nm = e < 8 ? n0 : n1;
                         float x0, x1;
-                        ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nm, nm);
+                        ptx::ffma2(x0, x1, sv[c * 32 + 2 * e], sv[c * 32 + 2 * e + 1], cl, cl, nmu, nmu);
                         const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                         ptx::fadd2(acc[(2 * e) & 7], acc[(2 * e + 1) & 7], acc[(2 * e) & 7],
                                    acc[(2 * e + 1) & 7], p0, p1);
@@ -886,10 +462,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             };
 
-            // ---- P in columns of its own (one buffer): the P V product that
-            //      last read them (key tile j - 1) must be done.  P over S needs no
-            //      wait: the Q K^T that wrote this S was issued after the P V that
-            //      read the P last held here, and MMAs complete in issue order.
+            // ---- P in columns of its own: the P V product that last read them
+            //      (key tile j - 1) must be done.  P over S needs no wait: the
+            //      Q K^T that wrote this S was issued after the P V that read the
+            //      P last held here, and MMAs complete in issue order.
             bool prev_done = false;              // P V of tile j - 1 observed complete
             if (C::SEP_P && j >= 1) {
                 if (!wait_pv(j - 1)) {
@@ -903,13 +479,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             //      stands, with no tile maximum.  P only has to stay finite in its
             //      16-bit type, not below 1: a tile whose row sum exceeds 2^24 (2^15
             //      for f16, whose largest finite value is 65504) or is not finite
-            //      (scores far above m, or m still the garbage of a row whose
-            //      first tiles were all outside its window) is redone below
-            //      against its own maximum.  After the first tiles m is close to
-            //      the row maximum and the redo almost never runs.
-            bool fast = j > 0 && __all_sync(0xffffffffu, !(gmask != 0u && m == -INFINITY));
+            //      is redone below against its own maximum.  After the first tiles
+            //      m is close to the row maximum and the redo almost never runs.
+            bool fast = j > 0 && __all_sync(0xffffffffu, m != -INFINITY);
             if (fast) {
-                const float lt = emit_p(-m, gmask);
+                const float lt = emit_p(-m);
                 if (__any_sync(0xffffffffu, !(lt <= (F16 ? 32768.f : 16777216.f))))
                     fast = false;                 // redo the tile (P is rewritten below)
                 else
@@ -917,17 +491,18 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             }
 
             if (!fast) {
-                // ---- tile maximum over the groups this row may see
-                float tmax = -INFINITY;
+                // ---- tile maximum
+                float mx[8];
 #pragma unroll
-                for (int gq = 0; gq < NG; ++gq) {
-                    float mx[8];
+                for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[gq * 16 + i], sv[gq * 16 + 8 + i]);
-                    const float gmx = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
-                                                 ptx::fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-                    if ((gmask >> gq) & 1u) tmax = fmaxf(tmax, gmx);
+                for (int e = 0; e < BNt; e += 8) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], sv[e + i]);
                 }
+                const float tmax = fmaxf(ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]), ptx::fmax3(mx[3], mx[4], mx[5]),
+                                                    mx[6]),
+                                         mx[7]);
                 const float mt = tmax * cl;      // cl > 0: max commutes with the scaling
 
                 // ---- the previous P V must be done before O is rescaled
@@ -965,25 +540,20 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         m = mt;
                     }
                 }
-                l += emit_p((m == -INFINITY) ? 0.f : -m, gmask);
+                l += emit_p((m == -INFINITY) ? 0.f : -m);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bars->p_ready[2 * t + C::buf_of(j)]);
+            ptx::mbar_arrive(&bars->p_ready[t]);
         }
 
-        // ---- epilogue: O / l -> bf16 -> global
+        // ---- epilogue: O / l -> 16-bit -> global
         if (ok && nt > 0 && wait_pv(nt - 1)) {
             const float inv = 1.f / l;
             typename H16<F16>::T *orow = nullptr;
-            if (qvalid) {
-                size_t idx;
-                if constexpr (NA)
-                    idx = ((size_t(bh) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw) * D;
-                else
-                    idx = size_t(fb * p.o_sb + fh * p.o_sh + (long long)(q0 + t * kBM + row) * p.o_sn);
-                orow = static_cast<typename H16<F16>::T *>(p.o) + idx;
-            }
+            if (qvalid)
+                orow = static_cast<typename H16<F16>::T *>(p.o) +
+                       size_t(fb * p.o_sb + fh * p.o_sh + (long long)(q0 + t * kBM + row) * p.o_sn);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
@@ -995,7 +565,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         wp[e] = H16<F16>::pack(__uint_as_float(ov[2 * e]) * inv,
-                                            __uint_as_float(ov[2 * e + 1]) * inv);
+                                               __uint_as_float(ov[2 * e + 1]) * inv);
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dst[e] = w4[e];
@@ -1135,13 +705,13 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
 }
 
-template <int D, bool NA, bool CAUSAL = false, int KSH = 0, bool F16 = false>
+template <int D, bool CAUSAL = false, bool F16 = false>
 attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &tk,
                         const CUtensorMap &tv, const TcParams &p, dim3 grid) {
-    using C = TcCfg<D, NA, na_penalty<NA, F16>()>;
+    using C = TcCfg<D>;
     static int done_mask = 0;
     static int regs = -1;
-    auto kern = tc_attn_kernel<D, NA, CAUSAL, KSH, F16>;
+    auto kern = tc_attn_kernel<D, CAUSAL, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
     // The warpgroups re-split the launch's register file with setmaxnreg; the
@@ -1156,7 +726,7 @@ attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
     }
     if (regs != C::REGS_LAUNCH) return ATTN_ERR_UNSUPPORTED;
     kern<<<grid, C::NT, C::SMEM, c.stream>>>(tq, tk, tv, p);
-    return launch_status(NA ? kFamTcNa : kFamTcFlash);
+    return launch_status(kFamTcFlash);
 }
 
 }  // namespace
@@ -1245,10 +815,9 @@ attn_status_t tc_full(const Ctx &c, attn_dtype_t dt, const void *q, const void *
     p.o_sb = s4[3].b; p.o_sh = s4[3].h; p.o_sn = s4[3].n;
     const dim3 grid(cdiv(Nq, kNQ * kBM), B * H);
     if (f16)
-        return D == 128 ? launch_tc<128, false, false, 0, true>(c, tq, tk, tv, p, grid)
-                        : launch_tc<64, false, false, 0, true>(c, tq, tk, tv, p, grid);
-    return D == 128 ? launch_tc<128, false>(c, tq, tk, tv, p, grid)
-                    : launch_tc<64, false>(c, tq, tk, tv, p, grid);
+        return D == 128 ? launch_tc<128, false, true>(c, tq, tk, tv, p, grid)
+                        : launch_tc<64, false, true>(c, tq, tk, tv, p, grid);
+    return D == 128 ? launch_tc<128>(c, tq, tk, tv, p, grid) : launch_tc<64>(c, tq, tk, tv, p, grid);
 }
 
 attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const void *k,
@@ -1277,10 +846,9 @@ attn_status_t tc_causal_gqa(const Ctx &c, attn_dtype_t dt, const void *q, const 
     p.o_sb = so.b; p.o_sh = so.h; p.o_sn = so.n;
     const dim3 grid(cdiv(N, kNQ * kBM), B * Hq);
     if (f16)
-        return D == 128 ? launch_tc<128, false, true, 0, true>(c, tq, tk, tv, p, grid)
-                        : launch_tc<64, false, true, 0, true>(c, tq, tk, tv, p, grid);
-    return D == 128 ? launch_tc<128, false, true>(c, tq, tk, tv, p, grid)
-                    : launch_tc<64, false, true>(c, tq, tk, tv, p, grid);
+        return D == 128 ? launch_tc<128, true, true>(c, tq, tk, tv, p, grid)
+                        : launch_tc<64, true, true>(c, tq, tk, tv, p, grid);
+    return D == 128 ? launch_tc<128, true>(c, tq, tk, tv, p, grid) : launch_tc<64, true>(c, tq, tk, tv, p, grid);
 }
 
 attn_status_t tc_selftest(const Ctx &c, const void *q, const void *k, const void *v,

@@ -43,6 +43,9 @@ _NEAR_LIMIT_LENS = tuple(int(x) for x in np.random.default_rng(7902).integers(1,
     ("gqa_decode", dict(B=2, H=8, Hkv=2, D=128, Lmax=200, seq_len=(200, 37), seed=7901)),
     # 1000 (batch, kv-head) pairs x 8 heads x 128 channels: 4,164,000 of 4,194,304 bytes
     ("gqa_decode", dict(B=125, H=64, Hkv=8, D=128, Lmax=64, seq_len=_NEAR_LIMIT_LENS, seed=7902)),
+    # 8 (batch, kv-head) pairs of 4096 rows: 16 splits each, more than the
+    # merge that requests every split at once takes (its general loop runs)
+    ("gqa_decode", dict(B=1, H=32, Hkv=8, D=128, Lmax=4096, seq_len=(4096,), seed=7903)),
 ])
 def test_noalloc_decode_matches_workspace_decode_twice(name, overrides):
     import torch

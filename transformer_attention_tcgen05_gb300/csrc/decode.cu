@@ -51,6 +51,7 @@ constexpr int kSlots = 4;       // ring slots (one chunk each); chunk i -> slot 
 static_assert(kSlots % kCW == 0, "every slot must always feed the same consumer warp");
 constexpr int kMaxSplits = 256;
 constexpr int kMaxClusterSplits = 8;   // portable cluster size
+constexpr int kFastMergeSplits = 8;    // workspace merge with all split loads in flight at once
 
 template <int D, int GP>
 struct DecCfg {
@@ -122,6 +123,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int unit = b * p.Hkv + kvh;
 
+    // q of the G heads of this KV head: its loads go out first, before any
+    // cache copy of the grid floods the memory system (issued after the
+    // barrier set-up, they took ~3.6 us and held up the consumers while the
+    // ring sat full)
+    constexpr int QL = (GP * D / 8 + kCW * 32 - 1) / (kCW * 32);   // 16-byte loads per consumer thread
+    uint4 qraw[QL];
+#pragma unroll
+    for (int i = 0; i < QL; ++i) {
+        qraw[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int e = threadIdx.x + i * kCW * 32;
+        if (warp < kCW && e < GP * D / 8) {
+            const int h = (e * 8) / D, d = (e * 8) % D;
+            if (h < p.G)
+                qraw[i] = *reinterpret_cast<const uint4 *>(static_cast<const typename H16<F16>::T *>(p.q) +
+                                                          (size_t(b) * p.Hq + kvh * p.G + h) * D + d);
+        }
+    }
+
     const int len = p.seq_len[b];
     if (len < 1 || (!p.ring && len > p.Lmax)) {   // invalid length: report, touch nothing
         if (threadIdx.x == 0) raise_device_error(p.err, kDevCheck);
@@ -142,22 +161,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
     }
     __syncthreads();
     if (warp < kCW) {
-        // q of the G heads of this KV head, pre-scaled, fp32 (padding heads are
-        // zero), loaded by the consumers while the producer's first copies fly
-        for (int e = threadIdx.x; e < GP * D / 8; e += kCW * 32) {
-            const int h = (e * 8) / D, d = (e * 8) % D;
-            float x[8];
-            if (h < p.G) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(
-                    static_cast<const typename H16<F16>::T *>(p.q) +
-                    (size_t(b) * p.Hq + kvh * p.G + h) * D + d);
-                x8_to_f32<F16>(u, x);
-            } else {
+        // q pre-scaled to fp32 in shared memory (padding heads are zero)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        for (int i = 0; i < QL; ++i) {
+            const int e = threadIdx.x + i * kCW * 32;
+            if (e < GP * D / 8) {
+                float x[8];
+                x8_to_f32<F16>(qraw[i], x);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) q_s[e * 8 + c] = x[c] * p.qscale;
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q_s[h * D + d + i] = x[i] * p.qscale;
         }
         ptx::named_barrier_sync(2, kCW * 32);
     }
@@ -458,6 +471,33 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
         }
     }
     __syncthreads();
+    if (p.splits <= kFastMergeSplits) {
+        // every partial this thread needs is requested before the first is
+        // used (one round trip to L2 instead of one per output and 4 splits)
+        constexpr int OPT = (GP * D + C::NT - 1) / C::NT;   // outputs per thread
+        float v[OPT][kFastMergeSplits];
+#pragma unroll
+        for (int k = 0; k < OPT; ++k) {
+            const int e = threadIdx.x + k * C::NT, h = e / D, d = e % D;
+#pragma unroll
+            for (int s = 0; s < kFastMergeSplits; ++s)
+                v[k][s] = (e < p.G * D && s < p.splits) ? __ldcg(po + (s * GP + h) * D + d) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < OPT; ++k) {
+            const int e = threadIdx.x + k * C::NT, h = e / D, d = e % D;
+            if (e < p.G * D) {
+                float O = 0.f;
+#pragma unroll
+                for (int s = 0; s < kFastMergeSplits; ++s)
+                    if (s < p.splits) O += v[k][s] * wgt[(s * GP + h) * 2 + 1];
+                static_cast<typename H16<F16>::T *>(p.o)[(size_t(b) * p.Hq + kvh * p.G + h) * D + d] =
+                    H16<F16>::from(O);
+            }
+        }
+        if (threadIdx.x == 0) p.tickets[unit] = 0u;   // ready for the next call
+        return;
+    }
     for (int e = threadIdx.x; e < p.G * D; e += C::NT) {
         const int h = e / D, d = e % D;
         float O = 0.f;
@@ -608,13 +648,21 @@ attn_status_t launch_cluster(const Ctx &c, const CUtensorMap &tk, const CUtensor
     return launch_status(kFamDecode);
 }
 
-// Cluster merge when every unit's cluster fits one wave; else the workspace
-// (atomic ticket) merge.
+// Cluster merge when every unit's cluster fits one wave, unless the
+// workspace (atomic ticket) merge at the call's split count spreads the cache
+// over the SMs clearly more evenly: the time of the loop is set by the SM
+// with the most CTAs, i.e. by ceil(units x splits / SMs) / splits of a unit.
+// (64 units on 152 SMs: clusters of 6 leave SMs with 3 and 2 CTAs of 1/6 of a
+// unit each, 7 workspace splits 3 CTAs of 1/7; measured 30.8 vs 30.1 us.)
 template <int D, int GP, bool F16>
 attn_status_t launch_best(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
                           DecParams p, int B, int Lmax) {
-    const int cs = cluster_splits<D, GP, F16>(c, B * p.Hkv, p.splits);
-    if (cs >= 2) {
+    const int units = B * p.Hkv;
+    const int cs = cluster_splits<D, GP, F16>(c, units, p.splits);
+    auto load = [&](int sp) { return double(cdiv(units * sp, imax(1, c.sm_count))) / sp; };
+    const bool ws_even =
+        cs >= 2 && p.splits <= kFastMergeSplits && p.splits > cs && load(p.splits) < 0.9 * load(cs);
+    if (cs >= 2 && !ws_even) {
         p.splits = cs;
         p.split_rows = cdiv(cdiv(Lmax, cs), kRowsPerChunk) * kRowsPerChunk;
         return launch_cluster<D, GP, F16>(c, tk, tv, p, B);

@@ -584,78 +584,85 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         int G = 0;                               // key tiles of this tile in earlier items
         unsigned long long last_sig = ~0ull;
         int rbs = 0;                             // channel rebuilds done by this warpgroup
-        for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+        // The key penalty channels of box gx, rebuilt unless they are the ones
+        // in place.  Every Q K^T of the tile so far must have completed (this
+        // warpgroup has read all their scores); the issuer waits for
+        // chan_ready before the next one.  For key (h, w) of the sub-box of h
+        // chunk hc and w chunk wc, channel c < bh holds -penalty if h lies
+        // outside the h window of box row offset c, channel bh + c' likewise
+        // for w: tabulated per union row / column first, then each channel row
+        // is the OR of two entries.
+        auto ensure_channels = [&](const NaTile &gx) -> bool {
+            const unsigned long long sig = na_sig(p, gx);
+            if (sig == last_sig) return true;
+            last_sig = sig;
+            // every thread of the warpgroup is done reading the previous tables
+            if (rbs > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_free[t],
+                                                                             (rbs - 1) & 1, p.err, abort))) {
+                return false;
+            }
+            for (int i = row; i < 2 * C::TAB; i += 128) {
+                const int axis = i / C::TAB, e = i % C::TAB;
+                uint32_t m = 0u;
+                if (axis == 0 && e < gx.nhc * KH) {
+                    const int kh = gx.u0h + e;
+                    for (int c = 0; c < p.bh; ++c) {
+                        const int sh = na_window_start(imin(gx.h0 + c, p.Hg - 1), p.Hg, p.kh);
+                        if (unsigned(kh - sh) >= unsigned(p.eh)) m |= 1u << c;
+                    }
+                } else if (axis == 1 && e < gx.nwc * kKW) {
+                    const int kw = gx.u0w + e;
+                    for (int c = 0; c < p.bw; ++c) {
+                        const int sw = na_window_start(imin(gx.w0 + c, p.W - 1), p.W, p.kw);
+                        if (unsigned(kw - sw) >= unsigned(p.ew)) m |= 1u << (p.bh + c);
+                    }
+                }
+                (axis == 0 ? tab_h : tab_w)[e] = uint16_t(m);
+            }
+            ptx::mbar_arrive(&bars->tab_done[t]);
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_done[t], rbs & 1, p.err, abort))) {
+                return false;
+            }
+            const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
+            const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
+            const int nvt = gx.nhc * gx.nwc;
+            for (int i = row; i < nvt * kBN * 2; i += 128) {
+                const int half = i & 1, r = (i >> 1) % kBN, v = (i >> 1) / kBN;
+                // key r of sub-box v: union h row (v / nwc) KH + (r / 16) % KH,
+                // w column (v % nwc) 16 + r % 16 (the same in each of its KT frames)
+                const int hc = v / gx.nwc, wc = v - hc * gx.nwc;
+                const uint32_t m = uint32_t(tab_h[hc * KH + (r / kKW) % KH]) |
+                                   uint32_t(tab_w[wc * kKW + r % kKW]);
+                const uint32_t bits = (m >> (half * 8)) & 0xffu;
+                uint32_t w[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
+                            (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
+                *reinterpret_cast<uint4 *>(smem + C::kxv_off(t, v) + ptx::sw32_offset(r, half)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bars->chan_ready[t]);
+            ptx::mbar_arrive(&bars->tab_free[t]);
+            ++rbs;
+            return true;
+        };
+        // this tile's next item with work (the second box of a pair past the
+        // grid's w extent has none)
+        auto next_item = [&](int from) -> int {
+            for (int i = from; i < p.n_items; i += gridDim.x)
+                if (pick(na_item(p, i, KT, KH).n, t) > 0) return i;
+            return p.n_items;
+        };
+        int it = next_item(blockIdx.x);
+        if constexpr (PEN) {
+            if (it < p.n_items && !ensure_channels(pick(na_item(p, it, KT, KH).g, t))) ok = false;
+        }
+        while (ok && it < p.n_items) {
             const NaItem I = na_item(p, it, KT, KH);
             const int nt = pick(I.n, t);
-            if (nt == 0) continue;
             const NaTile gt = pick(I.g, t);
-
-            if constexpr (PEN) {
-                const unsigned long long sig = na_sig(p, gt);
-                if (sig != last_sig) {
-                    // ---- rebuild this tile's key penalty channels.  Every Q K^T
-                    // of the tile so far has completed (this warpgroup has read
-                    // all their scores); the issuer waits for chan_ready before
-                    // the next one.  For key (h, w) of the sub-box of h chunk hc
-                    // and w chunk wc, channel c < bh holds -penalty if h lies
-                    // outside the h window of box row offset c, channel bh + c'
-                    // likewise for w: tabulated per union row / column first,
-                    // then each channel row is the OR of two entries.
-                    last_sig = sig;
-                    // every thread of the warpgroup is done reading the previous tables
-                    if (rbs > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_free[t],
-                                                                                     (rbs - 1) & 1, p.err, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    for (int i = row; i < 2 * C::TAB; i += 128) {
-                        const int axis = i / C::TAB, e = i % C::TAB;
-                        uint32_t m = 0u;
-                        if (axis == 0 && e < gt.nhc * KH) {
-                            const int kh = gt.u0h + e;
-                            for (int c = 0; c < p.bh; ++c) {
-                                const int sh = na_window_start(imin(gt.h0 + c, p.Hg - 1), p.Hg, p.kh);
-                                if (unsigned(kh - sh) >= unsigned(p.eh)) m |= 1u << c;
-                            }
-                        } else if (axis == 1 && e < gt.nwc * kKW) {
-                            const int kw = gt.u0w + e;
-                            for (int c = 0; c < p.bw; ++c) {
-                                const int sw = na_window_start(imin(gt.w0 + c, p.W - 1), p.W, p.kw);
-                                if (unsigned(kw - sw) >= unsigned(p.ew)) m |= 1u << (p.bh + c);
-                            }
-                        }
-                        (axis == 0 ? tab_h : tab_w)[e] = uint16_t(m);
-                    }
-                    ptx::mbar_arrive(&bars->tab_done[t]);
-                    if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_done[t], rbs & 1, p.err, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
-                    const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
-                    const int nvt = gt.nhc * gt.nwc;
-                    for (int i = row; i < nvt * kBN * 2; i += 128) {
-                        const int half = i & 1, r = (i >> 1) % kBN, v = (i >> 1) / kBN;
-                        // key r of sub-box v: union h row (v / nwc) KH + (r / 16) % KH,
-                        // w column (v % nwc) 16 + r % 16 (the same in each of its KT frames)
-                        const int hc = v / gt.nwc, wc = v - hc * gt.nwc;
-                        const uint32_t m = uint32_t(tab_h[hc * KH + (r / kKW) % KH]) |
-                                           uint32_t(tab_w[wc * kKW + r % kKW]);
-                        const uint32_t bits = (m >> (half * 8)) & 0xffu;
-                        uint32_t w[4];
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
-                                    (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
-                        *reinterpret_cast<uint4 *>(smem + C::kxv_off(t, v) + ptx::sw32_offset(r, half)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                    ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&bars->chan_ready[t]);
-                    ptx::mbar_arrive(&bars->tab_free[t]);
-                    ++rbs;
-                }
-            }
 
             // query of this row and its window
             const int qt = gt.t0 + dt, qh = gt.h0 + dh, qw = gt.w0 + dw;
@@ -824,6 +831,18 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             }
             if (!ok) break;
 
+            // ---- the next item's channels before this item's outputs: every
+            //      Q K^T of the tile has completed (its last scores are read),
+            //      the rebuild overlaps the last P V, and the issuer can start
+            //      the next item's Q K^T while the outputs are written
+            const int nx = next_item(it + gridDim.x);
+            if constexpr (PEN) {
+                if (nx < p.n_items && !ensure_channels(pick(na_item(p, nx, KT, KH).g, t))) {
+                    ok = false;
+                    break;
+                }
+            }
+
             // ---- epilogue: O / l -> 16-bit -> global.  The issuer overwrites O
             //      with the next item's first P V only after this warpgroup has
             //      written that item's P(0), i.e. after these reads.
@@ -853,6 +872,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 }
             }
             G += nt;
+            it = nx;
         }
     }
 

@@ -74,7 +74,7 @@ constexpr int kNQ = 2;              // query tiles (boxes) per item
 constexpr int kBN = 96;             // keys per key tile: a (KT, KH, 16) sub-box, KT KH = 6
 constexpr int kD = 64;              // head dimension
 constexpr int kKW = 16;             // key sub-box width along w
-constexpr int kMaxPenaltyTiles = 8; // distinct key penalty tiles per query box
+constexpr int kMaxPenaltyTiles = 7; // distinct key penalty tiles per query box
 
 template <bool PEN>
 struct NaCfg {
@@ -84,32 +84,36 @@ struct NaCfg {
     // window channels: 16 16-bit values per row, 32-byte swizzle
     static constexpr int X_ROW = 32;
     static constexpr int MAXV = PEN ? kMaxPenaltyTiles : 0;
-    static constexpr int QX_BYTES = PEN ? kNQ * kBM * X_ROW : 0;
+    // (both boxes of an item have the same shape, so one set of query
+    // channels serves both query tiles)
+    static constexpr int QX_BYTES = PEN ? kBM * X_ROW : 0;
     static constexpr int KX_BYTES = kBN * X_ROW;         // one key penalty tile
     static constexpr int KXV_BYTES = kNQ * MAXV * KX_BYTES;
     // violation tables per query tile: 16-bit channel masks per union h row
-    // and w column; a box has <= 8 (h chunk, w chunk) pairs, so <= 8 chunks of
+    // and w column; a box has <= 7 (h chunk, w chunk) pairs, so <= 7 chunks of
     // <= 6 rows or 16 columns per axis
     static constexpr int TAB = kMaxPenaltyTiles * kKW;
     static constexpr int TAB_BYTES = PEN ? kNQ * 2 * TAB * 2 : 0;
-    static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int NS_ALL =
-        (BUDGET - kNQ * PANEL - QX_BYTES - KXV_BYTES - TAB_BYTES) / STAGE_BYTES;
-    // a K stage is needed a whole key tile before the V stage of the same
-    // tile, so K gets the deeper ring when the stages come out odd
-    static constexpr int KS_RAW = (NS_ALL + 1) / 2;
-    static constexpr int KS = KS_RAW > 4 ? 4 : KS_RAW;
-    static constexpr int VS = NS_ALL - KS_RAW > 4 ? 4 : NS_ALL - KS_RAW;
-    static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
+    static constexpr int BUDGET = 227 * 1024 - 1536;      // all but the barrier block and alignment slack
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_QX = OFF_Q + kNQ * PANEL;
     static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
     static constexpr int OFF_TAB = OFF_KXV + KXV_BYTES;
-    static constexpr int OFF_K = OFF_TAB + TAB_BYTES;
+    static constexpr int OFF_K = (OFF_TAB + TAB_BYTES + 1023) / 1024 * 1024;   // 128-byte swizzle atoms
+    static constexpr int NS_ALL = (BUDGET - OFF_K) / STAGE_BYTES;
+    // V gets the deeper ring: a V stage is refilled only once the P V that
+    // read it has completed, and the issuer runs that P V late (it waits for
+    // P), so the next V tile has less lead than the next K tile, whose stage
+    // is freed by a Q K^T issued two key tiles ahead.  Measured on the large
+    // workload: K 2 / V 4 stages 944.7 us, K 3 / V 3 946.8, K 3 / V 2 (before
+    // the query channels were shared) 966.0, K 2 / V 3 953.1.
+    static constexpr int VS = NS_ALL - 2 > 4 ? 4 : NS_ALL - 2;
+    static constexpr int KS = NS_ALL - VS > 4 ? 4 : NS_ALL - VS;
+    static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
     static constexpr int OFF_V = OFF_K + KS * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_V + VS * STAGE_BYTES;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers + 1024 B alignment slack
-    static_assert(OFF_K % 1024 == 0, "128-byte swizzled stages start on 1024-byte boundaries");
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
     // tensor memory
     static constexpr uint32_t tm_s(int t, int b) { return t * 256 + b * kBN; }
     static constexpr uint32_t tm_o(int t) { return t * 256 + 2 * kBN; }
@@ -330,8 +334,8 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         if constexpr (PEN) {
             // one-hot offset channels of every query row: channel dh, then
             // bh + dw (rows past the box: zero)
-            for (int i = threadIdx.x; i < kNQ * kBM * 2; i += C::NBUILD) {
-                const int t = i / (kBM * 2), r = (i / 2) % kBM, half = i % 2;
+            for (int i = threadIdx.x; i < kBM * 2; i += C::NBUILD) {
+                const int r = i / 2, half = i % 2;
                 uint32_t w[4] = {0u, 0u, 0u, 0u};
                 if (r < rows) {
                     const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
@@ -342,8 +346,8 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                         if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
                     }
                 }
-                *reinterpret_cast<uint4 *>(smem + C::OFF_QX + t * kBM * C::X_ROW +
-                                           ptx::sw32_offset(r, half)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QX + ptx::sw32_offset(r, half)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
         ptx::fence_proxy_async_smem();
@@ -444,7 +448,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             const uint32_t dv0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::v_off(0, tt)), C::KV_BYTES);
             uint32_t dqx = 0, dkx0 = 0;
             if constexpr (PEN) {
-                dqx = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::OFF_QX + tt * kBM * C::X_ROW));
+                dqx = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::OFF_QX));
                 dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(tt, 0)));
             }
             int vq = 0, nv = 1;               // penalty tile of the next Q K^T

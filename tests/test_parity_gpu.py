@@ -389,6 +389,20 @@ def test_tc_na3d_parity(ta, grid, kernel, H):
     assert ta.device_status() == 0
 
 
+def test_tc_na3d_batch_parity(ta):
+    """Batch and heads together index the kernel's (box pair, head) items:
+    B = 3 batches of 5 heads, several items per CTA."""
+    w = WORKLOADS["na3d_21x60x104_k11"].with_(B=3, H=5, grid=(3, 9, 40), kernel=(5, 3, 9),
+                                             N=3 * 9 * 40, seed=7790)
+    x = make_inputs(w)
+    with launched(ta, "tc_na"):
+        o = ta.na3d_fwd(*_dev(x, w), w.grid, w.kernel)
+    ref = oracle.na3d_fwd(*_f64(x, w), w.grid, w.kernel)
+    assert ref.shape[0] == 3
+    assert_close(to_host64(o), ref, "bf16", "tc na3d batch 3")
+    assert ta.device_status() == 0
+
+
 def test_na3d_large_full_size_sampled_rows(ta):
     w = WORKLOADS["na3d_21x60x104_k11"]
     x = make_inputs(w)

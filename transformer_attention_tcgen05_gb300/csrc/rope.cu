@@ -78,19 +78,16 @@ __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p, int heads
     const long long e = blockIdx.x * 256ll + threadIdx.x;
     if (e >= (long long)p.N * groups) return;
     const int t = int(e / groups), g = int(e % groups);
-    float cs[4], sn[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int pr = g * 4 + i;
-        const float ang = float(p.pos[t * 4 + p.axis[pr]]) * p.freq[pr];
-        sincosf(ang, &sn[i], &cs[i]);
-    }
     const int h0 = blockIdx.y * heads_per_cta, h1 = imin(h0 + heads_per_cta, p.BH);
     const T *src[2] = {static_cast<const T *>(p.q), static_cast<const T *>(p.k)};
     T *dst[2] = {static_cast<T *>(p.qr), static_cast<T *>(p.kr)};
     // kBatch heads at a time, every load of the batch issued before the first
-    // store, so 2 * kBatch 16-byte loads per thread are in flight at once
+    // store, so 2 * kBatch 16-byte loads per thread are in flight at once; the
+    // first batch's loads go out before the angles are computed, so the
+    // sincos work overlaps them instead of delaying them
     constexpr int kBatch = 4;
+    float cs[4], sn[4];
+    bool have_angles = false;
     for (int hb = h0; hb < h1; hb += kBatch) {
         Vec8<T> x[2][kBatch];
 #pragma unroll
@@ -100,6 +97,15 @@ __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p, int heads
                 x[0][b].load(src[0] + off);
                 x[1][b].load(src[1] + off);
             }
+        if (!have_angles) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int pr = g * 4 + i;
+                const float ang = float(p.pos[t * 4 + p.axis[pr]]) * p.freq[pr];
+                sincosf(ang, &sn[i], &cs[i]);
+            }
+            have_angles = true;
+        }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b)
             if (hb + b < h1) {

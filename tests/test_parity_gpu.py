@@ -376,7 +376,7 @@ def test_flux_joint_full_size_sampled_rows(ta):
 @pytest.mark.parametrize("grid,kernel,H", [((6, 20, 24), (3, 7, 11), 2), ((9, 16, 16), (11, 11, 11), 1),
                                            ((3, 9, 40), (5, 3, 9), 2), ((1, 4, 4), (3, 7, 7), 2),
                                            ((13, 17, 19), (7, 9, 5), 1),
-                                           # several (box pair, head) items per CTA
+                                           # several (box, head) items per stream
                                            ((3, 9, 40), (5, 3, 9), 48), ((6, 20, 24), (3, 7, 11), 24)])
 def test_tc_na3d_parity(ta, grid, kernel, H):
     w = WORKLOADS["na3d_21x60x104_k11"].with_(grid=grid, kernel=kernel, H=H,
@@ -390,8 +390,8 @@ def test_tc_na3d_parity(ta, grid, kernel, H):
 
 
 def test_tc_na3d_batch_parity(ta):
-    """Batch and heads together index the kernel's (box pair, head) items:
-    B = 3 batches of 5 heads, several items per CTA."""
+    """Batch and heads together index the kernel's (box, head) items:
+    B = 3 batches of 5 heads, several items per stream."""
     w = WORKLOADS["na3d_21x60x104_k11"].with_(B=3, H=5, grid=(3, 9, 40), kernel=(5, 3, 9),
                                              N=3 * 9 * 40, seed=7790)
     x = make_inputs(w)

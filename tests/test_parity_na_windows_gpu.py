@@ -73,13 +73,16 @@ def _dev(x: np.ndarray, dtype: str):
 
 # (grid, kernel, heads): the pages' two clamp shapes at D = 64, the large
 # workload's grid, and odd/even extents where windows clamp on some axes.  The
-# kernel runs one CTA per SM over (box pair, head) items, so the many-head
-# cases give every CTA several items whose window geometry changes from one
-# to the next ((1, 4, 4) also leaves the second box of every pair empty).
+# kernel runs one CTA per SM with two streams of (box, head) items, so the
+# many-head cases give every stream several boxes whose window geometry
+# changes from one to the next; (1, 4, 4) is one box per head, so one head
+# leaves the second stream without work and seven give the last CTA one box.
 CASES = [
     ((9, 64, 64), (11, 11, 11), 1),
     ((21, 60, 104), (11, 11, 11), 1),
     ((1, 4, 4), (3, 7, 7), 2),
+    ((1, 4, 4), (3, 7, 7), 1),
+    ((1, 4, 4), (3, 7, 7), 7),
     ((4, 6, 33), (5, 7, 9), 1),
     ((2, 5, 16), (3, 5, 17), 1),
     ((7, 8, 9), (7, 9, 11), 2),

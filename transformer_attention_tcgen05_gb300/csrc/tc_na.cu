@@ -4,49 +4,54 @@
 // clamp(i - k/2, 0, n - k_eff) per axis), computed as a fused flash-style
 // kernel whose scores never leave the SM.
 //
-// Work item = two 3D query boxes adjacent in w (<= 128 queries each) of one
-// (batch, head).  One CTA per SM walks items blockIdx.x, + gridDim.x, ...,
-// so the CTAs in flight always hold neighbouring boxes of one head (their key
-// windows overlap in L2), and the set-up that a CTA per item paid every time
-// (barriers, tensor memory, the query-offset channels, the first copies and
-// the first Q K^T) is paid once or hidden behind the previous item: the K and
-// V loaders stream the next item's key tiles as soon as ring stages free up,
-// the next item's queries load once the last Q K^T of the current one has
-// completed, and its first two Q K^T are issued while the softmax warps are
-// still writing out the current item's outputs.
+// Each CTA (one per SM) runs two independent query-tile streams: stream t
+// of CTA c takes the 3D query boxes (<= 128 queries each, w fastest, then h,
+// t, batch x head) 2c + t, 2c + t + 2 grid, ..., so the CTAs in flight hold
+// neighbouring boxes of one head (their key windows overlap in L2), and the
+// set-up that a CTA per box paid every time (barriers, tensor memory, the
+// query-offset channels, the first copies and the first Q K^T) is paid once
+// or hidden behind the previous box: a stream's loader streams the next box's
+// key tiles as soon as its ring stages free up, the next box's queries load
+// once the last Q K^T of the current one has completed, and its first two
+// Q K^T are issued while the softmax warps are still writing out the current
+// box's outputs.  A box change still idles a stream's issuer for the length
+// of the epilogue and the next box's first softmax, so stream 1 starts about
+// half a box late: the two streams change boxes at different times, and
+// while one changes the other has the tensor pipe to itself.
 //
-// Per item and query tile t the keys are the union of the box's clamped
-// windows (a 3D box again, the window start being monotone), streamed as
-// (KT, KH, 16) key sub-boxes of 96 keys by 5D TMA, K and V in rings of their
-// own.  bf16 applies the h and w window tests on the tensor core: every query
-// row carries 16 one-hot channels (its h and w offset inside the box) and
-// every key sub-box 16 matching channels holding -2^100 (at least; see the
-// host) where the key lies outside the window of that offset, so one extra
-// 16-deep MMA step adds -2^100 per violated axis to S and every masked key
-// gets P = 0 exactly whenever the raw scores are below 2^98 in magnitude.  f16
-// cannot hold such a penalty and tests h and w per key in the softmax.  The t
-// window is tested per 16-key group (one frame of the sub-box).
+// Per box the keys are the union of the box's clamped windows (a 3D box
+// again, the window start being monotone), streamed as (KT, KH, 16) key
+// sub-boxes of 96 keys by 5D TMA into each stream's own K and V rings.
+// bf16 applies the h and w window tests on the tensor core: every query row
+// carries 16 one-hot channels (its h and w offset inside the box) and every
+// key sub-box 16 matching channels holding -2^100 (at least; see the host)
+// where the key lies outside the window of that offset, so one extra 16-deep
+// MMA step adds -2^100 per violated axis to S and every masked key gets P = 0
+// exactly whenever the raw scores are below 2^98 in magnitude.  f16 cannot
+// hold such a penalty and tests h and w per key in the softmax.  The t window
+// is tested per 16-key group (one frame of the sub-box).
 //
 // The key-side penalty channels of a box depend only on the box's window
 // geometry relative to its union (chunk counts and where the clamped window
-// starts stop advancing), so a tile rebuilds them only when that changes from
-// its previous item: the interior boxes of a grid all share one set.
+// starts stop advancing), so a stream rebuilds them only when that changes
+// from its previous box: the interior boxes of a grid all share one set.
 //
-// Warps: 0-3 softmax of query tile 0 (thread = query row = TMEM lane), 4-7 of
-// tile 1, 8 MMA issuer of tile 0 and TMEM owner, 9 TMA loader of Q and the K
-// ring, 10 TMA loader of the V ring, 11 MMA issuer of tile 1 (and barrier
-// set-up).  The third warpgroup drops to 72 registers (setmaxnreg) so the
-// softmax warpgroups hold a whole score row in registers (216).
+// Warps: 0-3 softmax of stream 0 (thread = query row = TMEM lane), 4-7 of
+// stream 1, 8 MMA issuer of stream 0 and TMEM owner, 9 and 10 TMA loaders of
+// stream 0 and 1 (Q, K and V in the order the issuer consumes them), 11 MMA
+// issuer of stream 1 (and barrier set-up).  The third warpgroup drops to 72
+// registers (setmaxnreg) so the softmax warpgroups hold a whole score row in
+// registers (216).
 //
-// Tensor memory per query tile t: [S_t,0 | S_t,1 | O_t] (96 + 96 + 64
-// columns) at 256 t.  Key tile g of the tile (counted over all items of the
-// CTA) has its scores in buffer g % 2, and its P is written over them; the
-// issuer of tile t issues P V (g) as soon as the softmax has written P(g) and
-// right behind it Q K^T (g + 2) into the same buffer (one thread's MMAs
-// execute in order), so the next scores are ready when the softmax finishes a
-// key tile.  Every barrier is waited for phase by phase, never skipping one,
-// and each is at most one phase ahead of any waiter (argued per barrier
-// below): a parity wait cannot tell phase k from phase k + 2.
+// Tensor memory per stream t: [S_t,0 | S_t,1 | O_t] (96 + 96 + 64 columns)
+// at 256 t.  Key tile g of the stream (counted over all its boxes) has its
+// scores in buffer g % 2, and its P is written over them; the issuer of
+// stream t issues P V (g) as soon as the softmax has written P(g) and right
+// behind it Q K^T (g + 2) into the same buffer (one thread's MMAs execute in
+// order), so the next scores are ready when the softmax finishes a key tile.
+// Every barrier is waited for phase by phase, never skipping one, and each is
+// at most one phase ahead of any waiter (argued per barrier below): a parity
+// wait cannot tell phase k from phase k + 2.
 //
 // Softmax (base 2): x = s * scale * log2(e); the first key tile sets the
 // running max m, later tiles are exponentiated against m as it stands and a
@@ -70,7 +75,7 @@ namespace attn {
 namespace {
 
 constexpr int kBM = 128;            // query rows per tile (MMA M)
-constexpr int kNQ = 2;              // query tiles (boxes) per item
+constexpr int kNQ = 2;              // query-tile streams per CTA
 constexpr int kBN = 96;             // keys per key tile: a (KT, KH, 16) sub-box, KT KH = 6
 constexpr int kD = 64;              // head dimension
 constexpr int kKW = 16;             // key sub-box width along w
@@ -79,17 +84,17 @@ constexpr int kMaxPenaltyTiles = 7; // distinct key penalty tiles per query box
 template <bool PEN>
 struct NaCfg {
     static constexpr int PANEL = kBM * 128;              // one query tile (64 channels, 128 B rows)
-    static constexpr int KV_BYTES = kBN * 128;           // one K or V tile of one query tile
-    static constexpr int STAGE_BYTES = kNQ * KV_BYTES;   // both query tiles' key tiles
+    static constexpr int KV_BYTES = kBN * 128;           // one K or V tile
+    static constexpr int STAGE_BYTES = kNQ * KV_BYTES;   // stage s of both streams' rings
     // window channels: 16 16-bit values per row, 32-byte swizzle
     static constexpr int X_ROW = 32;
     static constexpr int MAXV = PEN ? kMaxPenaltyTiles : 0;
-    // (both boxes of an item have the same shape, so one set of query
-    // channels serves both query tiles)
+    // (every box has the same shape, so one set of query channels serves
+    // both streams)
     static constexpr int QX_BYTES = PEN ? kBM * X_ROW : 0;
     static constexpr int KX_BYTES = kBN * X_ROW;         // one key penalty tile
     static constexpr int KXV_BYTES = kNQ * MAXV * KX_BYTES;
-    // violation tables per query tile: 16-bit channel masks per union h row
+    // violation tables per stream: 16-bit channel masks per union h row
     // and w column; a box has <= 7 (h chunk, w chunk) pairs, so <= 7 chunks of
     // <= 6 rows or 16 columns per axis
     static constexpr int TAB = kMaxPenaltyTiles * kKW;
@@ -105,8 +110,9 @@ struct NaCfg {
     // read it has completed, and the issuer runs that P V late (it waits for
     // P), so the next V tile has less lead than the next K tile, whose stage
     // is freed by a Q K^T issued two key tiles ahead.  Measured on the large
-    // workload: K 2 / V 4 stages 944.7 us, K 3 / V 3 946.8, K 3 / V 2 (before
-    // the query channels were shared) 966.0, K 2 / V 3 953.1.
+    // workload (with rings shared by both query tiles): K 2 / V 4 stages
+    // 944.7 us, K 3 / V 3 946.8, K 3 / V 2 (before the query channels were
+    // shared) 966.0, K 2 / V 3 953.1.
     static constexpr int VS = NS_ALL - 2 > 4 ? 4 : NS_ALL - 2;
     static constexpr int KS = NS_ALL - VS > 4 ? 4 : NS_ALL - VS;
     static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
@@ -121,10 +127,10 @@ struct NaCfg {
     static_assert(tm_o(kNQ - 1) + kD <= TM_COLS, "tensor-memory layout must fit 512 columns");
     // warps
     static constexpr int NSOFT = 4 * kNQ;
-    static constexpr int W_MMA = NSOFT;       // issuer of tile 0, TMEM owner
-    static constexpr int W_LOAD = NSOFT + 1;  // Q and K copies
-    static constexpr int W_LOADV = NSOFT + 2; // V copies
-    static constexpr int W_MMA1 = NSOFT + 3;  // issuer of tile 1, barrier set-up
+    static constexpr int W_MMA = NSOFT;       // issuer of stream 0, TMEM owner
+    static constexpr int W_LOAD = NSOFT + 1;  // Q, K and V copies of stream 0
+    static constexpr int W_LOAD1 = NSOFT + 2; // Q, K and V copies of stream 1
+    static constexpr int W_MMA1 = NSOFT + 3;  // issuer of stream 1, barrier set-up
     static constexpr int NT = (NSOFT + 4) * 32;
     static constexpr int NBUILD = NT - 32;    // threads that build the query channels
     // register split: launch 168 x 384 = 64512 = 2 x 128 x 216 + 128 x 72
@@ -147,30 +153,33 @@ struct NaParams {
     int kt, kh, kw;          // requested kernel
     int et, eh, ew;          // effective kernel (min(k, extent))
     int bt, bh, bw;          // query box
-    int nbt, nbh, nbw, nbw2; // boxes along t, h, w; box pairs along w
+    int nbt, nbh, nbw;       // boxes along t, h, w
     int KT, KH;              // key sub-box frames and rows (KT KH 16 = 96 keys)
-    int n_items;             // box pairs x (batch x heads)
+    int n_boxes;             // boxes x (batch x heads)
+    int stagger;             // stream 1 starts once stream 0 has issued this many P V
 };
 
-// Barrier block at OFF_BAR.  Phases (k counts from 0):
-//   q_full   k: the queries of the CTA's item k have landed
-//   q_free   k: every Q K^T of item k has completed (one commit per issuer)
-//   k_full / v_full [s]: the K / V tile of CTA key step s + KS n has landed
-//   k_empty / v_empty [s]: both issuers are done with that stage
-//   s_full [2 t + b]: Q K^T of tile t's key tile g (g % 2 = b) has completed
+// Barrier block at OFF_BAR.  Phases (k counts from 0) of stream t's barriers:
+//   q_full [t] k: the queries of the stream's box k have landed
+//   q_free [t] k: every Q K^T of box k has completed
+//   k_full / v_full [t][s]: the stream's K / V tile s + KS n (s + VS n) has landed
+//   k_empty / v_empty [t][s]: the issuer is done with that stage
+//   s_full [2 t + b]: Q K^T of the stream's key tile g (g % 2 = b) has completed
 //   p_ready[2 t + b]: the softmax has written P(g) there (128 arrivals)
 //   o_done [2 t + b]: P V (g) has completed
-//   chan_ready[t]: tile t's key penalty channels are rebuilt (128 arrivals)
-//   tab_done[t] / tab_free[t]: tile t's violation tables of rebuild k are
+//   chan_ready[t]: the stream's key penalty channels are rebuilt (128 arrivals)
+//   tab_done[t] / tab_free[t]: the stream's violation tables of rebuild k are
 //                  written / no longer read (128 arrivals; bounded waits, so
 //                  a warp that gave up on a timeout cannot strand the others
 //                  the way a named barrier would)
+//   go: stream 1 may start (one phase, one arrival from issuer 0)
 template <int KS, int VS>
 struct NaBars {
-    uint64_t q_full, q_free;
-    uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+    uint64_t q_full[kNQ], q_free[kNQ];
+    uint64_t k_full[kNQ][KS], k_empty[kNQ][KS], v_full[kNQ][VS], v_empty[kNQ][VS];
     uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
     uint64_t chan_ready[kNQ], tab_done[kNQ], tab_free[kNQ];
+    uint64_t go;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -181,7 +190,7 @@ struct NaTile {
     int t0, h0, w0;          // box origin
     int u0t, u0h, u0w;       // union origin
     int ntc, nhc, nwc;       // union chunks along t, h, w (KT frames, KH rows, 16 columns)
-    int ntiles;              // key tiles = ntc nhc nwc (0 for a box past the grid)
+    int ntiles;              // key tiles = ntc nhc nwc
 };
 
 __host__ __device__ __forceinline__ NaTile na_tile(const NaParams &p, int bi_t, int bi_h, int bi_w,
@@ -190,11 +199,6 @@ __host__ __device__ __forceinline__ NaTile na_tile(const NaParams &p, int bi_t, 
     g.t0 = bi_t * p.bt;
     g.h0 = bi_h * p.bh;
     g.w0 = bi_w * p.bw;
-    if (bi_w >= p.nbw) {
-        g.ntiles = 0;
-        g.u0t = g.u0h = g.u0w = g.ntc = g.nhc = g.nwc = 0;
-        return g;
-    }
     const int t1 = imin(g.t0 + p.bt, p.T) - 1, h1 = imin(g.h0 + p.bh, p.Hg) - 1,
               w1 = imin(g.w0 + p.bw, p.W) - 1;
     g.u0t = na_window_start(g.t0, p.T, p.kt);
@@ -210,28 +214,19 @@ __host__ __device__ __forceinline__ NaTile na_tile(const NaParams &p, int bi_t, 
     return g;
 }
 
-// Work item it: (batch x head) it / pairs, box pair it % pairs (w pairs
-// fastest, then h, then t) -- the order of the old one-CTA-per-item grid.
-struct NaItem {
-    NaTile g[kNQ];
-    int n[kNQ];              // key tiles of each query tile
-    int steps;               // key-tile steps of the item (the larger n)
+// Box b: (batch x head) b / boxes, then box t, h, w (w fastest).
+struct NaBox {
+    NaTile g;
     int bhd;                 // batch x head
 };
 
-__device__ __forceinline__ NaItem na_item(const NaParams &p, int it, int KT, int KH) {
-    NaItem I;
-    const int pairs = p.nbt * p.nbh * p.nbw2;
-    I.bhd = it / pairs;
-    const int pr = it - I.bhd * pairs;
-    const int bi_t = pr / (p.nbh * p.nbw2), bi_h = (pr / p.nbw2) % p.nbh, bi_w2 = pr % p.nbw2;
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) {
-        I.g[t] = na_tile(p, bi_t, bi_h, 2 * bi_w2 + t, KT, KH);
-        I.n[t] = I.g[t].ntiles;
-    }
-    I.steps = imax(I.n[0], I.n[1]);
-    return I;
+__device__ __forceinline__ NaBox na_box(const NaParams &p, int b, int KT, int KH) {
+    NaBox x;
+    const int per = p.nbt * p.nbh * p.nbw;
+    x.bhd = b / per;
+    const int r = b - x.bhd * per;
+    x.g = na_tile(p, r / (p.nbh * p.nbw), (r / p.nbw) % p.nbh, r % p.nbw, KT, KH);
+    return x;
 }
 
 // Exact signature of a box's key penalty channels: they depend only on the
@@ -254,17 +249,6 @@ __device__ __forceinline__ unsigned long long na_sig(const NaParams &p, const Na
     }
     return (static_cast<unsigned long long>(g.nhc) << 48) | (static_cast<unsigned long long>(g.nwc) << 40) |
            (static_cast<unsigned long long>(ih) << 20) | iw;
-}
-
-// a[t] for a per-tile array and a run-time t, by selects (indexing the array
-// with a run-time value would place it in local memory)
-template <typename T>
-__device__ __forceinline__ T pick(const T (&a)[kNQ], int t) {
-    T r = a[0];
-#pragma unroll
-    for (int i = 1; i < kNQ; ++i)
-        if (t == i) r = a[i];
-    return r;
 }
 
 // Origin (t, h, w) of key sub-box j of a tile: w chunk fastest, then h, then t.
@@ -301,15 +285,17 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
     // ---- set-up: barriers (one thread of the last warp) beside the query
     //      channels, which are the same for every box
     if (threadIdx.x == C::NT - 32) {
-        ptx::mbar_init(&bars->q_full, 1);
-        ptx::mbar_init(&bars->q_free, kNQ);
-        for (int s = 0; s < C::KS; ++s) {
-            ptx::mbar_init(&bars->k_full[s], 1);
-            ptx::mbar_init(&bars->k_empty[s], kNQ);
-        }
-        for (int s = 0; s < C::VS; ++s) {
-            ptx::mbar_init(&bars->v_full[s], 1);
-            ptx::mbar_init(&bars->v_empty[s], kNQ);
+        for (int t = 0; t < kNQ; ++t) {
+            ptx::mbar_init(&bars->q_full[t], 1);
+            ptx::mbar_init(&bars->q_free[t], 1);
+            for (int s = 0; s < C::KS; ++s) {
+                ptx::mbar_init(&bars->k_full[t][s], 1);
+                ptx::mbar_init(&bars->k_empty[t][s], 1);
+            }
+            for (int s = 0; s < C::VS; ++s) {
+                ptx::mbar_init(&bars->v_full[t][s], 1);
+                ptx::mbar_init(&bars->v_empty[t][s], 1);
+            }
         }
         for (int b = 0; b < 2 * kNQ; ++b) {
             ptx::mbar_init(&bars->s_full[b], 1);
@@ -321,6 +307,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             ptx::mbar_init(&bars->tab_done[t], 128);
             ptx::mbar_init(&bars->tab_free[t], 128);
         }
+        ptx::mbar_init(&bars->go, 1);
         ptx::mbar_init(&bars->drain, kNQ);
         bars->abort = 0;
         ptx::fence_barrier_init();
@@ -363,80 +350,78 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 
     if (warp >= C::NSOFT) {
         ptx::regs_decrease<C::REGS_OTHER>();
-        if ((warp == C::W_LOAD || warp == C::W_LOADV) && lane == 0) {
-            // ============================================= TMA loaders: the K
-            // (and Q) and V rings run on across items; stage s of CTA key step
-            // g = (steps of earlier items) + j is g % depth
-            const int which = warp == C::W_LOAD ? 0 : 1;
-            const CUtensorMap *tm = which == 0 ? &tk : &tv;
-            uint64_t *full = which == 0 ? bars->k_full : bars->v_full;
-            uint64_t *empty = which == 0 ? bars->k_empty : bars->v_empty;
-            const int NS = which == 0 ? C::KS : C::VS;
-            ptx::prefetch_tmap(tm);
-            if (which == 0) ptx::prefetch_tmap(&tq);
+        if ((warp == C::W_LOAD || warp == C::W_LOAD1) && lane == 0) {
+            // ============================================= TMA loaders, one
+            // per stream: the box's queries, then K and V of each key tile in
+            // the order the issuer consumes them.  The rings run on across
+            // boxes: key tile g of the stream (counted over its boxes) goes to
+            // K stage g % KS and V stage g % VS.
+            const int tt = warp == C::W_LOAD ? 0 : 1;
+            ptx::prefetch_tmap(&tq);
+            ptx::prefetch_tmap(&tk);
+            ptx::prefetch_tmap(&tv);
             const uint64_t pol_kv = ptx::l2_policy_evict_last();
             const uint64_t pol_q = ptx::l2_policy_evict_first();
-            int g0 = 0;                       // CTA key steps of earlier items
-            int issued = 0;                   // key steps whose copies were issued
+            int G = 0;                        // key tiles of earlier boxes
+            int k_issued = 0, v_issued = 0;   // key tiles whose K / V copies were issued
             int q_issued = 0;                 // query loads issued
             bool ok = true;
             int ci = 0;
-            for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++ci) {
-                const NaItem I = na_item(p, it, KT, KH);
-                if (which == 0) {
-                    // the queries of item ci overwrite those of item ci - 1 once
-                    // every Q K^T that read them has completed.  q_free is one
-                    // phase per item, and its phase ci needs the queries loaded
-                    // here, so it is never two phases ahead of this wait.
-                    if (ci > 0 && !ptx::mbar_wait_or_abort(&bars->q_free, (ci - 1) & 1, p.err, abort)) {
+            for (int b = 2 * blockIdx.x + tt; ok && b < p.n_boxes; b += 2 * gridDim.x, ++ci) {
+                const NaBox x = na_box(p, b, KT, KH);
+                // the queries of box ci overwrite those of box ci - 1 once every
+                // Q K^T that read them has completed.  q_free is one phase per
+                // box, and its phase ci needs the queries loaded here, so it is
+                // never two phases ahead of this wait.
+                if (ci > 0 && !ptx::mbar_wait_or_abort(&bars->q_free[tt], (ci - 1) & 1, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(&bars->q_full[tt], rows * 128);
+                ptx::tma_load_5d(smem + C::OFF_Q + tt * C::PANEL, &tq, 0, x.g.w0, x.g.h0, x.g.t0, x.bhd,
+                                 &bars->q_full[tt], pol_q);
+                q_issued = ci + 1;
+                for (int j = 0; j < x.g.ntiles; ++j) {
+                    const int g = G + j;
+                    int kt_, kh_, kw_;
+                    na_key_box(x.g, KT, KH, j, kt_, kh_, kw_);
+                    // a stage phase needs the fill issued here, so the empty
+                    // barrier is never two phases ahead of these waits
+                    const int sk = g % C::KS;
+                    if (g >= C::KS &&
+                        !ptx::mbar_wait_or_abort(&bars->k_empty[tt][sk], ((g / C::KS) - 1) & 1, p.err, abort)) {
                         ok = false;
                         break;
                     }
-                    uint32_t qbytes = 0;
-#pragma unroll
-                    for (int t = 0; t < kNQ; ++t)
-                        if (I.n[t] > 0) qbytes += rows * 128;
-                    ptx::mbar_arrive_expect_tx(&bars->q_full, qbytes);
-#pragma unroll
-                    for (int t = 0; t < kNQ; ++t)
-                        if (I.n[t] > 0)
-                            ptx::tma_load_5d(smem + C::OFF_Q + t * C::PANEL, &tq, 0, I.g[t].w0, I.g[t].h0,
-                                             I.g[t].t0, I.bhd, &bars->q_full, pol_q);
-                    q_issued = ci + 1;
-                }
-                for (int j = 0; j < I.steps; ++j) {
-                    const int gs = g0 + j, s = gs % NS;
-                    if (gs >= NS && !ptx::mbar_wait_or_abort(&empty[s], ((gs / NS) - 1) & 1, p.err, abort)) {
+                    ptx::mbar_arrive_expect_tx(&bars->k_full[tt][sk], C::KV_BYTES);
+                    ptx::tma_load_5d(smem + C::k_off(sk, tt), &tk, 0, kw_, kh_, kt_, x.bhd, &bars->k_full[tt][sk],
+                                     pol_kv);
+                    k_issued = g + 1;
+                    const int sv = g % C::VS;
+                    if (g >= C::VS &&
+                        !ptx::mbar_wait_or_abort(&bars->v_empty[tt][sv], ((g / C::VS) - 1) & 1, p.err, abort)) {
                         ok = false;
                         break;
                     }
-                    issued = gs + 1;
-                    uint32_t bytes = 0;
-#pragma unroll
-                    for (int u = 0; u < kNQ; ++u)
-                        if (j < I.n[u]) bytes += kBN * 128;
-                    ptx::mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-                    for (int u = 0; u < kNQ; ++u) {
-                        if (j >= I.n[u]) continue;
-                        int kt_, kh_, kw_;
-                        na_key_box(I.g[u], KT, KH, j, kt_, kh_, kw_);
-                        ptx::tma_load_5d(smem + (which == 0 ? C::k_off(s, u) : C::v_off(s, u)), tm, 0, kw_,
-                                         kh_, kt_, I.bhd, &full[s], pol_kv);
-                    }
+                    ptx::mbar_arrive_expect_tx(&bars->v_full[tt][sv], C::KV_BYTES);
+                    ptx::tma_load_5d(smem + C::v_off(sv, tt), &tv, 0, kw_, kh_, kt_, x.bhd, &bars->v_full[tt][sv],
+                                     pol_kv);
+                    v_issued = g + 1;
                 }
-                g0 += I.steps;
+                G += x.g.ntiles;
             }
             // after a timeout elsewhere: let the copies this thread issued land
             // (bounded) before the CTA's shared memory is released
             if (*abort) {
-                if (which == 0 && q_issued > 0) ptx::mbar_wait(&bars->q_full, (q_issued - 1) & 1, nullptr);
-                for (int gs = imax(0, issued - NS); gs < issued; ++gs)
-                    ptx::mbar_wait(&full[gs % NS], (gs / NS) & 1, nullptr);
+                if (q_issued > 0) ptx::mbar_wait(&bars->q_full[tt], (q_issued - 1) & 1, nullptr);
+                for (int g = imax(0, k_issued - C::KS); g < k_issued; ++g)
+                    ptx::mbar_wait(&bars->k_full[tt][g % C::KS], (g / C::KS) & 1, nullptr);
+                for (int g = imax(0, v_issued - C::VS); g < v_issued; ++g)
+                    ptx::mbar_wait(&bars->v_full[tt][g % C::VS], (g / C::VS) & 1, nullptr);
             }
         } else if ((warp == C::W_MMA || warp == C::W_MMA1) && lane == 0) {
             // ============================================= MMA issuers: one
-            // thread per query tile (warps of different SM sub-partitions)
+            // thread per stream (warps of different SM sub-partitions)
             const int tt = warp == C::W_MMA ? 0 : 1;
             const uint32_t id_qk = ptx::idesc_16_f32(kBM, kBN, false, F16);
             const uint32_t id_pv = ptx::idesc_16_f32(kBM, kD, true, F16);
@@ -452,9 +437,9 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(tt, 0)));
             }
             int vq = 0, nv = 1;               // penalty tile of the next Q K^T
-            // S(g) of key tile j (CTA step gs) into buffer g % 2
-            auto issue_qk = [&](int g, int gs) {
-                const uint32_t b0 = dk0 + uint32_t(((gs % C::KS) * C::STAGE_BYTES) >> 4);
+            // S(g) of the stream's key tile g into buffer g % 2
+            auto issue_qk = [&](int g) {
+                const uint32_t b0 = dk0 + uint32_t(((g % C::KS) * C::STAGE_BYTES) >> 4);
                 const uint32_t d = tmem + C::tm_s(tt, g & 1);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
@@ -469,9 +454,9 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 }
                 ptx::tc_commit(&bars->s_full[2 * tt + (g & 1)]);
             };
-            // O (+)= P(g) V of CTA step gs; the first key tile of an item overwrites O
-            auto issue_pv = [&](int g, int gs, bool first) {
-                const uint32_t b0 = dv0 + uint32_t(((gs % C::VS) * C::STAGE_BYTES) >> 4);
+            // O (+)= P(g) V(g); the first key tile of a box overwrites O
+            auto issue_pv = [&](int g, bool first) {
+                const uint32_t b0 = dv0 + uint32_t(((g % C::VS) * C::STAGE_BYTES) >> 4);
                 const uint32_t a0 = tmem + C::tm_s(tt, g & 1);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
@@ -481,80 +466,66 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 ptx::tc_commit(&bars->o_done[2 * tt + (g & 1)]);
             };
             bool ok = true;
-            int G = 0;                        // key tiles of this tile in earlier items
-            int g0 = 0;                       // CTA key steps of earlier items
+            int G = 0;                        // key tiles of the stream's earlier boxes
             int rb = 0;                       // channel rebuilds waited for
             unsigned long long last_sig = ~0ull;
+            // stream 1 starts once issuer 0 has issued p.stagger P V (or run out
+            // of boxes): one arrival, one phase, waited for once
+            bool go_sent = tt != 0;
+            auto send_go = [&]() {
+                if (!go_sent) ptx::mbar_arrive(&bars->go);
+                go_sent = true;
+            };
+            if (p.stagger <= 0) send_go();
+            if (tt != 0) ok = ptx::mbar_wait_or_abort(&bars->go, 0, p.err, abort);
             int ci = 0;
-            for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++ci) {
-                const NaItem I = na_item(p, it, KT, KH);
-                const int nt = pick(I.n, tt), steps = I.steps;
-                // every phase of q_full is waited for (even by a tile without
-                // work in this item), so no wait can fall two phases behind
-                ok = ptx::mbar_wait_or_abort(&bars->q_full, ci & 1, p.err, abort);
+            for (int b = 2 * blockIdx.x + tt; ok && b < p.n_boxes; b += 2 * gridDim.x, ++ci) {
+                const NaBox x = na_box(p, b, KT, KH);
+                const int nt = x.g.ntiles;
+                ok = ptx::mbar_wait_or_abort(&bars->q_full[tt], ci & 1, p.err, abort);
                 if (!ok) break;
                 if constexpr (PEN) {
-                    if (nt > 0) {
-                        const NaTile gt = pick(I.g, tt);
-                        const unsigned long long sig = na_sig(p, gt);
-                        if (sig != last_sig) {
-                            // the softmax of this tile rebuilds the channels
-                            // after it has read every earlier S of the tile
-                            ok = ptx::mbar_wait_or_abort(&bars->chan_ready[tt], rb & 1, p.err, abort);
-                            ++rb;
-                            last_sig = sig;
-                            if (!ok) break;
-                        }
-                        nv = imax(1, gt.nhc * gt.nwc);
+                    const unsigned long long sig = na_sig(p, x.g);
+                    if (sig != last_sig) {
+                        // the softmax of this stream rebuilds the channels after
+                        // it has read every earlier S of the stream
+                        ok = ptx::mbar_wait_or_abort(&bars->chan_ready[tt], rb & 1, p.err, abort);
+                        ++rb;
+                        last_sig = sig;
+                        if (!ok) break;
                     }
+                    nv = imax(1, x.g.nhc * x.g.nwc);
                     vq = 0;
                 }
-                // q_free: one commit per issuer and item, right after the last
-                // Q K^T of the tile (at once for a tile without work)
-                bool q_done = false;
-                auto release_q = [&]() {
-                    if (!q_done) ptx::tc_commit(&bars->q_free);
-                    q_done = true;
-                };
-                if (nt == 0) release_q();
                 ptx::tc_fence_after();
-                // Each stage is released once per issuer and use; a stage this
-                // tile does not read is released only once it has been filled,
-                // so that an issuer running ahead never completes a stage phase
-                // in place of the other one.
-                auto next_qk = [&](int j) {          // Q K^T of key tile j (CTA step g0 + j)
-                    const int gs = g0 + j;
-                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[gs % C::KS], (gs / C::KS) & 1, p.err, abort);
+                // Q K^T of key tile j; q_free right behind the box's last one
+                auto next_qk = [&](int j) {
+                    const int g = G + j;
+                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[tt][g % C::KS], (g / C::KS) & 1, p.err, abort);
                     if (!ok) return;
-                    if (j < nt) {
-                        ptx::tc_fence_after();
-                        issue_qk(G + j, gs);
-                        if (j == nt - 1) release_q();
-                    }
-                    ptx::tc_commit(&bars->k_empty[gs % C::KS]);
+                    ptx::tc_fence_after();
+                    issue_qk(g);
+                    if (j == nt - 1) ptx::tc_commit(&bars->q_free[tt]);
+                    ptx::tc_commit(&bars->k_empty[tt][g % C::KS]);
                 };
-                for (int j = 0; ok && j < 2 && j < steps; ++j) next_qk(j);
-                for (int j = 0; ok && j < steps; ++j) {
-                    const int gs = g0 + j;
+                for (int j = 0; ok && j < 2 && j < nt; ++j) next_qk(j);
+                for (int j = 0; ok && j < nt; ++j) {
+                    const int g = G + j;
                     // P V (j) once the softmax has written P(j) and V(j) has landed
-                    if (j < nt)
-                        ok = ptx::mbar_wait_or_abort(&bars->p_ready[2 * tt + ((G + j) & 1)], ((G + j) >> 1) & 1,
-                                                     p.err, abort);
-                    ok = ok && ptx::mbar_wait_or_abort(&bars->v_full[gs % C::VS], (gs / C::VS) & 1, p.err, abort);
+                    ok = ptx::mbar_wait_or_abort(&bars->p_ready[2 * tt + (g & 1)], (g >> 1) & 1, p.err, abort) &&
+                         ptx::mbar_wait_or_abort(&bars->v_full[tt][g % C::VS], (g / C::VS) & 1, p.err, abort);
                     if (!ok) break;
-                    if (j < nt) {
-                        ptx::tc_fence_after();
-                        issue_pv(G + j, gs, j == 0);
-                    }
+                    ptx::tc_fence_after();
+                    issue_pv(g, j == 0);
                     // then Q K^T (j + 2) into the buffer P(j) came from
-                    if (j + 2 < steps) next_qk(j + 2);
+                    if (j + 2 < nt) next_qk(j + 2);
                     if (!ok) break;
-                    ptx::tc_commit(&bars->v_empty[gs % C::VS]);
+                    ptx::tc_commit(&bars->v_empty[tt][g % C::VS]);
+                    if (g + 1 >= p.stagger) send_go();
                 }
-                if (ok) release_q();
                 G += nt;
-                g0 += steps;
             }
+            send_go();
             // drain: every MMA of both issuers has completed before TMEM is freed
             ptx::tc_commit(&bars->drain);
             ptx::mbar_wait(&bars->drain, 0, p.err);
@@ -562,7 +533,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
     } else {
         // ================================================= softmax warpgroups
         ptx::regs_increase<C::REGS_SOFTMAX>();
-        const int t = warp >> 2;                 // query tile
+        const int t = warp >> 2;                 // stream
         const int quarter = warp & 3;            // TMEM lanes [32 quarter, 32 quarter + 32)
         const int row = quarter * 32 + lane;     // query row within the box
         const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
@@ -585,7 +556,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         };
 
         bool ok = true;
-        int G = 0;                               // key tiles of this tile in earlier items
+        int G = 0;                               // key tiles of the stream's earlier boxes
         unsigned long long last_sig = ~0ull;
         int rbs = 0;                             // channel rebuilds done by this warpgroup
         // The key penalty channels of box gx, rebuilt unless they are the ones
@@ -652,21 +623,14 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             ++rbs;
             return true;
         };
-        // this tile's next item with work (the second box of a pair past the
-        // grid's w extent has none)
-        auto next_item = [&](int from) -> int {
-            for (int i = from; i < p.n_items; i += gridDim.x)
-                if (pick(na_item(p, i, KT, KH).n, t) > 0) return i;
-            return p.n_items;
-        };
-        int it = next_item(blockIdx.x);
+        int b = 2 * blockIdx.x + t;              // the stream's boxes: b, b + 2 grid, ...
         if constexpr (PEN) {
-            if (it < p.n_items && !ensure_channels(pick(na_item(p, it, KT, KH).g, t))) ok = false;
+            if (b < p.n_boxes && !ensure_channels(na_box(p, b, KT, KH).g)) ok = false;
         }
-        while (ok && it < p.n_items) {
-            const NaItem I = na_item(p, it, KT, KH);
-            const int nt = pick(I.n, t);
-            const NaTile gt = pick(I.g, t);
+        while (ok && b < p.n_boxes) {
+            const NaBox x = na_box(p, b, KT, KH);
+            const int nt = x.g.ntiles;
+            const NaTile &gt = x.g;
 
             // query of this row and its window
             const int qt = gt.t0 + dt, qh = gt.h0 + dh, qw = gt.w0 + dw;
@@ -835,21 +799,21 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             }
             if (!ok) break;
 
-            // ---- the next item's channels before this item's outputs: every
-            //      Q K^T of the tile has completed (its last scores are read),
-            //      the rebuild overlaps the last P V, and the issuer can start
-            //      the next item's Q K^T while the outputs are written
-            const int nx = next_item(it + gridDim.x);
+            // ---- the next box's channels before this box's outputs: every
+            //      Q K^T of the stream has completed (its last scores are
+            //      read), the rebuild overlaps the last P V, and the issuer can
+            //      start the next box's Q K^T while the outputs are written
+            const int nb = b + 2 * gridDim.x;
             if constexpr (PEN) {
-                if (nx < p.n_items && !ensure_channels(pick(na_item(p, nx, KT, KH).g, t))) {
+                if (nb < p.n_boxes && !ensure_channels(na_box(p, nb, KT, KH).g)) {
                     ok = false;
                     break;
                 }
             }
 
             // ---- epilogue: O / l -> 16-bit -> global.  The issuer overwrites O
-            //      with the next item's first P V only after this warpgroup has
-            //      written that item's P(0), i.e. after these reads.
+            //      with the next box's first P V only after this warpgroup has
+            //      written that box's P(0), i.e. after these reads.
             if (!wait_pv(G + nt - 1)) {
                 ok = false;
                 break;
@@ -858,7 +822,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             typename H16<F16>::T *orow = nullptr;
             if (qvalid)
                 orow = static_cast<typename H16<F16>::T *>(p.o) +
-                       ((size_t(I.bhd) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw) * kD;
+                       ((size_t(x.bhd) * (size_t(p.T) * p.Hg * p.W)) + (size_t(qt) * p.Hg + qh) * p.W + qw) * kD;
 #pragma unroll
             for (int c = 0; c < kD / 32; ++c) {
                 uint32_t ov[32];
@@ -876,7 +840,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 }
             }
             G += nt;
-            it = nx;
+            b = nb;
         }
     }
 
@@ -894,7 +858,8 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 // Query box and key sub-box: at most 128 queries per box and key tiles of KT
 // frames x KH rows x 16 columns (KT KH = 6, 96 keys), minimising the key tiles
 // -- i.e. the (query row, key) slots the MMAs compute -- over all boxes.
-bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KT, int &KH) {
+bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw, int &KT, int &KH,
+             double &tiles) {
     const int ext[3] = {T, Hg, W};
     constexpr int kShapes[4][2] = {{1, 6}, {2, 3}, {3, 2}, {6, 1}};
     double best = -1;
@@ -923,13 +888,11 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
                         }
                         axis[a] = acc;
                     }
-                    const int nbw = cdiv(W, cbw);
-                    // odd box count along w leaves one query tile idle per (t, h) box row
-                    const double w_pairs_waste = (nbw & 1) ? double(nbw + 1) / nbw : 1.0;
-                    const double cost = axis[0] * axis[1] * axis[2] * w_pairs_waste;
+                    const double cost = axis[0] * axis[1] * axis[2];
                     if (best < 0 || cost < best) {
                         best = cost;
                         bt = cbt; bh = cbh; bw = cbw; KT = ckt; KH = ckh;
+                        tiles = cost;
                     }
                 }
             }
@@ -939,6 +902,7 @@ bool plan_na(int T, int Hg, int W, const int kern[3], int &bt, int &bh, int &bw,
 // Plans are cached per (grid, kernel): the search is a few thousand candidates.
 struct NaPlan {
     int bt, bh, bw, KT, KH;
+    double tiles;            // key tiles of all boxes of one (batch, head)
     bool ok;
 };
 
@@ -958,7 +922,7 @@ NaPlan cached_plan(int T, int Hg, int W, const int kern[3]) {
         if (same) return cache[i].plan;
     }
     NaPlan pl{};
-    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KT, pl.KH);
+    pl.ok = plan_na(T, Hg, W, kern, pl.bt, pl.bh, pl.bw, pl.KT, pl.KH, pl.tiles);
     Entry &e = cache[used < 64 ? used++ : 63];
     for (int a = 0; a < 6; ++a) e.key[a] = key[a];
     e.plan = pl;
@@ -985,9 +949,9 @@ attn_status_t launch_na(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
         regs = fa.numRegs;
     }
     if (regs != C::REGS_LAUNCH) return ATTN_ERR_UNSUPPORTED;
-    // one CTA per SM (the shared memory allows no second), each walking items
-    // blockIdx.x, blockIdx.x + gridDim.x, ...
-    const int grid = imin(p.n_items, imax(1, c.sm_count));
+    // one CTA per SM (the shared memory allows no second), each running two
+    // streams of boxes
+    const int grid = imin(cdiv(p.n_boxes, kNQ), imax(1, c.sm_count));
     kern<<<grid, C::NT, C::SMEM, c.stream>>>(tq, tk, tv, p);
     return launch_status(kFamTcNa);
 }
@@ -1033,10 +997,11 @@ attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *
     p.nbt = cdiv(T, p.bt);
     p.nbh = cdiv(Hg, p.bh);
     p.nbw = cdiv(W, p.bw);
-    p.nbw2 = cdiv(p.nbw, 2);
-    const long long items = (long long)p.nbt * p.nbh * p.nbw2 * B * H;
-    if (items > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    p.n_items = int(items);
+    const long long boxes = (long long)p.nbt * p.nbh * p.nbw * B * H;
+    if (boxes > 0x7fffffffLL - 4096) return ATTN_ERR_UNSUPPORTED;   // box indices + 2 grid fit int
+    p.n_boxes = int(boxes);
+    // stream 1 starts half a mean box (in key tiles) behind stream 0
+    p.stagger = int(0.5 * pl.tiles / (double(p.nbt) * p.nbh * p.nbw) + 0.5);
     // the planner's key sub-box shapes have compile-time kernels (bf16)
     if (f16) return launch_na<0, true>(c, tq, tk, tv, p);
     switch (p.KT * 10 + p.KH) {

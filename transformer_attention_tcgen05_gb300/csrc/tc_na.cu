@@ -22,19 +22,19 @@
 // Per box the keys are the union of the box's clamped windows (a 3D box
 // again, the window start being monotone), streamed as (KT, KH, 16) key
 // sub-boxes of 96 keys by 5D TMA into each stream's own K and V rings.
-// bf16 applies the h and w window tests on the tensor core: every query row
-// carries 16 one-hot channels (its h and w offset inside the box) and every
-// key sub-box 16 matching channels holding -2^100 (at least; see the host)
-// where the key lies outside the window of that offset, so one extra 16-deep
-// MMA step adds -2^100 per violated axis to S and every masked key gets P = 0
-// exactly whenever the raw scores are below 2^98 in magnitude.  f16 cannot
-// hold such a penalty and tests h and w per key in the softmax.  The t window
-// is tested per 16-key group (one frame of the sub-box).
-//
-// The key-side penalty channels of a box depend only on the box's window
-// geometry relative to its union (chunk counts and where the clamped window
-// starts stop advancing), so a stream rebuilds them only when that changes
-// from its previous box: the interior boxes of a grid all share one set.
+// bf16 applies the h and w window tests on the tensor core.  Measured from
+// the union's origin, a query's h window is [a, a + eh) and its w window
+// [b, b + ew), with a < bh and b < bw (the clamped window start advances by
+// 0 or 1 per row); every query row carries 16 one-hot channels (channel a and
+// channel bh + b) and every key sub-box 16 channels holding -2^100 (at least;
+// see the host) where the key's union row / column lies outside the window of
+// that offset.  One extra 16-deep MMA step thus adds -2^100 per violated axis
+// to S, and every masked key gets P = 0 exactly whenever the raw scores are
+// below 2^98 in magnitude.  The key side depends only on the sub-box's place
+// in the union, not on the box, so its channel tiles are built once per CTA;
+// a softmax thread writes its own row's query channels for each box.  f16
+// cannot hold such a penalty and tests h and w per key in the softmax.  The t
+// window is tested per 16-key group (one frame of the sub-box).
 //
 // Warps: 0-3 softmax of stream 0 (thread = query row = TMEM lane), 4-7 of
 // stream 1, 8 MMA issuer of stream 0 and TMEM owner, 9 and 10 TMA loaders of
@@ -79,7 +79,7 @@ constexpr int kNQ = 2;              // query-tile streams per CTA
 constexpr int kBN = 96;             // keys per key tile: a (KT, KH, 16) sub-box, KT KH = 6
 constexpr int kD = 64;              // head dimension
 constexpr int kKW = 16;             // key sub-box width along w
-constexpr int kMaxPenaltyTiles = 7; // distinct key penalty tiles per query box
+constexpr int kMaxPenaltyTiles = 7; // key penalty tiles: union h chunks x w chunks
 
 template <bool PEN>
 struct NaCfg {
@@ -89,22 +89,14 @@ struct NaCfg {
     // window channels: 16 16-bit values per row, 32-byte swizzle
     static constexpr int X_ROW = 32;
     static constexpr int MAXV = PEN ? kMaxPenaltyTiles : 0;
-    // (every box has the same shape, so one set of query channels serves
-    // both streams)
-    static constexpr int QX_BYTES = PEN ? kBM * X_ROW : 0;
+    static constexpr int QX_BYTES = PEN ? kNQ * kBM * X_ROW : 0;   // query channels per stream
     static constexpr int KX_BYTES = kBN * X_ROW;         // one key penalty tile
-    static constexpr int KXV_BYTES = kNQ * MAXV * KX_BYTES;
-    // violation tables per stream: 16-bit channel masks per union h row
-    // and w column; a box has <= 7 (h chunk, w chunk) pairs, so <= 7 chunks of
-    // <= 6 rows or 16 columns per axis
-    static constexpr int TAB = kMaxPenaltyTiles * kKW;
-    static constexpr int TAB_BYTES = PEN ? kNQ * 2 * TAB * 2 : 0;
+    static constexpr int KXV_BYTES = MAXV * KX_BYTES;    // shared by both streams
     static constexpr int BUDGET = 227 * 1024 - 1536;      // all but the barrier block and alignment slack
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_QX = OFF_Q + kNQ * PANEL;
     static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
-    static constexpr int OFF_TAB = OFF_KXV + KXV_BYTES;
-    static constexpr int OFF_K = (OFF_TAB + TAB_BYTES + 1023) / 1024 * 1024;   // 128-byte swizzle atoms
+    static constexpr int OFF_K = (OFF_KXV + KXV_BYTES + 1023) / 1024 * 1024;   // 128-byte swizzle atoms
     static constexpr int NS_ALL = (BUDGET - OFF_K) / STAGE_BYTES;
     // V gets the deeper ring: a V stage is refilled only once the P V that
     // read it has completed, and the issuer runs that P V late (it waits for
@@ -141,7 +133,8 @@ struct NaCfg {
                   "setmaxnreg split must fit the launch's register file share");
     static constexpr int k_off(int s, int u) { return OFF_K + s * STAGE_BYTES + u * KV_BYTES; }
     static constexpr int v_off(int s, int u) { return OFF_V + s * STAGE_BYTES + u * KV_BYTES; }
-    static constexpr int kxv_off(int u, int v) { return OFF_KXV + (u * MAXV + v) * KX_BYTES; }
+    static constexpr int qx_off(int u) { return OFF_QX + u * kBM * X_ROW; }
+    static constexpr int kxv_off(int v) { return OFF_KXV + v * KX_BYTES; }
 };
 
 struct NaParams {
@@ -155,6 +148,7 @@ struct NaParams {
     int bt, bh, bw;          // query box
     int nbt, nbh, nbw;       // boxes along t, h, w
     int KT, KH;              // key sub-box frames and rows (KT KH 16 = 96 keys)
+    int nhv, nwv;            // most union h / w chunks of a box (penalty tiles nhv nwv)
     int n_boxes;             // boxes x (batch x heads)
     int stagger;             // stream 1 starts once stream 0 has issued this many P V
 };
@@ -167,18 +161,15 @@ struct NaParams {
 //   s_full [2 t + b]: Q K^T of the stream's key tile g (g % 2 = b) has completed
 //   p_ready[2 t + b]: the softmax has written P(g) there (128 arrivals)
 //   o_done [2 t + b]: P V (g) has completed
-//   chan_ready[t]: the stream's key penalty channels are rebuilt (128 arrivals)
-//   tab_done[t] / tab_free[t]: the stream's violation tables of rebuild k are
-//                  written / no longer read (128 arrivals; bounded waits, so
-//                  a warp that gave up on a timeout cannot strand the others
-//                  the way a named barrier would)
+//   chan_ready[t] k: the query channels of the stream's box k are written
+//                  (128 arrivals)
 //   go: stream 1 may start (one phase, one arrival from issuer 0)
 template <int KS, int VS>
 struct NaBars {
     uint64_t q_full[kNQ], q_free[kNQ];
     uint64_t k_full[kNQ][KS], k_empty[kNQ][KS], v_full[kNQ][VS], v_empty[kNQ][VS];
     uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
-    uint64_t chan_ready[kNQ], tab_done[kNQ], tab_free[kNQ];
+    uint64_t chan_ready[kNQ];
     uint64_t go;
     uint64_t drain;
     uint32_t tmem_base;
@@ -227,28 +218,6 @@ __device__ __forceinline__ NaBox na_box(const NaParams &p, int b, int KT, int KH
     const int r = b - x.bhd * per;
     x.g = na_tile(p, r / (p.nbh * p.nbw), (r / p.nbw) % p.nbh, r % p.nbw, KT, KH);
     return x;
-}
-
-// Exact signature of a box's key penalty channels: they depend only on the
-// union's h and w chunk counts and on the window starts of the box's rows /
-// columns relative to the union origin, which advance by 0 or 1 per row
-// (a bit per row: did it advance).
-__device__ __forceinline__ unsigned long long na_sig(const NaParams &p, const NaTile &g) {
-    uint32_t ih = 0u, iw = 0u;
-    int prev = g.u0h;
-    for (int c = 1; c < p.bh; ++c) {
-        const int s = na_window_start(imin(g.h0 + c, p.Hg - 1), p.Hg, p.kh);
-        if (s != prev) ih |= 1u << c;
-        prev = s;
-    }
-    prev = g.u0w;
-    for (int c = 1; c < p.bw; ++c) {
-        const int s = na_window_start(imin(g.w0 + c, p.W - 1), p.W, p.kw);
-        if (s != prev) iw |= 1u << c;
-        prev = s;
-    }
-    return (static_cast<unsigned long long>(g.nhc) << 48) | (static_cast<unsigned long long>(g.nwc) << 40) |
-           (static_cast<unsigned long long>(ih) << 20) | iw;
 }
 
 // Origin (t, h, w) of key sub-box j of a tile: w chunk fastest, then h, then t.
@@ -302,11 +271,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             ptx::mbar_init(&bars->p_ready[b], 128);
             ptx::mbar_init(&bars->o_done[b], 1);
         }
-        for (int t = 0; t < kNQ; ++t) {
-            ptx::mbar_init(&bars->chan_ready[t], 128);
-            ptx::mbar_init(&bars->tab_done[t], 128);
-            ptx::mbar_init(&bars->tab_free[t], 128);
-        }
+        for (int t = 0; t < kNQ; ++t) ptx::mbar_init(&bars->chan_ready[t], 128);
         ptx::mbar_init(&bars->go, 1);
         ptx::mbar_init(&bars->drain, kNQ);
         bars->abort = 0;
@@ -319,21 +284,31 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 make_uint4(0, 0, 0, 0);
         }
         if constexpr (PEN) {
-            // one-hot offset channels of every query row: channel dh, then
-            // bh + dw (rows past the box: zero)
-            for (int i = threadIdx.x; i < kBM * 2; i += C::NBUILD) {
-                const int r = i / 2, half = i % 2;
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
-                if (r < rows) {
-                    const int dh = (r / p.bw) % p.bh, dw = r % p.bw;
-                    const int ch[2] = {dh, p.bh + dw};
-#pragma unroll
-                    for (int a = 0; a < 2; ++a) {
-                        const int c = ch[a] - half * 8;
-                        if (c >= 0 && c < 8) w[c >> 1] |= uint32_t(H16<F16>::kOne) << ((c & 1) * 16);
-                    }
+            // key penalty tile v = hc nwv + wc (union h chunk hc, w chunk wc):
+            // key r lies on union row hc KH + (r / 16) % KH and column
+            // wc 16 + r % 16 (the same in each of its KT frames); channel
+            // c < bh holds -penalty where that row is outside [c, c + eh),
+            // channel bh + c where the column is outside [c, c + ew)
+            const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
+            const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
+            for (int i = threadIdx.x; i < p.nhv * p.nwv * kBN * 2; i += C::NBUILD) {
+                const int half = i & 1, r = (i >> 1) % kBN, v = (i >> 1) / kBN;
+                const int hc = v / p.nwv, wc = v - hc * p.nwv;
+                const int uh = hc * KH + (r / kKW) % KH, uw = wc * kKW + r % kKW;
+                uint32_t bits = 0u;
+                for (int c = 0; c < 8; ++c) {
+                    const int ch = half * 8 + c;
+                    const bool out = ch < p.bh ? unsigned(uh - ch) >= unsigned(p.eh)
+                                   : ch < p.bh + p.bw ? unsigned(uw - (ch - p.bh)) >= unsigned(p.ew)
+                                                      : false;
+                    if (out) bits |= 1u << c;
                 }
-                *reinterpret_cast<uint4 *>(smem + C::OFF_QX + ptx::sw32_offset(r, half)) =
+                uint32_t w[4];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
+                            (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
+                *reinterpret_cast<uint4 *>(smem + C::kxv_off(v) + ptx::sw32_offset(r, half)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
@@ -433,10 +408,10 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             const uint32_t dv0 = ptx::desc_lo_sw128(ptx::smem_addr(smem + C::v_off(0, tt)), C::KV_BYTES);
             uint32_t dqx = 0, dkx0 = 0;
             if constexpr (PEN) {
-                dqx = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::OFF_QX));
-                dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(tt, 0)));
+                dqx = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::qx_off(tt)));
+                dkx0 = ptx::desc_lo_sw32(ptx::smem_addr(smem + C::kxv_off(0)));
             }
-            int vq = 0, nv = 1;               // penalty tile of the next Q K^T
+            int hq = 0, wq = 0, nhq = 1, nwq = 1;   // union h / w chunk of the next Q K^T (of nhq / nwq)
             // S(g) of the stream's key tile g into buffer g % 2
             auto issue_qk = [&](int g) {
                 const uint32_t b0 = dk0 + uint32_t(((g % C::KS) * C::STAGE_BYTES) >> 4);
@@ -447,9 +422,12 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                                 ptx::desc_join(b0 + uint32_t(kk * 2), HI128), id_qk, kk > 0);
                 if constexpr (PEN) {
                     // + window penalties: one more k-step over the 16 extra
-                    // channels; key tile j uses penalty tile j mod (h x w chunks)
-                    const uint32_t b = dkx0 + uint32_t((vq * C::KX_BYTES) >> 4);
-                    if (++vq == nv) vq = 0;
+                    // channels with the key tile's (h chunk, w chunk) tile
+                    const uint32_t b = dkx0 + uint32_t(((hq * p.nwv + wq) * C::KX_BYTES) >> 4);
+                    if (++wq == nwq) {
+                        wq = 0;
+                        if (++hq == nhq) hq = 0;
+                    }
                     ptx::mma_ss(d, ptx::desc_join(dqx, HI32), ptx::desc_join(b, HI32), id_qk, 1u);
                 }
                 ptx::tc_commit(&bars->s_full[2 * tt + (g & 1)]);
@@ -467,8 +445,6 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             };
             bool ok = true;
             int G = 0;                        // key tiles of the stream's earlier boxes
-            int rb = 0;                       // channel rebuilds waited for
-            unsigned long long last_sig = ~0ull;
             // stream 1 starts once issuer 0 has issued p.stagger P V (or run out
             // of boxes): one arrival, one phase, waited for once
             bool go_sent = tt != 0;
@@ -485,17 +461,13 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 ok = ptx::mbar_wait_or_abort(&bars->q_full[tt], ci & 1, p.err, abort);
                 if (!ok) break;
                 if constexpr (PEN) {
-                    const unsigned long long sig = na_sig(p, x.g);
-                    if (sig != last_sig) {
-                        // the softmax of this stream rebuilds the channels after
-                        // it has read every earlier S of the stream
-                        ok = ptx::mbar_wait_or_abort(&bars->chan_ready[tt], rb & 1, p.err, abort);
-                        ++rb;
-                        last_sig = sig;
-                        if (!ok) break;
-                    }
-                    nv = imax(1, x.g.nhc * x.g.nwc);
-                    vq = 0;
+                    // the softmax of this stream has written the box's query
+                    // channels (after reading every S of the previous box)
+                    ok = ptx::mbar_wait_or_abort(&bars->chan_ready[tt], ci & 1, p.err, abort);
+                    if (!ok) break;
+                    hq = wq = 0;
+                    nhq = x.g.nhc;
+                    nwq = x.g.nwc;
                 }
                 ptx::tc_fence_after();
                 // Q K^T of key tile j; q_free right behind the box's last one
@@ -541,8 +513,6 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         const float cl = p.c_log2;
         constexpr int NG = kBN / 16;             // 16-key groups per key tile
         const int dt = row / (p.bh * p.bw), dh = (row / p.bw) % p.bh, dw = row % p.bw;
-        uint16_t *tab_h = reinterpret_cast<uint16_t *>(smem + C::OFF_TAB) + t * 2 * C::TAB;
-        uint16_t *tab_w = tab_h + C::TAB;
 
         // waits for P V (gg) of this tile (and every earlier one: one thread's
         // MMAs complete in issue order).  Valid once P V (gg - 2) is known
@@ -557,75 +527,33 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 
         bool ok = true;
         int G = 0;                               // key tiles of the stream's earlier boxes
-        unsigned long long last_sig = ~0ull;
-        int rbs = 0;                             // channel rebuilds done by this warpgroup
-        // The key penalty channels of box gx, rebuilt unless they are the ones
-        // in place.  Every Q K^T of the tile so far must have completed (this
-        // warpgroup has read all their scores); the issuer waits for
-        // chan_ready before the next one.  For key (h, w) of the sub-box of h
-        // chunk hc and w chunk wc, channel c < bh holds -penalty if h lies
-        // outside the h window of box row offset c, channel bh + c' likewise
-        // for w: tabulated per union row / column first, then each channel row
-        // is the OR of two entries.
-        auto ensure_channels = [&](const NaTile &gx) -> bool {
-            const unsigned long long sig = na_sig(p, gx);
-            if (sig == last_sig) return true;
-            last_sig = sig;
-            // every thread of the warpgroup is done reading the previous tables
-            if (rbs > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_free[t],
-                                                                             (rbs - 1) & 1, p.err, abort))) {
-                return false;
-            }
-            for (int i = row; i < 2 * C::TAB; i += 128) {
-                const int axis = i / C::TAB, e = i % C::TAB;
-                uint32_t m = 0u;
-                if (axis == 0 && e < gx.nhc * KH) {
-                    const int kh = gx.u0h + e;
-                    for (int c = 0; c < p.bh; ++c) {
-                        const int sh = na_window_start(imin(gx.h0 + c, p.Hg - 1), p.Hg, p.kh);
-                        if (unsigned(kh - sh) >= unsigned(p.eh)) m |= 1u << c;
-                    }
-                } else if (axis == 1 && e < gx.nwc * kKW) {
-                    const int kw = gx.u0w + e;
-                    for (int c = 0; c < p.bw; ++c) {
-                        const int sw = na_window_start(imin(gx.w0 + c, p.W - 1), p.W, p.kw);
-                        if (unsigned(kw - sw) >= unsigned(p.ew)) m |= 1u << (p.bh + c);
-                    }
-                }
-                (axis == 0 ? tab_h : tab_w)[e] = uint16_t(m);
-            }
-            ptx::mbar_arrive(&bars->tab_done[t]);
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->tab_done[t], rbs & 1, p.err, abort))) {
-                return false;
-            }
-            const typename H16<F16>::T negh = H16<F16>::from(-p.penalty);
-            const uint32_t neg = uint32_t(*reinterpret_cast<const uint16_t *>(&negh));
-            const int nvt = gx.nhc * gx.nwc;
-            for (int i = row; i < nvt * kBN * 2; i += 128) {
-                const int half = i & 1, r = (i >> 1) % kBN, v = (i >> 1) / kBN;
-                // key r of sub-box v: union h row (v / nwc) KH + (r / 16) % KH,
-                // w column (v % nwc) 16 + r % 16 (the same in each of its KT frames)
-                const int hc = v / gx.nwc, wc = v - hc * gx.nwc;
-                const uint32_t m = uint32_t(tab_h[hc * KH + (r / kKW) % KH]) |
-                                   uint32_t(tab_w[wc * kKW + r % kKW]);
-                const uint32_t bits = (m >> (half * 8)) & 0xffu;
-                uint32_t w[4];
+        // This row's query channels for box gx: one-hot at the offsets of
+        // its h and w windows from the union origin (zero for a row outside
+        // the box or the grid).  Every Q K^T of the previous box must have
+        // completed (this warpgroup has read all their scores); the issuer
+        // waits for chan_ready before the box's first one.
+        auto write_qx = [&](const NaTile &gx) {
+            const int qh = gx.h0 + dh, qw = gx.w0 + dw;
+            const bool in = row < rows && gx.t0 + dt < p.T && qh < p.Hg && qw < p.W;
+            const int ch0 = in ? na_window_start(qh, p.Hg, p.kh) - gx.u0h : -1;
+            const int ch1 = in ? p.bh + na_window_start(qw, p.W, p.kw) - gx.u0w : -1;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    w[cc] = (((bits >> (2 * cc)) & 1u) ? neg : 0u) |
-                            (((bits >> (2 * cc + 1)) & 1u) ? (neg << 16) : 0u);
-                *reinterpret_cast<uint4 *>(smem + C::kxv_off(t, v) + ptx::sw32_offset(r, half)) =
+            for (int half = 0; half < 2; ++half) {
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = half * 8 + e;
+                    if (c == ch0 || c == ch1) w[e >> 1] |= uint32_t(H16<F16>::kOne) << ((e & 1) * 16);
+                }
+                *reinterpret_cast<uint4 *>(smem + C::qx_off(t) + ptx::sw32_offset(row, half)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bars->chan_ready[t]);
-            ptx::mbar_arrive(&bars->tab_free[t]);
-            ++rbs;
-            return true;
         };
         int b = 2 * blockIdx.x + t;              // the stream's boxes: b, b + 2 grid, ...
         if constexpr (PEN) {
-            if (b < p.n_boxes && !ensure_channels(na_box(p, b, KT, KH).g)) ok = false;
+            if (b < p.n_boxes) write_qx(na_box(p, b, KT, KH).g);
         }
         while (ok && b < p.n_boxes) {
             const NaBox x = na_box(p, b, KT, KH);
@@ -799,16 +727,13 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             }
             if (!ok) break;
 
-            // ---- the next box's channels before this box's outputs: every
-            //      Q K^T of the stream has completed (its last scores are
-            //      read), the rebuild overlaps the last P V, and the issuer can
-            //      start the next box's Q K^T while the outputs are written
+            // ---- the next box's query channels before this box's outputs:
+            //      every Q K^T of the stream has completed (its last scores
+            //      are read), so the issuer can start the next box's Q K^T
+            //      while the outputs are written
             const int nb = b + 2 * gridDim.x;
             if constexpr (PEN) {
-                if (nb < p.n_boxes && !ensure_channels(na_box(p, nb, KT, KH).g)) {
-                    ok = false;
-                    break;
-                }
+                if (nb < p.n_boxes) write_qx(na_box(p, nb, KT, KH).g);
             }
 
             // ---- epilogue: O / l -> 16-bit -> global.  The issuer overwrites O
@@ -997,6 +922,8 @@ attn_status_t tc_na3d(const Ctx &c, attn_dtype_t dt, const void *q, const void *
     p.nbt = cdiv(T, p.bt);
     p.nbh = cdiv(Hg, p.bh);
     p.nbw = cdiv(W, p.bw);
+    p.nhv = cdiv(imin(p.bh + p.eh - 1, Hg), p.KH);   // the planner keeps nhv nwv <= 7
+    p.nwv = cdiv(imin(p.bw + p.ew - 1, W), kKW);
     const long long boxes = (long long)p.nbt * p.nbh * p.nbw * B * H;
     if (boxes > 0x7fffffffLL - 4096) return ATTN_ERR_UNSUPPORTED;   // box indices + 2 grid fit int
     p.n_boxes = int(boxes);

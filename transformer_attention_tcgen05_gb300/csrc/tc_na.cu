@@ -6,7 +6,8 @@
 //
 // Each CTA (one per SM) runs two independent query-tile streams: stream t
 // of CTA c takes the 3D query boxes (<= 128 queries each, w fastest, then h,
-// t, batch x head) 2c + t, 2c + t + 2 grid, ..., so the CTAs in flight hold
+// t, batch x head) 2c + t, 2c + t + 2 grid, ... (the last, partial round
+// spread one box per CTA), so the CTAs in flight hold
 // neighbouring boxes of one head (their key windows overlap in L2), and the
 // set-up that a CTA per box paid every time (barriers, tensor memory, the
 // query-offset channels, the first copies and the first Q K^T) is paid once
@@ -220,6 +221,18 @@ __device__ __forceinline__ NaBox na_box(const NaParams &p, int b, int KT, int KH
     return x;
 }
 
+// Box k of stream t of CTA c (-1 past the stream's last): the full rounds of
+// 2 grid boxes go out in order (stream t of CTA c takes box 2c + t of each),
+// and the boxes of the last, partial round one per CTA first (stream 0 of
+// CTAs 0, 1, ..., then stream 1), so no CTA gets two boxes more than another
+// and a CTA's extra box runs while its other stream is idle.
+__device__ __forceinline__ int na_stream_box(const NaParams &p, int t, int k) {
+    const int S = 2 * int(gridDim.x), K = p.n_boxes / S;
+    if (k < K) return k * S + 2 * int(blockIdx.x) + t;
+    const int i = t * int(gridDim.x) + int(blockIdx.x);
+    return (k == K && i < p.n_boxes - K * S) ? K * S + i : -1;
+}
+
 // Origin (t, h, w) of key sub-box j of a tile: w chunk fastest, then h, then t.
 __device__ __forceinline__ void na_key_box(const NaTile &g, int KT, int KH, int j, int &t, int &h,
                                            int &w) {
@@ -342,7 +355,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             int q_issued = 0;                 // query loads issued
             bool ok = true;
             int ci = 0;
-            for (int b = 2 * blockIdx.x + tt; ok && b < p.n_boxes; b += 2 * gridDim.x, ++ci) {
+            for (int b = na_stream_box(p, tt, 0); ok && b >= 0; b = na_stream_box(p, tt, ++ci)) {
                 const NaBox x = na_box(p, b, KT, KH);
                 // the queries of box ci overwrite those of box ci - 1 once every
                 // Q K^T that read them has completed.  q_free is one phase per
@@ -455,7 +468,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             if (p.stagger <= 0) send_go();
             if (tt != 0) ok = ptx::mbar_wait_or_abort(&bars->go, 0, p.err, abort);
             int ci = 0;
-            for (int b = 2 * blockIdx.x + tt; ok && b < p.n_boxes; b += 2 * gridDim.x, ++ci) {
+            for (int b = na_stream_box(p, tt, 0); ok && b >= 0; b = na_stream_box(p, tt, ++ci)) {
                 const NaBox x = na_box(p, b, KT, KH);
                 const int nt = x.g.ntiles;
                 ok = ptx::mbar_wait_or_abort(&bars->q_full[tt], ci & 1, p.err, abort);
@@ -551,11 +564,12 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bars->chan_ready[t]);
         };
-        int b = 2 * blockIdx.x + t;              // the stream's boxes: b, b + 2 grid, ...
+        int ci = 0;
+        int b = na_stream_box(p, t, 0);          // the stream's box ci
         if constexpr (PEN) {
-            if (b < p.n_boxes) write_qx(na_box(p, b, KT, KH).g);
+            if (b >= 0) write_qx(na_box(p, b, KT, KH).g);
         }
-        while (ok && b < p.n_boxes) {
+        while (ok && b >= 0) {
             const NaBox x = na_box(p, b, KT, KH);
             const int nt = x.g.ntiles;
             const NaTile &gt = x.g;
@@ -731,9 +745,9 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             //      every Q K^T of the stream has completed (its last scores
             //      are read), so the issuer can start the next box's Q K^T
             //      while the outputs are written
-            const int nb = b + 2 * gridDim.x;
+            const int nb = na_stream_box(p, t, ci + 1);
             if constexpr (PEN) {
-                if (nb < p.n_boxes) write_qx(na_box(p, nb, KT, KH).g);
+                if (nb >= 0) write_qx(na_box(p, nb, KT, KH).g);
             }
 
             // ---- epilogue: O / l -> 16-bit -> global.  The issuer overwrites O
@@ -766,6 +780,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             }
             G += nt;
             b = nb;
+            ++ci;
         }
     }
 

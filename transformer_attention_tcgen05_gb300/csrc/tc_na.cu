@@ -99,16 +99,16 @@ struct NaCfg {
     static constexpr int OFF_KXV = OFF_QX + QX_BYTES;
     static constexpr int OFF_K = (OFF_KXV + KXV_BYTES + 1023) / 1024 * 1024;   // 128-byte swizzle atoms
     static constexpr int NS_ALL = (BUDGET - OFF_K) / STAGE_BYTES;
-    // V gets the deeper ring: a V stage is refilled only once the P V that
-    // read it has completed, and the issuer runs that P V late (it waits for
-    // P), so the next V tile has less lead than the next K tile, whose stage
-    // is freed by a Q K^T issued two key tiles ahead.  Measured on the large
-    // workload (with rings shared by both query tiles): K 2 / V 4 stages
-    // 944.7 us, K 3 / V 3 946.8, K 3 / V 2 (before the query channels were
-    // shared) 966.0, K 2 / V 3 953.1.
+    // V gets the deeper ring: the K tile of step g + 2 and the V tile of
+    // step g are read by the same issuer step, so with K 2 / V 4 stages one
+    // completion (Q K^T (g)) frees both stages that tile g + 2 refills.
+    // Measured on the large workload (with rings shared by both query tiles
+    // and separate stage releases): K 2 / V 4 stages 944.7 us, K 3 / V 3
+    // 946.8, K 3 / V 2 (before the query channels were shared) 966.0, K 2 /
+    // V 3 953.1.
     static constexpr int VS = NS_ALL - 2 > 4 ? 4 : NS_ALL - 2;
     static constexpr int KS = NS_ALL - VS > 4 ? 4 : NS_ALL - VS;
-    static_assert(KS >= 2 && VS >= 2, "at least two K and two V stages");
+    static_assert(KS >= 2 && VS >= 4, "Q K^T (g) must free the K and V stages of tile g + 2");
     static constexpr int OFF_V = OFF_K + KS * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_V + VS * STAGE_BYTES;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers + 1024 B alignment slack
@@ -158,8 +158,12 @@ struct NaParams {
 //   q_full [t] k: the queries of the stream's box k have landed
 //   q_free [t] k: every Q K^T of box k has completed
 //   k_full / v_full [t][s]: the stream's K / V tile s + KS n (s + VS n) has landed
-//   k_empty / v_empty [t][s]: the issuer is done with that stage
-//   s_full [2 t + b]: Q K^T of the stream's key tile g (g % 2 = b) has completed
+//   s_full [2 t + b]: Q K^T of the stream's key tile g (g % 2 = b) has completed;
+//                  this also frees the K and V stages of tile g + 2: the K
+//                  stage last held tile g + 2 - KS (KS >= 2), read by a Q K^T
+//                  issued no later than Q K^T (g), and the V stage tile
+//                  g + 2 - VS (VS >= 4), read by a P V issued before it (the
+//                  issuer puts P V (g - 2) before Q K^T (g))
 //   p_ready[2 t + b]: the softmax has written P(g) there (128 arrivals)
 //   o_done [2 t + b]: P V (g) has completed
 //   chan_ready[t] k: the query channels of the stream's box k are written
@@ -168,7 +172,7 @@ struct NaParams {
 template <int KS, int VS>
 struct NaBars {
     uint64_t q_full[kNQ], q_free[kNQ];
-    uint64_t k_full[kNQ][KS], k_empty[kNQ][KS], v_full[kNQ][VS], v_empty[kNQ][VS];
+    uint64_t k_full[kNQ][KS], v_full[kNQ][VS];
     uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
     uint64_t chan_ready[kNQ];
     uint64_t go;
@@ -270,14 +274,8 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         for (int t = 0; t < kNQ; ++t) {
             ptx::mbar_init(&bars->q_full[t], 1);
             ptx::mbar_init(&bars->q_free[t], 1);
-            for (int s = 0; s < C::KS; ++s) {
-                ptx::mbar_init(&bars->k_full[t][s], 1);
-                ptx::mbar_init(&bars->k_empty[t][s], 1);
-            }
-            for (int s = 0; s < C::VS; ++s) {
-                ptx::mbar_init(&bars->v_full[t][s], 1);
-                ptx::mbar_init(&bars->v_empty[t][s], 1);
-            }
+            for (int s = 0; s < C::KS; ++s) ptx::mbar_init(&bars->k_full[t][s], 1);
+            for (int s = 0; s < C::VS; ++s) ptx::mbar_init(&bars->v_full[t][s], 1);
         }
         for (int b = 0; b < 2 * kNQ; ++b) {
             ptx::mbar_init(&bars->s_full[b], 1);
@@ -373,24 +371,20 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                     const int g = G + j;
                     int kt_, kh_, kw_;
                     na_key_box(x.g, KT, KH, j, kt_, kh_, kw_);
-                    // a stage phase needs the fill issued here, so the empty
-                    // barrier is never two phases ahead of these waits
-                    const int sk = g % C::KS;
-                    if (g >= C::KS &&
-                        !ptx::mbar_wait_or_abort(&bars->k_empty[tt][sk], ((g / C::KS) - 1) & 1, p.err, abort)) {
+                    // both stages of tile g are free once Q K^T (g - 2) has
+                    // completed.  Q K^T (g) needs the copies issued here, so
+                    // s_full is never two phases ahead of this wait.
+                    if (g >= 2 && !ptx::mbar_wait_or_abort(&bars->s_full[2 * tt + (g & 1)], ((g - 2) >> 1) & 1,
+                                                           p.err, abort)) {
                         ok = false;
                         break;
                     }
+                    const int sk = g % C::KS;
                     ptx::mbar_arrive_expect_tx(&bars->k_full[tt][sk], C::KV_BYTES);
                     ptx::tma_load_5d(smem + C::k_off(sk, tt), &tk, 0, kw_, kh_, kt_, x.bhd, &bars->k_full[tt][sk],
                                      pol_kv);
                     k_issued = g + 1;
                     const int sv = g % C::VS;
-                    if (g >= C::VS &&
-                        !ptx::mbar_wait_or_abort(&bars->v_empty[tt][sv], ((g / C::VS) - 1) & 1, p.err, abort)) {
-                        ok = false;
-                        break;
-                    }
                     ptx::mbar_arrive_expect_tx(&bars->v_full[tt][sv], C::KV_BYTES);
                     ptx::tma_load_5d(smem + C::v_off(sv, tt), &tv, 0, kw_, kh_, kt_, x.bhd, &bars->v_full[tt][sv],
                                      pol_kv);
@@ -491,7 +485,6 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                     ptx::tc_fence_after();
                     issue_qk(g);
                     if (j == nt - 1) ptx::tc_commit(&bars->q_free[tt]);
-                    ptx::tc_commit(&bars->k_empty[tt][g % C::KS]);
                 };
                 for (int j = 0; ok && j < 2 && j < nt; ++j) next_qk(j);
                 for (int j = 0; ok && j < nt; ++j) {
@@ -505,7 +498,6 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                     // then Q K^T (j + 2) into the buffer P(j) came from
                     if (j + 2 < nt) next_qk(j + 2);
                     if (!ok) break;
-                    ptx::tc_commit(&bars->v_empty[tt][g % C::VS]);
                     if (g + 1 >= p.stagger) send_go();
                 }
                 G += nt;

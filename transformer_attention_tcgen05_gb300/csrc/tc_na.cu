@@ -693,18 +693,22 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                         if ((gmask >> gq) & 1u) tmax = fmaxf(tmax, gmx);
                     }
                     const float mt = tmax * cl;  // cl > 0: max commutes with the scaling
-                    // ---- the previous P V must be done before O is rescaled
-                    const bool want = j == 0 || mt > m + 8.f;
-                    const bool any_want = __any_sync(0xffffffffu, want);
-                    if (j > 0 && any_want && !wait_pv(gg - 1)) {
+                    // ---- rows whose max moves: a row whose max grows by more
+                    //      than 8, or that sees its window for the first time (m
+                    //      = -inf, as every row on the box's first key tile).  Only
+                    //      the first kind holds anything to rescale (a row at m =
+                    //      -inf has had P = 0 so far: O and l are 0), and only
+                    //      then must the previous P V be done first.
+                    const bool want = mt > m + 8.f;
+                    const bool resc = want && m != -INFINITY;
+                    const bool any_resc = __any_sync(0xffffffffu, resc);
+                    if (any_resc && !wait_pv(gg - 1)) {
                         ok = false;
                         break;
                     }
-                    if (j == 0) {
-                        m = mt;
-                    } else if (any_want) {
-                        // rows that move m scale their O row; the others multiply by 1
-                        const float f = want ? ptx::ex2(m - mt) : 1.f;   // m == -inf -> 0
+                    if (any_resc) {
+                        // rows that move a finite m scale their O row; the others multiply by 1
+                        const float f = resc ? ptx::ex2(m - mt) : 1.f;
 #pragma unroll
                         for (int c = 0; c < kD / 32; ++c) {
                             uint32_t ov[32];
@@ -720,11 +724,9 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                             }
                             ptx::tmem_st32(o_addr + c * 32, ov);
                         }
-                        if (want) {
-                            l *= f;
-                            m = mt;
-                        }
+                        l *= f;
                     }
+                    if (want) m = mt;
                     l += emit_p((m == -INFINITY) ? 0.f : -m, gmask);
                 }
                 ptx::tmem_wait_st();

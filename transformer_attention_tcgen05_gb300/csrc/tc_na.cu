@@ -155,16 +155,24 @@ struct NaParams {
 };
 
 // Barrier block at OFF_BAR.  Phases (k counts from 0) of stream t's barriers:
-//   q_full [t] k: the queries of the stream's box k have landed
+//   q_full [t] k: the queries and the first two K tiles of the stream's box k
+//                  have landed
 //   q_free [t] k: every Q K^T of box k has completed
-//   k_full / v_full [t][s]: the stream's K / V tile s + KS n (s + VS n) has landed
 //   s_full [2 t + b]: Q K^T of the stream's key tile g (g % 2 = b) has completed;
 //                  this also frees the K and V stages of tile g + 2: the K
 //                  stage last held tile g + 2 - KS (KS >= 2), read by a Q K^T
 //                  issued no later than Q K^T (g), and the V stage tile
 //                  g + 2 - VS (VS >= 4), read by a P V issued before it (the
 //                  issuer puts P V (g - 2) before Q K^T (g))
-//   p_ready[2 t + b]: the softmax has written P(g) there (128 arrivals)
+//   ready [t][g % 4]: the issuer's key-tile step g may run: the softmax has
+//                  written P(g) (128 arrivals), V(g) has landed and K(g + 2)
+//                  has landed (one loader arrival with its bytes each; a plain
+//                  one where tile g + 2 is not in the same box, as its K
+//                  counts on its own box's q_full).  Every arrival of
+//                  step g comes after step g - 4 has run (P(g) and the copies
+//                  follow Q K^T (g - 2) or (g), issued at step g - 4 or later),
+//                  and the issuer waits for step g before it issues the
+//                  Q K^T (g + 2) that step g + 4 needs
 //   o_done [2 t + b]: P V (g) has completed
 //   chan_ready[t] k: the query channels of the stream's box k are written
 //                  (128 arrivals)
@@ -172,8 +180,8 @@ struct NaParams {
 template <int KS, int VS>
 struct NaBars {
     uint64_t q_full[kNQ], q_free[kNQ];
-    uint64_t k_full[kNQ][KS], v_full[kNQ][VS];
-    uint64_t s_full[2 * kNQ], p_ready[2 * kNQ], o_done[2 * kNQ];
+    uint64_t ready[kNQ][4];
+    uint64_t s_full[2 * kNQ], o_done[2 * kNQ];
     uint64_t chan_ready[kNQ];
     uint64_t go;
     uint64_t drain;
@@ -274,12 +282,10 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         for (int t = 0; t < kNQ; ++t) {
             ptx::mbar_init(&bars->q_full[t], 1);
             ptx::mbar_init(&bars->q_free[t], 1);
-            for (int s = 0; s < C::KS; ++s) ptx::mbar_init(&bars->k_full[t][s], 1);
-            for (int s = 0; s < C::VS; ++s) ptx::mbar_init(&bars->v_full[t][s], 1);
+            for (int s = 0; s < 4; ++s) ptx::mbar_init(&bars->ready[t][s], 128 + 2);
         }
         for (int b = 0; b < 2 * kNQ; ++b) {
             ptx::mbar_init(&bars->s_full[b], 1);
-            ptx::mbar_init(&bars->p_ready[b], 128);
             ptx::mbar_init(&bars->o_done[b], 1);
         }
         for (int t = 0; t < kNQ; ++t) ptx::mbar_init(&bars->chan_ready[t], 128);
@@ -349,7 +355,6 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
             const uint64_t pol_kv = ptx::l2_policy_evict_last();
             const uint64_t pol_q = ptx::l2_policy_evict_first();
             int G = 0;                        // key tiles of earlier boxes
-            int k_issued = 0, v_issued = 0;   // key tiles whose K / V copies were issued
             int q_issued = 0;                 // query loads issued
             bool ok = true;
             int ci = 0;
@@ -363,6 +368,11 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                     ok = false;
                     break;
                 }
+                // the box's first two K tiles count on its queries' barrier
+                // (registered before its arrival), so that no step waits for
+                // a copy of a later box
+                const int nt = x.g.ntiles;
+                ptx::mbar_expect_tx(&bars->q_full[tt], imin(nt, 2) * C::KV_BYTES);
                 ptx::mbar_arrive_expect_tx(&bars->q_full[tt], rows * 128);
                 ptx::tma_load_5d(smem + C::OFF_Q + tt * C::PANEL, &tq, 0, x.g.w0, x.g.h0, x.g.t0, x.bhd,
                                  &bars->q_full[tt], pol_q);
@@ -379,27 +389,30 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                         ok = false;
                         break;
                     }
-                    const int sk = g % C::KS;
-                    ptx::mbar_arrive_expect_tx(&bars->k_full[tt][sk], C::KV_BYTES);
-                    ptx::tma_load_5d(smem + C::k_off(sk, tt), &tk, 0, kw_, kh_, kt_, x.bhd, &bars->k_full[tt][sk],
-                                     pol_kv);
-                    k_issued = g + 1;
-                    const int sv = g % C::VS;
-                    ptx::mbar_arrive_expect_tx(&bars->v_full[tt][sv], C::KV_BYTES);
-                    ptx::tma_load_5d(smem + C::v_off(sv, tt), &tv, 0, kw_, kh_, kt_, x.bhd, &bars->v_full[tt][sv],
-                                     pol_kv);
-                    v_issued = g + 1;
+                    // K(g) serves step g - 2 (the box's first two: its queries'
+                    // barrier), V(g) step g
+                    uint64_t *bk = j >= 2 ? &bars->ready[tt][(g - 2) & 3] : &bars->q_full[tt];
+                    if (j >= 2) ptx::mbar_arrive_expect_tx(bk, C::KV_BYTES);
+                    ptx::tma_load_5d(smem + C::k_off(g % C::KS, tt), &tk, 0, kw_, kh_, kt_, x.bhd, bk, pol_kv);
+                    uint64_t *bv = &bars->ready[tt][g & 3];
+                    ptx::mbar_arrive_expect_tx(bv, C::KV_BYTES);
+                    ptx::tma_load_5d(smem + C::v_off(g % C::VS, tt), &tv, 0, kw_, kh_, kt_, x.bhd, bv, pol_kv);
                 }
-                G += x.g.ntiles;
+                // the box's last two steps have no K tile two ahead in the box
+                if (ok)
+                    for (int j = imax(0, nt - 2); j < nt; ++j) ptx::mbar_arrive(&bars->ready[tt][(G + j) & 3]);
+                G += nt;
             }
             // after a timeout elsewhere: let the copies this thread issued land
-            // (bounded) before the CTA's shared memory is released
+            // before the CTA's shared memory is released.  Their barriers also
+            // wait for softmax arrivals that may never come, so wait for the
+            // queries' barrier (bounded) and then a fixed 50 us, far above the
+            // latency of a copy.
             if (*abort) {
                 if (q_issued > 0) ptx::mbar_wait(&bars->q_full[tt], (q_issued - 1) & 1, nullptr);
-                for (int g = imax(0, k_issued - C::KS); g < k_issued; ++g)
-                    ptx::mbar_wait(&bars->k_full[tt][g % C::KS], (g / C::KS) & 1, nullptr);
-                for (int g = imax(0, v_issued - C::VS); g < v_issued; ++g)
-                    ptx::mbar_wait(&bars->v_full[tt][g % C::VS], (g / C::VS) & 1, nullptr);
+                const unsigned long long t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 50000ull) {
+                }
             }
         } else if ((warp == C::W_MMA || warp == C::W_MMA1) && lane == 0) {
             // ============================================= MMA issuers: one
@@ -480,18 +493,16 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 // Q K^T of key tile j; q_free right behind the box's last one
                 auto next_qk = [&](int j) {
                     const int g = G + j;
-                    ok = ok && ptx::mbar_wait_or_abort(&bars->k_full[tt][g % C::KS], (g / C::KS) & 1, p.err, abort);
                     if (!ok) return;
-                    ptx::tc_fence_after();
                     issue_qk(g);
                     if (j == nt - 1) ptx::tc_commit(&bars->q_free[tt]);
                 };
                 for (int j = 0; ok && j < 2 && j < nt; ++j) next_qk(j);
                 for (int j = 0; ok && j < nt; ++j) {
                     const int g = G + j;
-                    // P V (j) once the softmax has written P(j) and V(j) has landed
-                    ok = ptx::mbar_wait_or_abort(&bars->p_ready[2 * tt + (g & 1)], (g >> 1) & 1, p.err, abort) &&
-                         ptx::mbar_wait_or_abort(&bars->v_full[tt][g % C::VS], (g / C::VS) & 1, p.err, abort);
+                    // P V (j) once the softmax has written P(j) and V(j) has landed,
+                    // and K(j + 2) has landed for the Q K^T behind it
+                    ok = ptx::mbar_wait_or_abort(&bars->ready[tt][g & 3], (g >> 2) & 1, p.err, abort);
                     if (!ok) break;
                     ptx::tc_fence_after();
                     issue_pv(g, j == 0);
@@ -731,7 +742,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&bars->p_ready[2 * t + (gg & 1)]);
+                ptx::mbar_arrive(&bars->ready[t][gg & 3]);
             }
             if (!ok) break;
 

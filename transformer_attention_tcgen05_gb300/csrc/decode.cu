@@ -123,6 +123,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CU
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int unit = b * p.Hkv + kvh;
 
+    // launched as a programmatic dependent of the previous kernel on the
+    // stream: nothing global is read or written before that kernel has
+    // completed (the cache, the lengths or q may be its outputs); the next
+    // kernel may start launching at once
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+
     // q of the G heads of this KV head: its loads go out first, before any
     // cache copy of the grid floods the memory system (issued after the
     // barrier set-up, they took ~3.6 us and held up the consumers while the
@@ -573,7 +580,22 @@ attn_status_t launch(const Ctx &c, const CUtensorMap &tk, const CUtensorMap &tv,
     auto kern = decode_kernel<D, GP, false, F16>;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, c.device, &done_mask))
         return ATTN_ERR_RESOURCE;
-    kern<<<dim3(p.splits, p.Hkv, B), C::NT, C::SMEM, c.stream>>>(tk, tv, p);
+    // programmatic dependent launch: the grid may start (and set up) while
+    // the previous kernel finishes; the kernel waits for it before any read
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.splits, p.Hkv, B);
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
     return launch_status(kFamDecode);
 }
 
@@ -639,8 +661,12 @@ attn_status_t launch_cluster(const Ctx &c, const CUtensorMap &tk, const CUtensor
     if (!ensure_smem_attr(reinterpret_cast<const void *>(kern), DecCfg<D, GP>::SMEM, c.device,
                           &done_mask))
         return ATTN_ERR_RESOURCE;
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = cluster_config<D, GP>(c, p.splits, p.Hkv, B, &attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = cluster_config<D, GP>(c, p.splits, p.Hkv, B, attr);
+    // programmatic dependent launch, as for the workspace-merge kernel
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, tk, tv, p) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_CUDA;

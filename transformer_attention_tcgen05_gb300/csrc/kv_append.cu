@@ -15,6 +15,7 @@
 // all KV heads with 16-byte vector stores, and only then bumps the length, so
 // no other CTA ever reads a length this launch changed.
 #include "common.cuh"
+#include "ptx.cuh"
 #include "kernels.h"
 
 namespace attn {
@@ -25,6 +26,9 @@ __global__ void __launch_bounds__(128) kv_append_kernel(T *kc, T *vc, const T *k
                                                         int32_t *seq_len, int Hkv, int Lmax,
                                                         int D, int advance, int ring,
                                                         unsigned *err) {
+    // a decode launched behind this kernel may start setting up at once (it
+    // waits for this grid to complete before it reads anything)
+    ptx::griddep_launch_dependents();
     const int b = blockIdx.x;
     const int pos = seq_len[b];
     // linear cache: full or corrupt length; ring: a count that cannot advance

@@ -40,6 +40,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait returns once the grids this
+// one depends on have completed and their writes are visible (at once when
+// the launch carries no such dependency); griddep_launch_dependents lets the
+// grids that depend on this one start launching (their own griddep_wait still
+// waits for this grid to complete).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Raise the transaction count of the current phase without arriving.
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)

@@ -275,6 +275,10 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
     const int KT = KSH > 0 ? KSH / 10 : p.KT;
     const int KH = KSH > 0 ? KSH % 10 : p.KH;
     const int rows = p.bt * p.bh * p.bw;          // queries per box (<= 128)
+    // a kernel launched behind this one as a programmatic dependent (decode)
+    // may take the SMs this grid's CTAs leave; it waits for this grid to
+    // complete before it reads anything
+    ptx::griddep_launch_dependents();
 
     // ---- set-up: barriers (one thread of the last warp) beside the query
     //      channels, which are the same for every box

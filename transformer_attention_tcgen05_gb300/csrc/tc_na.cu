@@ -177,7 +177,6 @@ struct NaParams {
 //   chan_ready[t] k: the query channels of the stream's box k are written
 //                  (128 arrivals)
 //   go: stream 1 may start (one phase, one arrival from issuer 0)
-template <int KS, int VS>
 struct NaBars {
     uint64_t q_full[kNQ], q_free[kNQ];
     uint64_t ready[kNQ][4];
@@ -265,7 +264,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
              const __grid_constant__ CUtensorMap tv, const NaParams p) {
     constexpr bool PEN = !F16;
     using C = NaCfg<PEN>;
-    using BarsT = NaBars<C::KS, C::VS>;
+    using BarsT = NaBars;
     static_assert(sizeof(BarsT) <= 512, "barrier block must fit its reserved bytes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (ptx::smem_addr(smem_raw) & 1023)) & 1023);
@@ -280,8 +279,9 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
     // complete before it reads anything
     ptx::griddep_launch_dependents();
 
-    // ---- set-up: barriers (one thread of the last warp) beside the query
-    //      channels, which are the same for every box
+    // ---- set-up: barriers (one thread of the last warp) beside the zero
+    //      query rows past the box and the key penalty tiles, which are the
+    //      same for every box (the other threads)
     if (threadIdx.x == C::NT - 32) {
         for (int t = 0; t < kNQ; ++t) {
             ptx::mbar_init(&bars->q_full[t], 1);
@@ -782,9 +782,12 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         wp[e] = H16<F16>::pack(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+                    // streaming stores: the outputs are not read again here, and
+                    // evicting them early keeps the key tiles in L2 and leaves
+                    // less to write back after the kernel
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = w4[e];
+                    for (int e = 0; e < 4; ++e) __stcs(dst + e, w4[e]);
                 }
             }
             G += nt;

@@ -18,6 +18,7 @@
 // instead of once per head.  Frequencies come from the host in double
 // precision; the angle is one fp32 product, reduced by sincosf.
 #include "common.cuh"
+#include "ptx.cuh"
 #include "kernels.h"
 
 namespace attn {
@@ -74,6 +75,9 @@ template <> struct Vec8<float> {
 // grid: (ceil(N * D/8 / 256), ceil(BH / heads_per_cta)); thread -> (token, 8-channel group)
 template <typename T>
 __global__ void __launch_bounds__(256) rope_kernel(const RopeParams p, int heads_per_cta) {
+    // the attention kernel behind this pass may start setting up at once (it
+    // waits for this grid to complete before it reads the rotated copies)
+    ptx::griddep_launch_dependents();
     const int groups = p.D / 8;
     const long long e = blockIdx.x * 256ll + threadIdx.x;
     if (e >= (long long)p.N * groups) return;

@@ -217,6 +217,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // launched as a programmatic dependent of the previous kernel (the RoPE
+    // pass writes this kernel's Q and K): the set-up above touches nothing
+    // global, the copies below wait for that kernel to complete; a decode
+    // launched behind this kernel may start launching at once
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 
     if (warp >= C::NSOFT) {
         ptx::regs_decrease<C::REGS_OTHER>();
@@ -725,7 +731,22 @@ attn_status_t launch_tc(const Ctx &c, const CUtensorMap &tq, const CUtensorMap &
         regs = fa.numRegs;
     }
     if (regs != C::REGS_LAUNCH) return ATTN_ERR_UNSUPPORTED;
-    kern<<<grid, C::NT, C::SMEM, c.stream>>>(tq, tk, tv, p);
+    // programmatic dependent launch: the CTAs set up while the previous
+    // kernel finishes and wait for it before their first copy
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+    }
     return launch_status(kFamTcFlash);
 }
 

@@ -125,7 +125,8 @@ struct NaCfg {
     static constexpr int W_LOAD1 = NSOFT + 2; // Q, K and V copies of stream 1
     static constexpr int W_MMA1 = NSOFT + 3;  // issuer of stream 1, barrier set-up
     static constexpr int NT = (NSOFT + 4) * 32;
-    static constexpr int NBUILD = NT - 32;    // threads that build the query channels
+    // threads that zero the query rows past the box and build the key penalty tiles
+    static constexpr int NBUILD = NT - 32;
     // register split: launch 168 x 384 = 64512 = 2 x 128 x 216 + 128 x 72
     static constexpr int REGS_LAUNCH = 168;
     static constexpr int REGS_SOFTMAX = 216;
@@ -534,8 +535,8 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
         constexpr int NG = kBN / 16;             // 16-key groups per key tile
         const int dt = row / (p.bh * p.bw), dh = (row / p.bw) % p.bh, dw = row % p.bw;
 
-        // waits for P V (gg) of this tile (and every earlier one: one thread's
-        // MMAs complete in issue order).  Valid once P V (gg - 2) is known
+        // waits for P V (gg) of this stream (and every earlier one: one
+        // thread's MMAs complete in issue order).  Valid once P V (gg - 2) is known
         // complete: it is while the softmax holds S(gg), issued after it.
         auto wait_pv = [&](int gg) -> bool {
             if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&bars->o_done[2 * t + (gg & 1)],

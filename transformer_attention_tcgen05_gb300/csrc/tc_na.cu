@@ -594,6 +594,21 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 
             float m = -INFINITY, l = 0.f;
             int tc = 0, hc = 0, wc = 0;          // key sub-box counters (w fastest, then h, then t)
+            // t window per 16-key group of the current t chunk (group gq holds
+            // frame kt0 + gq / KH): bit gq of gmask clear -> P = 0 there; wlive:
+            // the groups any row of the warp sees.  Both change with tc only.
+            auto group_mask = [&](int tcc) -> uint32_t {
+                uint32_t gmv = 0u;
+                if (qvalid) {
+                    const int kt0 = gt.u0t + tcc * KT;
+#pragma unroll
+                    for (int gq = 0; gq < NG; ++gq)
+                        if (unsigned(kt0 + gq / KH - wst) < unsigned(p.et)) gmv |= 1u << gq;
+                }
+                return gmv;
+            };
+            uint32_t gmask = group_mask(0);
+            uint32_t wlive = __reduce_or_sync(0xffffffffu, gmask);
             for (int j = 0; j < nt; ++j) {
                 const int gg = G + j;
                 const uint32_t s_addr = lane_base + C::tm_s(t, gg & 1);
@@ -604,22 +619,15 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 }
                 ptx::tc_fence_after();
 
-                // ---- t window per 16-key group (group gq holds frame kt0 + gq / KH):
-                //      bit gq of gmask clear -> P = 0 there
-                const int kt0 = gt.u0t + tc * KT;
                 const int kh0 = gt.u0h + hc * KH, kw0 = gt.u0w + wc * kKW;
+                bool new_tc = false;
                 if (++wc == gt.nwc) {
                     wc = 0;
                     if (++hc == gt.nhc) {
                         hc = 0;
                         ++tc;
+                        new_tc = true;
                     }
-                }
-                uint32_t gmask = 0u;
-                if (qvalid) {
-#pragma unroll
-                    for (int gq = 0; gq < NG; ++gq)
-                        if (unsigned(kt0 + gq / KH - wst) < unsigned(p.et)) gmask |= 1u << gq;
                 }
 
                 float sv[kBN];
@@ -648,7 +656,7 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
 
                 // 32-key chunks that no row of this warp may see: P = 0 without
                 // exponentials
-                const uint32_t wlive = __reduce_or_sync(0xffffffffu, gmask);
+                // (gmask and wlive of this key tile; the next t chunk's below)
 
                 // P = 2^(x - m) in 16-bit over S (groups outside gm: P = 0);
                 // returns the tile's row sum (fp32)
@@ -748,6 +756,10 @@ tc_na_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUt
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bars->ready[t][gg & 3]);
+                if (new_tc) {
+                    gmask = group_mask(tc);
+                    wlive = __reduce_or_sync(0xffffffffu, gmask);
+                }
             }
             if (!ok) break;
 

@@ -371,6 +371,8 @@ def ours(args, rank, world, dev_index):
         kt["na"].append(e[1].elapsed_time(e[2]))
         kt["decode"].append(e[2].elapsed_time(e[3]))
     kms = {k: statistics.mean(v) for k, v in kt.items()}
+    kmed = {k: statistics.median(v) for k, v in kt.items()}
+    kmin = {k: min(v) for k, v in kt.items()}
     assert ta.device_status() == 0
     gpu_out = {k: host64(step.output(k)) for k in ("joint", "na", "dec")}
     dec_proto = decode_protocol(step, ta)
@@ -404,12 +406,17 @@ def ours(args, rank, world, dev_index):
         return None
 
     tflops = job_throughput(STEP_FLOPS, world, ms)
+    # per kernel: the mean over the timed steps (the figures below), and
+    # their median and minimum
     comp = {
         "joint": {"ms": kms["joint"], "tflops": flops_joint() / (kms["joint"] * 1e-3) / 1e12},
         "na3d": {"ms": kms["na"], "tflops": flops_na() / (kms["na"] * 1e-3) / 1e12},
         "decode": {"ms": kms["decode"], "tflops": flops_dec() / (kms["decode"] * 1e-3) / 1e12,
                    "kv_gbs": bytes_dec() / (kms["decode"] * 1e-3) / 1e9},
     }
+    for k, kk in (("joint", "joint"), ("na3d", "na"), ("decode", "decode")):
+        comp[k]["ms_median"] = kmed[kk]
+        comp[k]["ms_min"] = kmin[kk]
     for k in ("joint", "na3d"):
         comp[k]["frac_of_bf16_peak"] = comp[k]["tflops"] / peaks["bf16"]
     comp["decode"]["frac_of_hbm"] = comp["decode"]["kv_gbs"] / peaks["hbm"]
